@@ -1,0 +1,279 @@
+"""Pins for the oracle's GEMM + epilogue against things other than itself (CPU only).
+
+* brute force on tiny inputs against exact rational arithmetic (fractions),
+  over every layout -- catches transposed operands, wrong strides, dropped or
+  mis-signed alpha/beta/bias terms;
+* closed forms: identity, all-ones, rank-1, alpha = 0, beta-only, K = 0;
+* GELU against the normal-CDF table and its symmetry identity;
+* the BLAS conventions (operands that must not be read are never read);
+* the error metric's behaviour, and that it flags planted mistakes.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from conftest import read_golden
+
+
+def _frac_ref(p):
+    """Exact rational evaluation of alpha*A*B + beta*C + bias from the logical values."""
+    a = oracle.decode(oracle.strided_codes(p.codes("A"), p.M, p.K, p.a_stride_m, p.a_stride_k), p.ab_dtype)
+    b = oracle.decode(oracle.strided_codes(p.codes("B"), p.K, p.N, p.b_stride_k, p.b_stride_n), p.ab_dtype)
+    c = oracle.decode(oracle.strided_codes(p.codes("C"), p.M, p.N, p.ldc, 1), p.c_dtype)
+    al, be = Fraction(float(np.float32(p.alpha))), Fraction(float(np.float32(p.beta)))
+    out = [[None] * p.N for _ in range(p.M)]
+    for i in range(p.M):
+        for j in range(p.N):
+            s = sum((Fraction(float(a[i, k])) * Fraction(float(b[k, j])) for k in range(p.K)), Fraction(0))
+            z = al * s
+            if p.beta != 0:
+                z += be * Fraction(float(c[i, j]))
+            if p.epilogue != wl.EPI_NONE:
+                z += Fraction(float(p.bias[j]))
+            out[i][j] = z
+    return out
+
+
+@pytest.mark.parametrize("layout", ["NN", "NT", "TN", "TT"])
+@pytest.mark.parametrize("dtype", [wl.F32, wl.F16, wl.BF16, wl.E4M3])
+def test_brute_force_tiny_exact(layout, dtype):
+    """All M, N, K in 1..4 with small-integer data: float64 result is exact."""
+    seed = 100
+    for M, N, K in itertools.product(range(1, 5), repeat=3):
+        seed += 7
+        p = wl.random_problem(seed, M, N, K, dtype, wl.F32, layout=layout, alpha=1.5, beta=-0.5,
+                              epilogue=wl.EPI_BIAS, integer=True, lda_pad=1, ldb_pad=2, ldc_pad=3)
+        y, D = oracle.gemm_reference(**p.oracle_args())
+        exact = _frac_ref(p)
+        for i in range(M):
+            for j in range(N):
+                assert Fraction(float(y[i, j])) == exact[i][j], (M, N, K, i, j)
+
+
+def test_brute_force_no_epilogue_alpha_only():
+    p = wl.random_problem(5, 3, 5, 7, wl.F16, wl.F16, layout="TN", alpha=-2.0, beta=0.0, integer=True)
+    y, _ = oracle.gemm_reference(**p.oracle_args())
+    exact = _frac_ref(p)
+    assert all(Fraction(float(y[i, j])) == exact[i][j] for i in range(3) for j in range(5))
+
+
+def _problem_from(a, b, c=None, *, alpha=1.0, beta=0.0, bias=None, epilogue=wl.EPI_NONE, layout="NN",
+                  ab=wl.F32, cd=wl.F32):
+    import torch
+    a = torch.as_tensor(a, dtype=torch.float32)
+    b = torch.as_tensor(b, dtype=torch.float32)
+    c = None if c is None else torch.as_tensor(c, dtype=torch.float32)
+    bias = None if bias is None else torch.as_tensor(bias, dtype=torch.float32)
+    M, K = a.shape
+    N = b.shape[1]
+    return wl.make_problem("closed", M, N, K, ab, cd, a, b, c, layout=layout, alpha=alpha, beta=beta,
+                           bias=bias, epilogue=epilogue)
+
+
+def test_identity_gives_alpha_b_plus_beta_c():
+    rng = np.random.default_rng(1)
+    n = 9
+    b = rng.integers(-8, 9, size=(n, 6)).astype(np.float32)
+    c = rng.integers(-8, 9, size=(n, 6)).astype(np.float32)
+    for layout in ["NN", "NT", "TN", "TT"]:
+        p = _problem_from(np.eye(n), b, c, alpha=2.0, beta=-3.0, layout=layout)
+        y, _ = oracle.gemm_reference(**p.oracle_args())
+        assert np.array_equal(y, 2.0 * b - 3.0 * c)
+
+
+def test_all_ones():
+    M, N, K = 5, 7, 13
+    c = np.arange(M * N, dtype=np.float32).reshape(M, N)
+    p = _problem_from(np.ones((M, K)), np.ones((K, N)), c, alpha=0.5, beta=2.0)
+    y, D = oracle.gemm_reference(**p.oracle_args())
+    assert np.array_equal(y, 0.5 * K + 2.0 * c)
+    assert np.array_equal(D, 0.5 * K + 2.0 * np.abs(c))
+
+
+def test_rank_one_outer_product():
+    u = np.array([1.0, -2.0, 3.0, 0.5], dtype=np.float32)
+    v = np.array([2.0, 0.25, -1.0], dtype=np.float32)
+    p = _problem_from(u[:, None], v[None, :], alpha=-1.5, layout="TT")
+    y, _ = oracle.gemm_reference(**p.oracle_args())
+    assert np.array_equal(y, -1.5 * np.outer(u, v))
+    # same outer product through a K>1 problem with zero columns beyond the first
+    A = np.zeros((4, 6), np.float32); A[:, 0] = u
+    B = np.zeros((6, 3), np.float32); B[0, :] = v
+    y2, _ = oracle.gemm_reference(**_problem_from(A, B, alpha=-1.5, layout="NT").oracle_args())
+    assert np.array_equal(y2, y)
+
+
+def test_alpha_zero_reads_neither_a_nor_b():
+    c = np.array([[1.0, -2.0], [4.0, 8.0]], dtype=np.float32)
+    p = _problem_from(np.full((2, 3), np.nan), np.full((3, 2), np.nan), c, alpha=0.0, beta=0.25)
+    y, D = oracle.gemm_reference(**p.oracle_args())
+    assert np.array_equal(y, 0.25 * c) and np.array_equal(D, 0.25 * np.abs(c))
+
+
+def test_beta_zero_reads_no_c():
+    p = _problem_from(np.ones((2, 2)), np.ones((2, 2)), np.full((2, 2), np.nan), alpha=1.0, beta=0.0)
+    y, _ = oracle.gemm_reference(**p.oracle_args())
+    assert np.array_equal(y, np.full((2, 2), 2.0))
+
+
+def test_beta_only_with_zero_operands():
+    c = np.array([[3.0, -1.0, 0.5]], dtype=np.float32)
+    p = _problem_from(np.zeros((1, 4)), np.zeros((4, 3)), c, alpha=1.0, beta=-2.0)
+    y, _ = oracle.gemm_reference(**p.oracle_args())
+    assert np.array_equal(y, -2.0 * c)
+
+
+def test_k_zero_is_epilogue_of_beta_c():
+    M, N = 3, 4
+    c = np.arange(12, dtype=np.float32).reshape(M, N) - 6
+    bias = np.array([0.5, -0.5, 1.0, 0.0], np.float32)
+    p = _problem_from(np.zeros((M, 0)), np.zeros((0, N)), c, alpha=1.0, beta=0.5, bias=bias,
+                      epilogue=wl.EPI_BIAS_GELU)
+    y, D = oracle.gemm_reference(**p.oracle_args())
+    z = 0.5 * c.astype(np.float64) + bias.astype(np.float64)
+    phi = np.array([[0.5 * (1 + math.erf(v / math.sqrt(2))) for v in row] for row in z])
+    assert np.allclose(y, z * phi, rtol=0, atol=1e-15)
+    assert np.array_equal(D, 0.5 * np.abs(c) + np.abs(bias))
+
+
+def test_zero_scale_output_is_exact_zero():
+    p = _problem_from(np.zeros((2, 0)), np.zeros((0, 2)), alpha=1.0, beta=0.0)
+    y, D = oracle.gemm_reference(**p.oracle_args())
+    assert np.array_equal(y, np.zeros((2, 2))) and np.array_equal(D, np.zeros((2, 2)))
+    assert oracle.max_normalized_error(np.zeros((2, 2)), y, D, 0) == 0.0
+    assert oracle.max_normalized_error(np.full((2, 2), 1e-30), y, D, 0) == math.inf
+
+
+def test_bias_epilogue_adds_per_column():
+    bias = np.array([1.0, -2.0, 0.25], np.float32)
+    p = _problem_from(np.ones((2, 1)), np.ones((1, 3)), bias=bias, epilogue=wl.EPI_BIAS)
+    y, _ = oracle.gemm_reference(**p.oracle_args())
+    assert np.array_equal(y, np.tile(1.0 + bias, (2, 1)))
+
+
+@pytest.mark.parametrize("row", read_golden("normal_cdf.txt"), ids=lambda r: r[0])
+def test_gelu_against_normal_cdf_table(row):
+    z, phi = float(row[0]), float(row[1])
+    assert abs(oracle.gelu(np.array([z]))[0] - z * phi) <= 1e-15 * max(1.0, abs(z))
+
+
+def test_gelu_identities():
+    z = np.linspace(-12, 12, 2401)
+    g = oracle.gelu(z)
+    # Phi(z) + Phi(-z) = 1  =>  GELU(z) - GELU(-z) = z
+    assert np.allclose(g - oracle.gelu(-z), z, rtol=0, atol=1e-14)
+    assert oracle.gelu(np.array([0.0]))[0] == 0.0
+    assert oracle.gelu(np.array([10.0]))[0] == 10.0 - 10.0 * 0.5 * math.erfc(10 / math.sqrt(2))
+    assert abs(oracle.gelu(np.array([-10.0]))[0]) < 1e-21
+
+
+def test_gelu_lipschitz_constant_is_max_slope():
+    z = np.linspace(-6, 6, 600001)
+    h = z[1] - z[0]
+    slope = np.abs(np.diff(oracle.gelu(z))) / h
+    assert abs(slope.max() - oracle.GELU_LIPSCHITZ) < 1e-6
+    assert abs(z[np.argmax(slope)] - math.sqrt(2)) < 1e-3
+
+
+def test_layouts_give_one_result():
+    """Every layout of one draw is the same logical product (and the same D)."""
+    outs = []
+    for layout in ["NN", "NT", "TN", "TT"]:
+        p = wl.random_problem(9, 37, 29, 41, wl.BF16, wl.F32, layout=layout, alpha=1.25, beta=0.0,
+                              lda_pad=3, ldb_pad=5)
+        outs.append(oracle.gemm_reference(**p.oracle_args()))
+    for y, D in outs[1:]:
+        assert np.allclose(y, outs[0][0], rtol=1e-13, atol=0) and np.allclose(D, outs[0][1], rtol=1e-13)
+
+
+def test_transpose_identity():
+    """(A B)^T = B^T A^T: swapping operands and strides gives the transposed result."""
+    p = wl.random_problem(11, 23, 31, 19, wl.F16, wl.F32, alpha=0.75)
+    y, D = oracle.gemm_reference(**p.oracle_args())
+    args = p.oracle_args()
+    yt, Dt = oracle.gemm_reference(
+        M=p.N, N=p.M, K=p.K, ab_dtype=p.ab_dtype,
+        A=args["B"], a_stride_m=p.b_stride_n, a_stride_k=p.b_stride_k,
+        B=args["A"], b_stride_k=p.a_stride_k, b_stride_n=p.a_stride_m,
+        C=np.zeros(p.N * p.M, np.int32), ldc=p.M, c_dtype=wl.F32, alpha=p.alpha, beta=0.0,
+        bias=None, epilogue=wl.EPI_NONE)
+    assert np.allclose(yt.T, y, rtol=1e-13, atol=0) and np.allclose(Dt.T, D, rtol=1e-13, atol=0)
+
+
+def test_row_sample_matches_full():
+    p = wl.fp16_alpha_beta(96, 80, 72)
+    y, D = oracle.gemm_reference(**p.oracle_args())
+    rows = [0, 5, 17, 95]
+    ys, Ds = oracle.gemm_reference(rows=rows, **p.oracle_args())
+    assert np.array_equal(ys, y[rows]) and np.array_equal(Ds, D[rows])
+
+
+def test_strided_view_never_reads_past_buffer():
+    with pytest.raises(IndexError):
+        oracle.strided_codes(np.zeros(10, np.int16), 3, 4, 4, 1)  # needs 12 elements
+    assert oracle.strided_codes(np.arange(12, dtype=np.int16), 3, 4, 4, 1).shape == (3, 4)
+
+
+# --- the error metric ---------------------------------------------------------
+
+def test_metric_tolerance_edges():
+    ref = np.array([[1.0, -2.0]])
+    D = np.array([[10.0, 20.0]])
+    assert oracle.max_normalized_error(ref, ref, D, 0) == 0.0
+    assert oracle.max_normalized_error(ref + 0.5e-3 * D, ref, D, 0) == pytest.approx(0.5e-3)
+    assert oracle.max_normalized_error(ref + 3e-3 * D, ref, D, 0) == pytest.approx(3e-3)
+    assert oracle.max_normalized_error(np.array([[np.nan, -2.0]]), ref, D, 0) == math.inf
+    g = oracle.max_normalized_error(ref + 1e-3 * D, ref, D, wl.EPI_BIAS_GELU)
+    assert g == pytest.approx(1e-3 / oracle.GELU_LIPSCHITZ)
+
+
+def test_tolerances_keyed_by_output():
+    assert oracle.tolerance(wl.F16, wl.F16) == 2e-3
+    assert oracle.tolerance(wl.E4M3, wl.BF16) == 2e-3
+    assert oracle.tolerance(wl.E4M3, wl.F32) == 1e-5
+    assert oracle.tolerance(wl.F32, wl.F32) == 1e-5
+
+
+def _fp16_rounded(y):
+    return np.asarray(y, np.float16).astype(np.float64)
+
+
+@pytest.mark.parametrize("mistake", ["transposed_b", "dropped_beta", "bias_sign", "tanh_gelu",
+                                     "off_by_one_k", "swapped_rows"])
+def test_metric_flags_planted_mistakes(mistake):
+    """Planted mistakes in a CPU copy of the reference exceed the fp16 tolerance."""
+    p = wl.random_problem(21, 64, 64, 64, wl.F16, wl.F16, alpha=1.0, beta=0.5,
+                          epilogue=wl.EPI_BIAS_GELU)
+    args = p.oracle_args()
+    y, D = oracle.gemm_reference(**args)
+    a = oracle.decode(oracle.strided_codes(args["A"], 64, 64, p.a_stride_m, p.a_stride_k), p.ab_dtype)
+    b = oracle.decode(oracle.strided_codes(args["B"], 64, 64, p.b_stride_k, p.b_stride_n), p.ab_dtype)
+    c = oracle.decode(oracle.strided_codes(args["C"], 64, 64, p.ldc, 1), p.c_dtype)
+    bias = p.bias.numpy().astype(np.float64)
+    acc = a @ b
+    z = acc + 0.5 * c + bias
+    if mistake == "transposed_b":
+        z = a @ b.T + 0.5 * c + bias
+    elif mistake == "dropped_beta":
+        z = acc + bias
+    elif mistake == "bias_sign":
+        z = acc + 0.5 * c - bias
+    elif mistake == "off_by_one_k":
+        z = a[:, :-1] @ b[:-1] + 0.5 * c + bias
+    elif mistake == "swapped_rows":
+        z = z[::-1]
+    out = oracle.gelu(z)
+    if mistake == "tanh_gelu":
+        out = 0.5 * z * (1 + np.tanh(math.sqrt(2 / math.pi) * (z + 0.044715 * z ** 3)))
+        # the tanh form differs by < 1e-3 absolute: flagged only against a tight tolerance
+        assert oracle.max_normalized_error(out, y, D, wl.EPI_BIAS_GELU) > 1e-5
+        return
+    assert oracle.max_normalized_error(_fp16_rounded(out), y, D, wl.EPI_BIAS_GELU) > 2e-3
+    # while the correct value rounded to fp16 passes
+    assert oracle.max_normalized_error(_fp16_rounded(oracle.gelu(acc + 0.5 * c + bias)), y, D,
+                                       wl.EPI_BIAS_GELU) <= 2e-3
