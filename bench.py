@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 dense GEMM with fused epilogue.
+
+Headline workload (one "step" = one call of the whole hot path: host dispatch,
+tile scheduler, TMA producer, tcgen05 MMA, fused epilogue and store):
+    fp16 GEMM M = N = K = 4096, C = 1.5*A*B + 0.5*C, fp16 output, fp32
+    accumulation, A, B ~ N(0,1)/sqrt(K), C ~ N(0,1) (seeded, synthetic).
+Metric: TFLOP/s (2*M*N*K per step) and % of the GB300 dense tensor peak.
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier +
+device synchronisation on both sides, each step bracketed by CUDA events on
+the launch stream.  Three input sets (288 MiB, more than the 129 MB L2) are
+used in rotation, so a step does not find its operands in L2.  Under torchrun
+every rank runs its own replica (no data-path collective: independent GEMMs),
+the time is the max over ranks and ``value`` is the whole job's throughput.
+
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded row sample of the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, REPO)
+
+METRIC = "GEMM TFLOP/s at 4096³ (bf16/fp16, fp8) and % of GB300 dense tensor peak"
+NOMINAL_PEAK_TFLOPS = {"f16": 2250.0, "bf16": 2250.0, "e4m3": 4500.0}
+FALLBACK_BF16_TFLOPS = 1900.0
+WORKLOAD = "fp16 GEMM M=N=K=4096, C=1.5*A*B+0.5*C, fp16 out, fp32 accumulation"
+
+
+def _args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--size", type=int, default=4096)
+    ap.add_argument("--no-cells", action="store_true", help="skip the extra per-dtype cells")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers --
+
+def bootstrap_ci(samples, reps=10000, seed=0, q=(2.5, 97.5)):
+    """Median and percentile-bootstrap CI of the median (fixed seed, 10^4 resamples)."""
+    import numpy as np
+    x = np.asarray(samples, dtype=np.float64)
+    if x.size == 0:
+        return float("nan"), [float("nan"), float("nan")]
+    rng = np.random.default_rng(seed)
+    idx = rng.integers(0, x.size, size=(reps, x.size))
+    meds = np.median(x[idx], axis=1)
+    return float(np.median(x)), [float(np.percentile(meds, q[0])), float(np.percentile(meds, q[1]))]
+
+
+def measured_peaks():
+    path = os.path.join(REPO, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]), "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def recorded_traffic(kernel_tag):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; otherwise None."""
+    from dense_gemm_epilogues_tcgen05_gb300 import build as b
+    fp = b.source_fingerprint()[:16]
+    path = os.path.join(REPO, "profiles", "dram_traffic.tsv")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.rstrip("\n").split("\t")
+            if len(parts) >= 3 and parts[0] == fp and parts[1] == kernel_tag:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0])); smax.append(float(r[1])); power.append(float(r[2]))
+                for nm, val in zip(names, r[4:8]):
+                    if val.strip().lower() in ("active", "1"):
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s, p in zip(sm, power) if p > 0.3 * max(power)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ------------------------------------------------------------------ our arm --
+
+def _make_sets(problem, n_sets, device):
+    sets = []
+    for _ in range(n_sets):
+        sets.append((problem.A.to(device), problem.B.to(device), problem.C.clone().to(device),
+                     None if problem.bias is None else problem.bias.to(device)))
+    return sets
+
+
+def _call(g, p, s, stream):
+    A, B, C, bias = s
+    g.gemm(p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k, p.b_stride_n, C, p.ldc,
+           p.c_dtype, p.alpha, p.beta, bias, p.epilogue, stream=stream)
+
+
+def time_steps(g, p, sets, steps, warmup, stream, sampler=None, dist=None):
+    """Warm up, then time `steps` calls; returns (per-step ms list, total ms)."""
+    import torch
+    for i in range(warmup):
+        _call(g, p, sets[i % len(sets)], stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(steps):
+            _call(g, p, sets[i % len(sets)], stream)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return per, ev[0].elapsed_time(ev[steps])
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def cell(g, p, steps, warmup, stream, n_sets=3):
+    import torch
+    sets = _make_sets(p, n_sets, torch.device("cuda", torch.cuda.current_device()))
+    per, total = time_steps(g, p, sets, steps, warmup, stream)
+    tf = [p.flops / (t * 1e-3) / 1e12 for t in per]
+    med, ci = bootstrap_ci(tf)
+    del sets
+    torch.cuda.empty_cache()
+    return {"median_tflops": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)],
+            "mean_ms": round(total / steps, 5), "reps": steps}
+
+
+def e2e_measure(g, p, steps, stream):
+    """Same metric through the public call with host buffers: H2D of A, B, C
+    from pinned memory, the GEMM, and D2H of C inside each timed step."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hA, hB, hC = p.A.pin_memory(), p.B.pin_memory(), p.C.clone().pin_memory()
+    dA, dB, dC = torch.empty_like(hA, device=dev), torch.empty_like(hB, device=dev), torch.empty_like(hC, device=dev)
+    hOut = torch.empty_like(hC).pin_memory()
+    bias = None
+
+    def step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        dC.copy_(hC, non_blocking=True)
+        g.gemm(p.M, p.N, p.K, p.ab_dtype, dA, p.a_stride_m, p.a_stride_k, dB, p.b_stride_k, p.b_stride_n, dC,
+               p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue, stream=stream)
+        hOut.copy_(dC, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + hC.numel() * hC.element_size()
+    d2h = hOut.numel() * hOut.element_size()
+    return {"value": round(p.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def cpu_baseline(p, seconds, single_sample=False):
+    """The float64 oracle, as it stands, on a bounded row sample of the workload."""
+    import numpy as np
+    import oracle
+    args = p.oracle_args()
+    rows_done, t_total, r = 0, 0.0, 16
+    rng = np.random.default_rng(5)
+    while t_total < seconds and rows_done < p.M:
+        rows = np.sort(rng.choice(p.M, size=min(r, p.M - rows_done), replace=False))
+        t0 = time.perf_counter()
+        oracle.gemm_reference(rows=rows, **args)
+        t_total += time.perf_counter() - t0
+        rows_done += len(rows)
+        if single_sample:
+            break
+        r = min(r * 2, 1024)
+    flops = 2.0 * rows_done * p.N * p.K
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows_done} of {p.M} output rows of the {p.M}x{p.N}x{p.K} workload "
+                      f"(full K and N per row), {t_total:.1f} s", "seconds": round(t_total, 2)}
+
+
+def run_ours(a):
+    import torch
+    import torch.distributed as tdist
+    import workloads as wl
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        tdist.init_process_group("nccl")
+        dist = tdist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from dense_gemm_epilogues_tcgen05_gb300 import build as b
+    b.build()
+    import dense_gemm_epilogues_tcgen05_gb300 as g
+
+    n = a.size
+    p = wl.fp16_alpha_beta(n)
+    stream = torch.cuda.current_stream()
+    sets = _make_sets(p, 3, dev)
+    sampler = ClockSampler(local)
+    per, total = time_steps(g, p, sets, a.steps, a.warmup, stream, sampler=sampler, dist=dist)
+    st = g.gemm_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {g.gemm_status_string(st)}")
+    total_s = total * 1e-3
+    if dist is not None:
+        t = torch.tensor([total_s], device=dev)
+        dist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = p.flops * a.steps * world / total_s / 1e12
+    tf = [p.flops / (t * 1e-3) / 1e12 for t in per]
+    med, ci = bootstrap_ci(tf)
+    peaks = measured_peaks()
+    avg_ms = sum(per) / len(per)
+    achieved = p.flops / (avg_ms * 1e-3) / 1e12
+    traffic = recorded_traffic("tcgen05_f16_4096")
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": round(total_s * 1e3 / a.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic: seeded A,B ~ N(0,1)/sqrt(K) fp16, C ~ N(0,1) fp16",
+        "config": {"workload": WORKLOAD, "M": n, "N": n, "K": n, "layout": "A row-major (K-major), B row-major",
+                   "l2": "3 rotating input sets (288 MiB > 129 MB L2)", "parallelism": f"replicas x{world}"},
+        "median_tflops": round(med, 2), "ci95": [round(ci[0], 2), round(ci[1], 2)],
+        "pct_of_nominal_peak": round(100 * med / NOMINAL_PEAK_TFLOPS["f16"], 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 burst (fp16 runs at the bf16 rate)",
+                     "kernel": "gemm_tcgen05_kernel<f16,f16,256,4>"},
+        "clocks": sampler.summary(),
+        "gpu_launches": a.steps,
+    }
+    if rank == 0:
+        out["e2e"] = e2e_measure(g, p, 10, stream)
+        del sets
+        torch.cuda.empty_cache()
+        if not a.no_cells and world == 1:
+            out["cells"] = extra_cells(g, stream)
+        out["cpu_baseline"] = cpu_baseline(p, a.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def extra_cells(g, stream):
+    """Per-dtype cells of the headline metric: bf16 and fp8 at 4096^3 (fp8 against
+    its fp16 twin), bf16 8192^3, and the cost of the fused bias+GELU epilogue."""
+    import workloads as wl
+    cells = {}
+    cells["bf16_4096_nn"] = cell(g, wl.bf16_nn_large(4096), 30, 5, stream)
+    cells["fp8_4096_bf16out"] = cell(g, wl.fp8_e4m3(4096), 30, 5, stream)
+    cells["fp16_twin_4096_bf16out"] = cell(g, wl.fp16_twin_of_fp8(4096), 30, 5, stream)
+    cells["fp8_over_fp16"] = round(cells["fp8_4096_bf16out"]["median_tflops"] /
+                                   cells["fp16_twin_4096_bf16out"]["median_tflops"], 3)
+    cells["bf16_8192_nn"] = cell(g, wl.bf16_nn_large(8192), 10, 3, stream, n_sets=2)
+    for M in (2048, 8192):
+        fused = cell(g, wl.bf16_bias_gelu(M), 30, 5, stream)
+        plain = cell(g, wl.bf16_bias_gelu(M, epilogue=wl.EPI_NONE), 30, 5, stream)
+        cells[f"gelu_M{M}"] = {"fused": fused, "none": plain,
+                               "fused_cost_pct": round(100 * (plain["median_tflops"] / fused["median_tflops"] - 1),
+                                                       2)}
+    return cells
+
+
+# ------------------------------------------------------------ reference arm --
+
+def run_reference(a):
+    """The float64 CPU oracle on the host cores, same metric and workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import workloads as wl
+    p = wl.fp16_alpha_beta(a.size)
+    per_sample = max(1.0, min(a.cpu_seconds / max(1, a.steps + a.warmup), 10.0))
+    for _ in range(a.warmup):
+        cpu_baseline(p, per_sample, single_sample=True)
+    vals, secs = [], 0.0
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        r = cpu_baseline(p, per_sample, single_sample=True)
+        vals.append(r["value"])
+        secs += r["seconds"]
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = f"each step: 16 random output rows of the {a.size}^3 workload (full K, N), float64 oracle"
+    out = {"metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": a.gpus,
+           "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(1e3 * wall / a.steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic: seeded A,B ~ N(0,1)/sqrt(K) fp16, C ~ N(0,1) fp16",
+           "config": {"workload": WORKLOAD, "M": a.size, "N": a.size, "K": a.size,
+                      "parallelism": "host cores (oracle)"},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    a = _args(argv)
+    if a.warmup < 3 and a.impl == "ours":
+        raise SystemExit("--warmup must be >= 3")
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,140 @@
+"""Python binding of the GB300 dense GEMM + fused-epilogue library.
+
+Argument marshalling only: every call goes straight to the C ABI in
+``libgemm_gb300.so`` (declared in ``include/gemm_gb300.h``); all arithmetic
+runs in that library's CUDA kernels.  Buffers may be given as torch tensors
+(their ``data_ptr()`` is passed) or as raw integer addresses.  PyTorch is used
+only for device memory and streams.
+
+Importing this package fails loudly (ImportError) when the library has not
+been built; build it with ``python -m dense_gemm_epilogues_tcgen05_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+__all__ = [
+    "F32", "F16", "BF16", "E4M3",
+    "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU",
+    "PATH_NOOP", "PATH_EPILOGUE_ONLY", "PATH_TCGEN05", "PATH_SIMT",
+    "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
+    "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
+]
+
+# gemm_dtype_t
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
+# gemm_epilogue_t
+EPI_NONE, EPI_BIAS, EPI_BIAS_GELU = 0, 1, 2
+# gemm_path_t
+PATH_NOOP, PATH_EPILOGUE_ONLY, PATH_TCGEN05, PATH_SIMT = 0, 1, 2, 3
+# gemm_status_t
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python -m dense_gemm_epilogues_tcgen05_gb300.build` (nvcc, sm_103a)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_i64, _f32, _vp, _int, _sz = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+lib.gemm.restype = _int
+lib.gemm.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _int,
+                     _f32, _f32, _vp, _int, _vp, _sz, _vp]
+lib.gemm_query_path.restype = _int
+lib.gemm_query_path.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _int,
+                                _f32, _f32, _vp, _int, ctypes.POINTER(_int)]
+lib.gemm_workspace_size.restype = _sz
+lib.gemm_workspace_size.argtypes = [_i64, _i64, _i64, _int]
+lib.gemm_bias_gelu.restype = _int
+lib.gemm_bias_gelu.argtypes = [_i64, _i64, _vp, _i64, _int, _vp, _vp]
+lib.gemm_device_status.restype = _int
+lib.gemm_device_status.argtypes = [_vp]
+lib.gemm_status_string.restype = ctypes.c_char_p
+lib.gemm_status_string.argtypes = [_int]
+lib.gemm_version.restype = ctypes.c_char_p
+lib.gemm_version.argtypes = []
+
+
+class GemmError(RuntimeError):
+    """A non-OK gemm_status_t; ``.status`` holds the code."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gemm_status_string(status)} (status {status})")
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    raise TypeError(f"expected a torch.Tensor, an int address or None, got {type(x).__name__}")
+
+
+def _stream(s):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str) -> int:
+    if status != OK:
+        raise GemmError(status, where)
+    return status
+
+
+def gemm(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc, c_dtype,
+         alpha, beta, bias, epilogue, workspace=None, workspace_bytes=0, stream=None) -> int:
+    """C = cast(epilogue(alpha*A*B + beta*C + bias)) on the GPU; see include/gemm_gb300.h.
+
+    ``stream`` defaults to PyTorch's current stream.  Raises GemmError on a
+    non-OK status; returns 0 once the work is enqueued.
+    """
+    st = lib.gemm(M, N, K, ab_dtype, _ptr(A), a_stride_m, a_stride_k, _ptr(B), b_stride_k, b_stride_n,
+                  _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue, _ptr(workspace), workspace_bytes,
+                  _stream(stream))
+    return _check(st, "gemm")
+
+
+def gemm_query_path(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc, c_dtype,
+                    alpha, beta, bias, epilogue) -> int:
+    """Which kernel family gemm() would run for these arguments (PATH_*); launches nothing."""
+    out = _int(-1)
+    st = lib.gemm_query_path(M, N, K, ab_dtype, _ptr(A), a_stride_m, a_stride_k, _ptr(B), b_stride_k,
+                             b_stride_n, _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue,
+                             ctypes.byref(out))
+    _check(st, "gemm_query_path")
+    return out.value
+
+
+def gemm_workspace_size(M, N, K, ab_dtype) -> int:
+    return int(lib.gemm_workspace_size(M, N, K, ab_dtype))
+
+
+def gemm_bias_gelu(M, N, C, ldc, c_dtype, bias, stream=None) -> int:
+    """Unfused pass C = cast(GELU(C + bias)) (measurement of what fusion saves)."""
+    return _check(lib.gemm_bias_gelu(M, N, _ptr(C), ldc, c_dtype, _ptr(bias), _stream(stream)),
+                  "gemm_bias_gelu")
+
+
+def gemm_device_status(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status as a gemm_status_t code."""
+    return int(lib.gemm_device_status(_stream(stream)))
+
+
+def gemm_status_string(status: int) -> str:
+    return lib.gemm_status_string(status).decode()
+
+
+def gemm_version() -> str:
+    return lib.gemm_version().decode()

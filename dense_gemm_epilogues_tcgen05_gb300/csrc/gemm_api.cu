@@ -1,0 +1,392 @@
+// gemm_api.cu -- host side of the C ABI declared in include/gemm_gb300.h:
+// argument validation, the choice of kernel family, TMA tensor-map encoding
+// for each operand along its contiguous dimension, launch geometry and the
+// device status word.
+//
+// The stride convention follows "Case Study: Steel's BlockMMA" (transposition
+// carried only by the A_str_m / A_str_k style stride constants); the launch
+// geometry replaces the one-threadgroup-per-tile grid of "X3: Metal GEMM"
+// section 6 by a persistent grid of at most one CTA per SM walking tiles.
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm_gb300.h"
+#include "kernel_args.h"
+
+namespace gb300 {
+cudaError_t launch_tcgen05_f16(int, int, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int, cudaStream_t);
+cudaError_t launch_tcgen05_bf16(int, int, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int, cudaStream_t);
+cudaError_t launch_tcgen05_e4m3(int, int, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int, cudaStream_t);
+}  // namespace gb300
+
+// Device status word: kernels OR status bits into it; gemm_device_status reads
+// and clears it.
+__device__ unsigned int g_gemm_status_word;
+
+namespace {
+
+using namespace gb300;
+
+constexpr int kMaxDevices = 64;
+
+int elem_bytes(int dt) { return dt == GEMM_F32 ? 4 : (dt == GEMM_E4M3 ? 1 : 2); }
+
+bool valid_dtype(int dt) { return dt >= GEMM_F32 && dt <= GEMM_E4M3; }
+
+// ----------------------------------------------------- driver entry points --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*AddrRangeFn)(CUdeviceptr *, size_t *, CUdeviceptr);
+
+struct DriverFns {
+    EncodeTiledFn encode = nullptr;
+    AddrRangeFn addr_range = nullptr;
+    bool ok = false;
+};
+
+const DriverFns &driver_fns() {
+    static DriverFns fns;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fns.encode = reinterpret_cast<EncodeTiledFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fns.addr_range = reinterpret_cast<AddrRangeFn>(p);
+        fns.ok = fns.encode != nullptr && fns.addr_range != nullptr;
+    });
+    return fns;
+}
+
+// ------------------------------------------------------- per-device state --
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    unsigned int *status = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceState g_dev[kMaxDevices];
+
+// State of the current device; initialised on first use with that device current.
+gemm_status_t device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            return GEMM_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_gemm_status_word) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
+        d.num_sms = sms;
+        d.status = static_cast<unsigned int *>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------- the plan --
+
+struct Operand {
+    bool tma = false;      // streamed by TMA
+    bool mn_major = false; // the M (or N) index is the contiguous one
+};
+
+// Can the (rows x cols) operand with element strides (s_rows, s_cols) be
+// described by a 2-D tensor map whose inner dimension is `cols` when
+// k_inner, else `rows`?  `inner_stride` must be 1; the outer stride in bytes
+// a multiple of 16 (unless the outer extent is 1); base 16-byte aligned.
+bool tma_ok(const void *base, int64_t outer_extent, int64_t inner_stride, int64_t outer_stride, int es) {
+    if (inner_stride != 1) return false;
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+    if (outer_extent == 1) return true;
+    const int64_t bytes = outer_stride * es;
+    return bytes % 16 == 0 && bytes > 0 && bytes < (int64_t(1) << 40);
+}
+
+// An operand with logical shape (mn x k), element (i, k) at i*s_mn + k*s_k.
+Operand plan_operand(const void *base, int64_t mn, int64_t k, int64_t s_mn, int64_t s_k, int es) {
+    Operand o;
+    if (tma_ok(base, mn, s_k, s_mn, es)) {
+        o.tma = true;
+        o.mn_major = false;
+    } else if (tma_ok(base, k, s_mn, s_k, es)) {
+        o.tma = true;
+        o.mn_major = true;
+    }
+    return o;
+}
+
+struct Plan {
+    gemm_path_t path = GEMM_PATH_NOOP;
+    Operand a, b;
+};
+
+gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int ab, const void *A, int64_t sam, int64_t sak,
+                        const void *B, int64_t sbk, int64_t sbn, const void *C, int64_t ldc, int cd, float alpha,
+                        const float *bias, int epi, Plan *plan) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (!valid_dtype(ab) || !valid_dtype(cd)) return GEMM_ERR_INVALID_ARG;
+    if (epi < GEMM_EPI_NONE || epi > GEMM_EPI_BIAS_GELU) return GEMM_ERR_INVALID_ARG;
+    if (cd == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+    if (ab == GEMM_F32 && cd != GEMM_F32) return GEMM_ERR_UNSUPPORTED;
+    if (ab == GEMM_E4M3 && cd == GEMM_F16) return GEMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) {
+        plan->path = GEMM_PATH_NOOP;
+        return GEMM_OK;
+    }
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (epi != GEMM_EPI_NONE && bias == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (K == 0 || alpha == 0.0f) {
+        plan->path = GEMM_PATH_EPILOGUE_ONLY;
+        return GEMM_OK;
+    }
+    if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (sam < 0 || sak < 0 || sbk < 0 || sbn < 0) return GEMM_ERR_INVALID_ARG;
+    if (ab == GEMM_F32) {
+        plan->path = GEMM_PATH_SIMT;
+        return GEMM_OK;
+    }
+    const int es = elem_bytes(ab);
+    plan->a = plan_operand(A, M, K, sam, sak, es);
+    plan->b = plan_operand(B, N, K, sbn, sbk, es);
+    const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    plan->path = (plan->a.tma && plan->b.tma && tiles < INT32_MAX) ? GEMM_PATH_TCGEN05 : GEMM_PATH_SIMT;
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------- pointer checks --
+
+// The byte range [p, p + bytes) must lie inside one device allocation, or in
+// host memory the device can address (pinned or managed).  Plain pageable
+// host pointers are rejected: a kernel given one would fault.
+gemm_status_t check_range(const void *p, size_t bytes) {
+    if (bytes == 0) return GEMM_OK;
+    if (p == nullptr) return GEMM_ERR_INVALID_ARG;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_INVALID_ARG;
+    }
+    if (attr.type == cudaMemoryTypeUnregistered) return GEMM_ERR_INVALID_ARG;
+    if (attr.type != cudaMemoryTypeDevice) return GEMM_OK;
+    const DriverFns &fns = driver_fns();
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (fns.addr_range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return GEMM_OK;
+    const uint64_t start = reinterpret_cast<uint64_t>(p);
+    if (start < base || start + bytes > base + size) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+size_t span_bytes(int64_t rows, int64_t cols, int64_t s_rows, int64_t s_cols, int es) {
+    if (rows == 0 || cols == 0) return 0;
+    return static_cast<size_t>(((rows - 1) * s_rows + (cols - 1) * s_cols + 1) * es);
+}
+
+// ------------------------------------------------------ tensor maps --
+
+CUtensorMapDataType tma_dtype(int ab) {
+    switch (ab) {
+    case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    }
+}
+
+// 2-D map over (inner, outer) with a box of (box_inner, box_outer) elements,
+// 128-byte swizzle, zero fill outside the tensor.
+gemm_status_t encode_2d(CUtensorMap *map, int ab, const void *base, int64_t inner, int64_t outer,
+                        int64_t outer_stride_elems, uint32_t box_inner, uint32_t box_outer) {
+    const int es = elem_bytes(ab);
+    int64_t stride_bytes = outer_stride_elems * es;
+    if (outer == 1) stride_bytes = ((inner * es + 15) / 16) * 16;  // never used to address an element
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride_bytes)};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = driver_fns().encode(map, tma_dtype(ab), 2, const_cast<void *>(base), dims, strides, box, estr,
+                                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Map for an operand of logical shape (mn x k): K-major boxes are
+// (k-block x tile rows); MN-major boxes are (one 128-byte swizzle row of MN x
+// k-block), several per tile.
+gemm_status_t encode_operand(CUtensorMap *map, int ab, const void *base, const Operand &o, int64_t mn, int64_t k,
+                             int64_t s_mn, int64_t s_k, uint32_t tile_mn) {
+    const uint32_t swz = 128u / elem_bytes(ab);
+    if (!o.mn_major) return encode_2d(map, ab, base, k, mn, s_mn, swz, tile_mn);
+    return encode_2d(map, ab, base, mn, k, s_k, swz, swz);
+}
+
+cudaError_t launch_tc(int ab, int cd, int bn, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
+                      int grid, cudaStream_t s) {
+    switch (ab) {
+    case GEMM_F16: return launch_tcgen05_f16(cd, bn, ta, tb, args, grid, s);
+    case GEMM_BF16: return launch_tcgen05_bf16(cd, bn, ta, tb, args, grid, s);
+    case GEMM_E4M3: return launch_tcgen05_e4m3(cd, bn, ta, tb, args, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alpha, float beta, const float *bias,
+                   int epi) {
+    EpiParams e;
+    e.M = static_cast<int>(M);
+    e.N = static_cast<int>(N);
+    e.C = C;
+    e.ldc = ldc;
+    e.bias = bias;
+    e.alpha = alpha;
+    e.beta = beta;
+    e.epilogue = epi;
+    const bool c_al = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (ldc * elem_bytes(cd)) % 16 == 0;
+    const bool b_al = epi == GEMM_EPI_NONE || (reinterpret_cast<uintptr_t>(bias) & 15u) == 0;
+    e.c_vec = (c_al && b_al) ? 1 : 0;
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_query_path(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const void *A,
+                              int64_t a_stride_m, int64_t a_stride_k, const void *B, int64_t b_stride_k,
+                              int64_t b_stride_n, const void *C, int64_t ldc, gemm_dtype_t c_dtype, float alpha,
+                              float beta, const float *bias, gemm_epilogue_t epilogue, gemm_path_t *path) {
+    (void)beta;
+    if (path == nullptr) return GEMM_ERR_INVALID_ARG;
+    Plan plan;
+    gemm_status_t st = make_plan(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc,
+                                 c_dtype, alpha, bias, epilogue, &plan);
+    if (st == GEMM_OK) *path = plan.path;
+    return st;
+}
+
+size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype) {
+    (void)M; (void)N; (void)K; (void)ab_dtype;
+    return 0;
+}
+
+gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const void *A, int64_t a_stride_m,
+                   int64_t a_stride_k, const void *B, int64_t b_stride_k, int64_t b_stride_n, void *C, int64_t ldc,
+                   gemm_dtype_t c_dtype, float alpha, float beta, const float *bias, gemm_epilogue_t epilogue,
+                   void *workspace, size_t workspace_bytes, gemm_stream_t stream) {
+    (void)workspace; (void)workspace_bytes;
+    Plan plan;
+    gemm_status_t st = make_plan(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc,
+                                 c_dtype, alpha, bias, epilogue, &plan);
+    if (st != GEMM_OK || plan.path == GEMM_PATH_NOOP) return st;
+    if (!driver_fns().ok) return GEMM_ERR_CUDA;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != GEMM_OK) return st;
+
+    const int es = elem_bytes(ab_dtype), ces = elem_bytes(c_dtype);
+    if ((st = check_range(C, span_bytes(M, N, ldc, 1, ces))) != GEMM_OK) return st;
+    if (epilogue != GEMM_EPI_NONE && (st = check_range(bias, static_cast<size_t>(N) * 4)) != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    EpiParams e = make_epi(M, N, C, ldc, c_dtype, alpha, beta, bias, epilogue);
+
+    if (plan.path == GEMM_PATH_EPILOGUE_ONLY)
+        return launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+
+    if ((st = check_range(A, span_bytes(M, K, a_stride_m, a_stride_k, es))) != GEMM_OK) return st;
+    if ((st = check_range(B, span_bytes(K, N, b_stride_k, b_stride_n, es))) != GEMM_OK) return st;
+
+    if (plan.path == GEMM_PATH_SIMT) {
+        SimtArgs a;
+        a.e = e;
+        a.K = static_cast<int>(K);
+        a.A = A; a.sam = a_stride_m; a.sak = a_stride_k;
+        a.B = B; a.sbk = b_stride_k; a.sbn = b_stride_n;
+        return launch_simt(ab_dtype, c_dtype, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+
+    // tcgen05 path.  Tile width: 256 unless that leaves SMs idle.
+    const int64_t tiles_m = (M + 127) / 128;
+    int bn = 256;
+    if (tiles_m * ((N + 255) / 256) < dev->num_sms) bn = 128;
+    const int64_t tiles_n = (N + bn - 1) / bn;
+    const int bk = 128 / es;
+    CUtensorMap ta, tb;
+    if ((st = encode_operand(&ta, ab_dtype, A, plan.a, M, K, a_stride_m, a_stride_k, 128)) != GEMM_OK) return st;
+    if ((st = encode_operand(&tb, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, bn)) != GEMM_OK) return st;
+    TcArgs t;
+    t.e = e;
+    t.K = static_cast<int>(K);
+    t.tiles_m = static_cast<int>(tiles_m);
+    t.tiles_n = static_cast<int>(tiles_n);
+    t.num_tiles = static_cast<int>(tiles_m * tiles_n);
+    t.num_kb = static_cast<int>((K + bk - 1) / bk);
+    t.group_m = 8;
+    t.a_mn_major = plan.a.mn_major ? 1u : 0u;
+    t.b_mn_major = plan.b.mn_major ? 1u : 0u;
+    t.status = dev->status;
+    const int grid = static_cast<int>(t.num_tiles < dev->num_sms ? t.num_tiles : dev->num_sms);
+    return launch_tc(ab_dtype, c_dtype, bn, ta, tb, t, grid, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dtype_t c_dtype, const float *bias,
+                             gemm_stream_t stream) {
+    if (M < 0 || N < 0 || M > INT32_MAX || N > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    if (!valid_dtype(c_dtype) || c_dtype == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (C == nullptr || bias == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (!driver_fns().ok) return GEMM_ERR_CUDA;
+    gemm_status_t st;
+    if ((st = check_range(C, span_bytes(M, N, ldc, 1, elem_bytes(c_dtype)))) != GEMM_OK) return st;
+    if ((st = check_range(bias, static_cast<size_t>(N) * 4)) != GEMM_OK) return st;
+    EpiParams e = make_epi(M, N, C, ldc, c_dtype, 1.0f, 0.0f, bias, GEMM_EPI_BIAS_GELU);
+    return launch_bias_gelu(c_dtype, e, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? GEMM_OK
+                                                                                                : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_device_status(gemm_stream_t stream) {
+    DeviceState *dev = nullptr;
+    gemm_status_t st = device_state(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpyAsync(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (cudaMemsetAsync(dev->status, 0, sizeof(word), s) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_ERR_CUDA;
+    return word != 0 ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+const char *gemm_status_string(gemm_status_t status) {
+    switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported dtype combination or size";
+    case GEMM_ERR_MISALIGNED: return "misaligned operand";
+    case GEMM_ERR_WORKSPACE: return "workspace missing or too small";
+    case GEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case GEMM_ERR_TIMEOUT: return "a device-side wait timed out";
+    default: return "unknown status";
+    }
+}
+
+const char *gemm_version(void) { return "gemm_gb300 0.1 (sm_103a, tcgen05)"; }
+
+}  // extern "C"

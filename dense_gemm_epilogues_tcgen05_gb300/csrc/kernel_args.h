@@ -1,0 +1,56 @@
+// kernel_args.h -- argument blocks passed by value from the host library to
+// the kernels, and the launcher entry points each kernel file exports to the
+// host library (internal; not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace gb300 {
+
+// Element type and epilogue codes, numbered like gemm_dtype_t / gemm_epilogue_t.
+enum : int { kDtF32 = 0, kDtF16 = 1, kDtBF16 = 2, kDtE4M3 = 3 };
+enum : int { kEpiNone = 0, kEpiBias = 1, kEpiBiasGelu = 2 };
+
+// Everything the epilogue needs: output geometry and the scalars.
+struct EpiParams {
+    int M, N;
+    void *C;          // M x ldc row-major output (input too when beta != 0)
+    long long ldc;    // elements
+    const float *bias;
+    float alpha, beta;
+    int epilogue;
+    int c_vec;        // C base and row pitch allow 16-byte vector access
+};
+
+// tcgen05 path: operands come through the two tensor maps.
+struct TcArgs {
+    EpiParams e;
+    int K;
+    int tiles_m, tiles_n, num_tiles, num_kb, group_m;
+    uint32_t a_mn_major, b_mn_major;  // 1: the M (resp. N) index is the contiguous one
+    unsigned int *status;             // device status word (timeouts)
+};
+
+// SIMT path: operands as (pointer, stride) views, any strides.
+struct SimtArgs {
+    EpiParams e;
+    int K;
+    const void *A;
+    long long sam, sak;
+    const void *B;
+    long long sbk, sbn;
+};
+
+// Launchers (each returns the launch's cudaError_t).  `bn` is the tile width.
+cudaError_t launch_tcgen05(int ab, int out, int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                           const TcArgs &args, int grid, cudaStream_t stream);
+cudaError_t launch_simt(int ab, int out, const SimtArgs &args, cudaStream_t stream);
+cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t stream);
+cudaError_t launch_bias_gelu(int out, const EpiParams &e, cudaStream_t stream);
+
+// Dynamic shared memory a tcgen05 configuration needs (host side, for checks).
+int tcgen05_smem_bytes(int ab, int bn);
+
+}  // namespace gb300

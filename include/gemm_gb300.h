@@ -1,0 +1,172 @@
+/*
+ * gemm_gb300.h -- C ABI of the GB300 (sm_103a) dense GEMM with fused epilogue.
+ *
+ * Operation (one call):
+ *
+ *     z[i][j] = alpha * sum_k A[i][k] * B[k][j]  +  beta * C[i][j]  +  bias[j]
+ *     C[i][j] = cast_out( epilogue(z[i][j]) )        for 0 <= i < M, 0 <= j < N
+ *
+ * with fp32 accumulation whatever the input type, the epilogue applied to the
+ * accumulators in registers and the result stored once.  Defined on the pages
+ * by: "Case Study: Steel's BlockMMA" (the paragraph on the ending where fusion
+ * plugs in -- store_result applies the Epilogue to every accumulator, and
+ * apply_epilogue reads an input C for alpha*AB + beta*C; AccumType = float;
+ * transposition by the A_str_m / A_str_k stride constants), "Case Study: The
+ * Tiled GEMM" (the fused alpha*AB + beta*C store), "X3: Metal GEMM" sections
+ * 2, 4 and 5 (out-of-range operand elements read as zero; the masked,
+ * casting write-back that never touches elements outside M x N) and Rigel
+ * (abstract and section 1: GEMM + bias + GELU fused into one kernel).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers except those documented as host pointers are DEVICE
+ *     pointers on the current CUDA device.  The caller owns every buffer;
+ *     the library allocates nothing per call and keeps no pointer after a
+ *     call returns.
+ *   - Strides and leading dimensions are in ELEMENTS, not bytes.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     A returned GEMM_OK means the work was enqueued; device-side failures
+ *     are reported later by gemm_device_status().
+ *   - No entry point prints, aborts or traps.  Argument errors return a
+ *     status code before anything is enqueued.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *gemm_stream_t;
+
+/* Element types.  E4M3 is OCP FP8 E4M3 ("fn": finite, saturating, NaN = S.1111.111). */
+typedef enum {
+    GEMM_F32 = 0,
+    GEMM_F16 = 1,
+    GEMM_BF16 = 2,
+    GEMM_E4M3 = 3
+} gemm_dtype_t;
+
+/* Epilogues, applied to z before the cast.  GELU is the exact erf form
+ * 0.5*z*(1 + erf(z/sqrt(2))). */
+typedef enum {
+    GEMM_EPI_NONE = 0,
+    GEMM_EPI_BIAS = 1,
+    GEMM_EPI_BIAS_GELU = 2
+} gemm_epilogue_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,   /* negative size, ldc < N, bad enum, NULL where a buffer is needed */
+    GEMM_ERR_UNSUPPORTED = 2,   /* dtype combination the library does not implement */
+    GEMM_ERR_MISALIGNED = 3,    /* reserved: every stride/alignment has a path, so not returned today */
+    GEMM_ERR_WORKSPACE = 4,     /* workspace missing or smaller than gemm_workspace_size() */
+    GEMM_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+    GEMM_ERR_TIMEOUT = 6        /* a device-side wait gave up (reported by gemm_device_status) */
+} gemm_status_t;
+
+/* Which kernel family a call runs on (see gemm_query_path). */
+typedef enum {
+    GEMM_PATH_NOOP = 0,           /* M == 0 or N == 0: nothing to do */
+    GEMM_PATH_EPILOGUE_ONLY = 1,  /* K == 0 or alpha == 0: C = cast(epilogue(beta*C + bias)) */
+    GEMM_PATH_TCGEN05 = 2,        /* TMA -> shared memory -> tcgen05.mma (TMEM accumulators) */
+    GEMM_PATH_SIMT = 3            /* CUDA-core FFMA kernel (fp32 inputs, or strides TMA cannot take) */
+} gemm_path_t;
+
+/*
+ * gemm -- C = cast(epilogue(alpha*A*B + beta*C + bias)), C updated in place.
+ *
+ *   M, N, K        problem sizes, each >= 0.  M == 0 or N == 0 is a no-op.
+ *                  K == 0 (or alpha == 0) gives C = cast(epilogue(beta*C + bias))
+ *                  and reads neither A nor B (BLAS convention).
+ *   ab_dtype       element type of A and B: F32, F16, BF16 or E4M3.
+ *   A              element (i, k) is A[i*a_stride_m + k*a_stride_k].
+ *   B              element (k, j) is B[k*b_stride_k + j*b_stride_n].
+ *                  Transposition is expressed only through these strides; any
+ *                  non-negative strides are accepted.  When one stride of an
+ *                  operand is 1, the base is 16-byte aligned and the other
+ *                  stride is a multiple of 16 bytes, the operand is streamed
+ *                  by TMA; otherwise the call runs on the SIMT kernel.
+ *   C, ldc         row-major M x N output (and input when beta != 0) inside an
+ *                  M x ldc buffer, ldc >= N.  Columns N..ldc-1 and anything
+ *                  outside the M x N block are never written.
+ *   c_dtype        F32, F16 or BF16.  F32 inputs require F32 output; E4M3
+ *                  inputs require BF16 or F32 output.
+ *   alpha, beta    fp32 scalars.  beta == 0: C is not read (NaNs in C do not
+ *                  propagate).  For fp8 with per-tensor dequantisation scales
+ *                  s_a, s_b, pass alpha * s_a * s_b.
+ *   bias           fp32[N] device array, required (non-NULL) when epilogue is
+ *                  BIAS or BIAS_GELU, ignored otherwise.
+ *   epilogue       GEMM_EPI_NONE, GEMM_EPI_BIAS or GEMM_EPI_BIAS_GELU; the
+ *                  order is z = alpha*AB + beta*C + bias, then GELU, then cast
+ *                  (round to nearest even).
+ *   workspace      device scratch of at least gemm_workspace_size(...) bytes,
+ *   workspace_bytes  or NULL / 0 when that size is 0 (it is 0 for every
+ *                  configuration today).
+ *   stream         CUDA stream the work is enqueued on.
+ *
+ * Aliasing: C must not overlap A, B or bias.  Returns GEMM_OK once enqueued.
+ */
+gemm_status_t gemm(int64_t M, int64_t N, int64_t K,
+                   gemm_dtype_t ab_dtype,
+                   const void *A, int64_t a_stride_m, int64_t a_stride_k,
+                   const void *B, int64_t b_stride_k, int64_t b_stride_n,
+                   void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                   float alpha, float beta,
+                   const float *bias, gemm_epilogue_t epilogue,
+                   void *workspace, size_t workspace_bytes,
+                   gemm_stream_t stream);
+
+/*
+ * gemm_workspace_size -- bytes of device scratch gemm() needs for this shape
+ * and input type (0 today for every configuration).  Never fails.
+ */
+size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype);
+
+/*
+ * gemm_query_path -- validate the same arguments gemm() takes and report, in
+ * *path (host pointer), which kernel family gemm() would launch.  Launches
+ * nothing and touches no device memory.  Returns the status gemm() would
+ * return before enqueueing.
+ */
+gemm_status_t gemm_query_path(int64_t M, int64_t N, int64_t K,
+                              gemm_dtype_t ab_dtype,
+                              const void *A, int64_t a_stride_m, int64_t a_stride_k,
+                              const void *B, int64_t b_stride_k, int64_t b_stride_n,
+                              const void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                              float alpha, float beta,
+                              const float *bias, gemm_epilogue_t epilogue,
+                              gemm_path_t *path);
+
+/*
+ * gemm_bias_gelu -- the UNFUSED second pass, for measuring what fusion saves
+ * (Rigel abstract: fused GEMM + bias + GELU against the decomposed path):
+ * C[i][j] = cast(GELU(C[i][j] + bias[j])) in place, for an M x N block of an
+ * M x ldc row-major buffer of type c_dtype (F32, F16 or BF16).  bias is fp32[N]
+ * on the device.  Asynchronous on `stream`; same error behaviour as gemm().
+ */
+gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                             const float *bias, gemm_stream_t stream);
+
+/*
+ * gemm_device_status -- synchronise `stream`, then return and clear the
+ * device-side status word of the current device: GEMM_ERR_TIMEOUT if any
+ * kernel gave up on a bounded wait since the last call, GEMM_ERR_CUDA if the
+ * synchronisation itself failed, GEMM_OK otherwise.
+ */
+gemm_status_t gemm_device_status(gemm_stream_t stream);
+
+/* gemm_status_string -- static, NUL-terminated description of a status code. */
+const char *gemm_status_string(gemm_status_t status);
+
+/* gemm_version -- static version string of the library build. */
+const char *gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

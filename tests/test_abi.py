@@ -1,0 +1,118 @@
+"""The C-ABI library (CPU only: no kernel launches).
+
+* the shared library loads and exports every function include/*.h declares;
+* the host-side argument validation and kernel-family choice, which run
+  before any CUDA call, behave as the header documents.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import REPO
+
+
+@pytest.fixture(scope="module")
+def g():
+    from dense_gemm_epilogues_tcgen05_gb300 import build as b
+    b.build()
+    import dense_gemm_epilogues_tcgen05_gb300 as g
+    return g
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(REPO, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b([A-Za-z_]\w*)\s*\(([^;{}]*)\)\s*;", text):
+            if m.group(1) not in ("if", "while", "for", "return", "sizeof"):
+                names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    assert {"gemm", "gemm_workspace_size", "gemm_query_path", "gemm_bias_gelu", "gemm_device_status",
+            "gemm_status_string", "gemm_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(g):
+    lib = ctypes.CDLL(g.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(g):
+    assert g.gemm_status_string(0) == "ok"
+    assert "timed out" in g.gemm_status_string(6)
+    assert g.gemm_status_string(99) == "unknown status"
+    assert "sm_103a" in g.gemm_version()
+
+
+def test_workspace_is_zero(g):
+    assert g.gemm_workspace_size(4096, 4096, 4096, g.F32) == 0
+    assert g.gemm_workspace_size(4096, 4096, 4096, g.BF16) == 0
+
+
+# Fake, aligned device addresses: query_path never dereferences them.
+PA, PB, PC, PBIAS = 0x7F0000000000, 0x7F1000000000, 0x7F2000000000, 0x7F3000000000
+
+
+def q(g, M=256, N=256, K=256, ab=None, A=PA, sam=256, sak=1, B=PB, sbk=256, sbn=1, C=PC, ldc=256, cd=None,
+      alpha=1.0, beta=0.0, bias=None, epi=0):
+    ab = g.BF16 if ab is None else ab
+    cd = g.BF16 if cd is None else cd
+    return g.gemm_query_path(M, N, K, ab, A, sam, sak, B, sbk, sbn, C, ldc, cd, alpha, beta, bias, epi)
+
+
+def test_path_choice_by_layout(g):
+    # NN (A K-major, B N-major), NT, TN, TT: all on the tensor cores
+    assert q(g) == g.PATH_TCGEN05
+    assert q(g, sbk=1, sbn=256) == g.PATH_TCGEN05
+    assert q(g, sam=1, sak=256) == g.PATH_TCGEN05
+    assert q(g, sam=1, sak=256, sbk=1, sbn=256) == g.PATH_TCGEN05
+    assert q(g, ab=g.E4M3) == g.PATH_TCGEN05
+    assert q(g, ab=g.F16, cd=g.F32) == g.PATH_TCGEN05
+
+
+def test_path_choice_fallbacks(g):
+    assert q(g, ab=g.F32, cd=g.F32) == g.PATH_SIMT                    # fp32 inputs: FFMA kernel
+    assert q(g, A=PA + 2) == g.PATH_SIMT                               # base not 16-byte aligned
+    assert q(g, K=1001, sam=1001) == g.PATH_SIMT                       # row pitch not a multiple of 16 B
+    assert q(g, K=1000, sam=1000) == g.PATH_TCGEN05                    # 2000 B pitch is fine
+    assert q(g, sam=512, sak=2) == g.PATH_SIMT                         # no unit stride
+    assert q(g, M=1, sam=3) == g.PATH_TCGEN05                          # single row: pitch unused
+    assert q(g, ab=g.E4M3, K=24, sam=24) == g.PATH_SIMT                # 24 B pitch
+
+
+def test_degenerate_paths(g):
+    assert q(g, M=0) == g.PATH_NOOP
+    assert q(g, N=0, A=None, B=None, C=None) == g.PATH_NOOP
+    assert q(g, K=0, A=None, B=None) == g.PATH_EPILOGUE_ONLY
+    assert q(g, alpha=0.0, A=None, B=None) == g.PATH_EPILOGUE_ONLY
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), 1), (dict(K=-5), 1), (dict(ldc=255), 1), (dict(C=None), 1), (dict(A=None), 1),
+    (dict(epi=1), 1), (dict(epi=3, bias=PBIAS), 1), (dict(ab=7), 1), (dict(sam=-256), 1),
+    (dict(ab=0, cd=2), 2), (dict(ab=3, cd=1), 2), (dict(cd=3), 2), (dict(M=1 << 31), 2),
+])
+def test_argument_errors(g, kw, status):
+    with pytest.raises(g.GemmError) as ei:
+        q(g, **kw)
+    assert ei.value.status == status
+
+
+def test_gemm_rejects_bad_arguments_before_any_cuda_call(g):
+    with pytest.raises(g.GemmError) as ei:
+        g.gemm(-1, 4, 4, g.BF16, PA, 4, 1, PB, 4, 1, PC, 4, g.BF16, 1.0, 0.0, None, 0, stream=0)
+    assert ei.value.status == g.ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as ei:
+        g.gemm(4, 4, 4, g.F32, PA, 4, 1, PB, 4, 1, PC, 4, g.F16, 1.0, 0.0, None, 0, stream=0)
+    assert ei.value.status == g.ERR_UNSUPPORTED
+    # M == 0: a no-op that succeeds without touching anything
+    assert g.gemm(0, 4, 4, g.BF16, None, 4, 1, None, 4, 1, None, 4, g.BF16, 1.0, 0.0, None, 0, stream=0) == 0

@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA library through its C ABI against the float64 oracle.
+
+Bar: integer-valued inputs (exact in every storage type, sums < 2^24) must come
+back bit-exact with fp32 output; random workloads must meet the normalised
+tolerance (2e-3 for 16-bit outputs, 1e-5 for fp32 outputs).  Every run also
+checks that nothing outside the M x N block of C was written (guards and ldc
+padding compared bit for bit).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import run_gemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TC_SHAPES = [
+    (128, 256, 128),     # one tile, two k-blocks (16-bit)
+    (16, 16, 16),        # far smaller than a tile: TMA zero fill everywhere
+    (336, 208, 1008),    # ragged M, N and K, 16-byte row pitches
+    (256, 512, 1024),    # several tiles, ring wraps
+    (2048, 2048, 256),   # several tiles per CTA: double-buffered accumulator
+    (1024, 768, 4096),   # long K
+]
+
+
+def _assert_exact(run):
+    y, _ = oracle.gemm_reference(**run.p.oracle_args())
+    got = run.values()
+    bad = np.argwhere(got != y)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:3].tolist()}: got {got[tuple(bad[0])]} " \
+                          f"want {y[tuple(bad[0])]}"
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layout", ["NN", "NT", "TN", "TT"])
+@pytest.mark.parametrize("ab", [wl.F16, wl.BF16, wl.E4M3], ids=["f16", "bf16", "e4m3"])
+def test_integer_exact_tcgen05(cuda_lib, ab, layout, shape):
+    M, N, K = shape
+    p = wl.random_problem(1000 + M + N + K, M, N, K, ab, wl.F32, layout=layout, alpha=2.0, beta=-1.0,
+                          integer=True)
+    r = run_gemm(cuda_lib, p)
+    assert r.status == 0
+    assert r.path == cuda_lib.PATH_TCGEN05
+    _assert_exact(r)
+
+
+@pytest.mark.parametrize("ab", [wl.F16, wl.BF16, wl.E4M3], ids=["f16", "bf16", "e4m3"])
+def test_integer_exact_simt_fallback(cuda_lib, ab):
+    """Row pitches that TMA cannot take run on the SIMT kernel, still exact."""
+    for (M, N, K, layout) in [(5, 260, 129, "NN"), (77, 33, 301, "TT"), (130, 129, 67, "NT")]:
+        p = wl.random_problem(7 + M, M, N, K, ab, wl.F32, layout=layout, alpha=1.0, beta=0.0, integer=True)
+        r = run_gemm(cuda_lib, p)
+        assert r.path == cuda_lib.PATH_SIMT
+        _assert_exact(r)
+
+
+def test_integer_exact_misaligned_base(cuda_lib):
+    p = wl.random_problem(3, 256, 256, 256, wl.BF16, wl.F32, integer=True)
+    r = run_gemm(cuda_lib, p, a_elem_offset=1)
+    assert r.path == cuda_lib.PATH_SIMT
+    _assert_exact(r)
+
+
+@pytest.mark.parametrize("out", [wl.F16, wl.BF16, wl.F32], ids=["f16", "bf16", "f32"])
+@pytest.mark.parametrize("epi", [wl.EPI_NONE, wl.EPI_BIAS, wl.EPI_BIAS_GELU], ids=["none", "bias", "gelu"])
+def test_epilogues_and_outputs_ragged(cuda_lib, out, epi):
+    for ab in (wl.F16, wl.BF16):
+        p = wl.random_problem(31, 300, 200, 520, ab, out, alpha=0.75, beta=0.5 if epi == 0 else 0.0,
+                              epilogue=epi)
+        r = run_gemm(cuda_lib, p)
+        assert r.path == cuda_lib.PATH_TCGEN05
+        res = r.check()
+        assert res["pass"], res
+
+
+def test_odd_ldc_uses_masked_store(cuda_lib):
+    p = wl.random_problem(41, 256, 256, 256, wl.BF16, wl.BF16, beta=1.0, ldc_pad=3, epilogue=wl.EPI_BIAS)
+    r = run_gemm(cuda_lib, p)
+    assert r.path == cuda_lib.PATH_TCGEN05 and r.check()["pass"]
+
+
+# ------------------------------------------------------------------ workloads --
+
+def test_fp32_256(cuda_lib):
+    r = run_gemm(cuda_lib, wl.fp32_square(256))
+    assert r.path == cuda_lib.PATH_SIMT
+    res = r.check()
+    assert res["pass"], res
+
+
+@pytest.mark.parametrize("n", [512, 1024, 2048, 1000])
+def test_fp16_alpha_beta_full(cuda_lib, n):
+    r = run_gemm(cuda_lib, wl.fp16_alpha_beta(n))
+    assert r.path == cuda_lib.PATH_TCGEN05
+    res = r.check()
+    assert res["pass"], res
+
+
+def test_fp16_alpha_beta_4096_sampled(cuda_lib):
+    r = run_gemm(cuda_lib, wl.fp16_alpha_beta(4096))
+    res = r.check(rows=sample_rows(4096))
+    assert res["pass"], res
+
+
+@pytest.mark.parametrize("M", [512, 2048])
+def test_bias_gelu_fused_and_unfused(cuda_lib, M):
+    g = cuda_lib
+    p = wl.bf16_bias_gelu(M)
+    r = run_gemm(g, p)
+    assert r.path == g.PATH_TCGEN05
+    res = r.check()
+    assert res["pass"], res
+    # decomposed path: GEMM with no epilogue, then the separate bias+GELU pass
+    A, B, bias = p.A.cuda(), p.B.cuda(), p.bias.cuda()
+    C = torch.empty(p.M * p.ldc, dtype=torch.bfloat16, device="cuda")
+    g.gemm(p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k, p.b_stride_n, C, p.ldc,
+           p.c_dtype, p.alpha, 0.0, None, wl.EPI_NONE)
+    g.gemm_bias_gelu(p.M, p.N, C, p.ldc, p.c_dtype, bias)
+    assert g.gemm_device_status() == 0
+    out = C.cpu().view(torch.int16).numpy()
+    res2 = oracle.check(p.oracle_args(), out)
+    assert res2["pass"], res2
+
+
+def test_bias_gelu_8192_sampled(cuda_lib):
+    r = run_gemm(cuda_lib, wl.bf16_bias_gelu(8192))
+    res = r.check(rows=sample_rows(8192))
+    assert res["pass"], res
+
+
+def test_fp8_2048_full_bf16_and_f32_out(cuda_lib):
+    r = run_gemm(cuda_lib, wl.fp8_e4m3(2048))
+    assert r.path == cuda_lib.PATH_TCGEN05
+    res = r.check()
+    assert res["pass"], res
+    r32 = run_gemm(cuda_lib, wl.fp8_e4m3(2048, c_dtype=wl.F32))
+    res32 = r32.check()
+    assert res32["pass"], res32
+
+
+@pytest.mark.parametrize("n", [4096, 8192])
+def test_fp8_sampled(cuda_lib, n):
+    r = run_gemm(cuda_lib, wl.fp8_e4m3(n))
+    res = r.check(rows=sample_rows(n))
+    assert res["pass"], res
+
+
+@pytest.mark.parametrize("layout", ["NN", "NT", "TN", "TT"])
+def test_fp32_layouts_4096_sampled(cuda_lib, layout):
+    r = run_gemm(cuda_lib, wl.fp32_layout(layout, 4096))
+    res = r.check(rows=sample_rows(4096, n_random=64))
+    assert res["pass"], res
+
+
+def test_bf16_nn_8192_sampled(cuda_lib):
+    r = run_gemm(cuda_lib, wl.bf16_nn_large(8192))
+    assert r.path == cuda_lib.PATH_TCGEN05
+    res = r.check(rows=sample_rows(8192, n_random=128))
+    assert res["pass"], res
+
+
+# ------------------------------------------------------------- degenerate cases --
+
+def test_m_or_n_zero_is_noop(cuda_lib):
+    g = cuda_lib
+    C = torch.full((64,), 7.0, device="cuda")
+    g.gemm(0, 8, 8, g.F32, None, 8, 1, None, 8, 1, C, 8, g.F32, 1.0, 1.0, None, 0)
+    g.gemm(8, 0, 8, g.F32, None, 8, 1, None, 8, 1, C, 8, g.F32, 1.0, 1.0, None, 0)
+    assert g.gemm_device_status() == 0
+    assert bool((C == 7.0).all())
+
+
+@pytest.mark.parametrize("kind", ["k0", "alpha0"])
+def test_epilogue_only(cuda_lib, kind):
+    K = 0 if kind == "k0" else 64
+    alpha = 1.0 if kind == "k0" else 0.0
+    p = wl.random_problem(51, 130, 70, K, wl.BF16, wl.BF16, alpha=alpha, beta=0.5, epilogue=wl.EPI_BIAS_GELU)
+    r = run_gemm(cuda_lib, p)
+    assert r.path == cuda_lib.PATH_EPILOGUE_ONLY
+    res = r.check()
+    assert res["pass"], res
+
+
+@pytest.mark.parametrize("ab,out", [(wl.BF16, wl.BF16), (wl.F32, wl.F32), (wl.E4M3, wl.F32)])
+def test_beta_zero_never_reads_c(cuda_lib, ab, out):
+    p = wl.random_problem(61, 200, 136, 96, ab, out, alpha=1.0, beta=0.0)
+    r = run_gemm(cuda_lib, p, nan_c=True)
+    assert not np.isnan(r.values()).any()
+    assert r.check()["pass"]
+
+
+def test_runs_on_a_side_stream(cuda_lib):
+    s = torch.cuda.Stream()
+    p = wl.fp16_alpha_beta(384, 256, 320)
+    with torch.cuda.stream(s):
+        r = run_gemm(cuda_lib, p, stream=s)
+    assert r.check()["pass"]
+
+
+def test_deterministic(cuda_lib):
+    p = wl.bf16_bias_gelu(512, N=1024, K=1024)
+    a = run_gemm(cuda_lib, p).out_codes
+    b = run_gemm(cuda_lib, p).out_codes
+    assert np.array_equal(a, b)
+
+
+def test_rejects_pageable_host_and_out_of_range_buffers(cuda_lib):
+    g = cuda_lib
+    A = torch.zeros(64 * 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(64 * 64, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(64 * 64, dtype=torch.bfloat16, device="cuda")
+    host = torch.zeros(64 * 64, dtype=torch.bfloat16)
+    with pytest.raises(g.GemmError) as ei:
+        g.gemm(64, 64, 64, g.BF16, host, 64, 1, B, 64, 1, C, 64, g.BF16, 1.0, 0.0, None, 0)
+    assert ei.value.status == g.ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as ei:
+        g.gemm(64, 64, 64, g.BF16, A, 1 << 34, 1, B, 64, 1, C, 64, g.BF16, 1.0, 0.0, None, 0)
+    assert ei.value.status == g.ERR_INVALID_ARG
+    assert g.gemm_device_status() == 0
