@@ -7,7 +7,7 @@ runs in that library's CUDA kernels.  Buffers may be given as torch tensors
 only for device memory and streams.
 
 Importing this package fails loudly (ImportError) when the library has not
-been built; build it with ``python -m dense_gemm_epilogues_tcgen05_gb300.build``.
+been built; build it with ``python dense_gemm_epilogues_tcgen05_gb300/build.py``.
 """
 from __future__ import annotations
 
@@ -37,7 +37,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm_gb3
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
-                      "`python -m dense_gemm_epilogues_tcgen05_gb300.build` (nvcc, sm_103a)")
+                      "`python dense_gemm_epilogues_tcgen05_gb300/build.py` (nvcc, sm_103a)")
 
 lib = ctypes.CDLL(LIB_PATH)
 

@@ -5,7 +5,7 @@ linked into one shared library next to this file, against the shared CUDA
 runtime (so a process that already loaded PyTorch's runtime reuses it).
 Object files and ptxas reports go to ``_build/`` at the repository root.
 
-Usage:  python -m dense_gemm_epilogues_tcgen05_gb300.build [--force] [-v]
+Usage:  python dense_gemm_epilogues_tcgen05_gb300/build.py [--force] [-v]
 """
 from __future__ import annotations
 
@@ -44,7 +44,9 @@ def _sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _fingerprint() -> str:
+def source_fingerprint() -> str:
+    """Hash of every kernel / header source and the nvcc flags (machine-independent:
+    profile records taken on the GPU host are matched against it)."""
     h = hashlib.sha256()
     for d in (CSRC, INCLUDE):
         for f in sorted(os.listdir(d)):
@@ -54,13 +56,11 @@ def _fingerprint() -> str:
                 with open(p, "rb") as fh:
                     h.update(fh.read())
     h.update(" ".join(NVCC_FLAGS).encode())
-    h.update(os.uname().machine.encode())
     return h.hexdigest()
 
 
-def source_fingerprint() -> str:
-    """Hash of every kernel / header source and the build flags."""
-    return _fingerprint()
+def _fingerprint() -> str:
+    return source_fingerprint() + "-" + os.uname().machine
 
 
 def _compile(nvcc: str, src: str) -> tuple[str, str]:

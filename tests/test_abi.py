@@ -16,8 +16,8 @@ from conftest import REPO
 
 @pytest.fixture(scope="module")
 def g():
-    from dense_gemm_epilogues_tcgen05_gb300 import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import dense_gemm_epilogues_tcgen05_gb300 as g
     return g
 

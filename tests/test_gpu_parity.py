@@ -173,11 +173,14 @@ def test_m_or_n_zero_is_noop(cuda_lib):
     assert bool((C == 7.0).all())
 
 
+@pytest.mark.parametrize("out", [wl.F16, wl.F32], ids=["f16", "f32"])
 @pytest.mark.parametrize("kind", ["k0", "alpha0"])
-def test_epilogue_only(cuda_lib, kind):
+def test_epilogue_only(cuda_lib, kind, out):
+    # Here |z| is of the order of the error scale D itself, so a bf16 output's
+    # rounding (unit roundoff 2^-8) alone would exceed 2e-3: f16 / f32 outputs.
     K = 0 if kind == "k0" else 64
     alpha = 1.0 if kind == "k0" else 0.0
-    p = wl.random_problem(51, 130, 70, K, wl.BF16, wl.BF16, alpha=alpha, beta=0.5, epilogue=wl.EPI_BIAS_GELU)
+    p = wl.random_problem(51, 130, 70, K, wl.BF16, out, alpha=alpha, beta=0.5, epilogue=wl.EPI_BIAS_GELU)
     r = run_gemm(cuda_lib, p)
     assert r.path == cuda_lib.PATH_EPILOGUE_ONLY
     res = r.check()
