@@ -20,7 +20,9 @@ __all__ = [
     "F32", "F16", "BF16", "E4M3",
     "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU",
     "PATH_NOOP", "PATH_EPILOGUE_ONLY", "PATH_TCGEN05", "PATH_SIMT",
+    "TILE_AUTO", "TILE_1SM_256", "TILE_1SM_128", "TILE_PAIR",
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
+    "gemm_set_tile_policy", "gemm_query_tile",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
 
@@ -30,6 +32,8 @@ F32, F16, BF16, E4M3 = 0, 1, 2, 3
 EPI_NONE, EPI_BIAS, EPI_BIAS_GELU = 0, 1, 2
 # gemm_path_t
 PATH_NOOP, PATH_EPILOGUE_ONLY, PATH_TCGEN05, PATH_SIMT = 0, 1, 2, 3
+# gemm_tile_policy_t
+TILE_AUTO, TILE_1SM_256, TILE_1SM_128, TILE_PAIR = 0, 1, 2, 3
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -53,6 +57,11 @@ lib.gemm_workspace_size.restype = _sz
 lib.gemm_workspace_size.argtypes = [_i64, _i64, _i64, _int]
 lib.gemm_bias_gelu.restype = _int
 lib.gemm_bias_gelu.argtypes = [_i64, _i64, _vp, _i64, _int, _vp, _vp]
+lib.gemm_set_tile_policy.restype = _int
+lib.gemm_set_tile_policy.argtypes = [_int, _int]
+lib.gemm_query_tile.restype = _int
+lib.gemm_query_tile.argtypes = [_i64, _i64, _i64, _int, _int, ctypes.POINTER(_int), ctypes.POINTER(_int),
+                                ctypes.POINTER(_int)]
 lib.gemm_device_status.restype = _int
 lib.gemm_device_status.argtypes = [_vp]
 lib.gemm_status_string.restype = ctypes.c_char_p
@@ -125,6 +134,20 @@ def gemm_bias_gelu(M, N, C, ldc, c_dtype, bias, stream=None) -> int:
     """Unfused pass C = cast(GELU(C + bias)) (measurement of what fusion saves)."""
     return _check(lib.gemm_bias_gelu(M, N, _ptr(C), ldc, c_dtype, _ptr(bias), _stream(stream)),
                   "gemm_bias_gelu")
+
+
+def gemm_set_tile_policy(policy, bn=0) -> int:
+    """Process-wide tile policy of the tcgen05 path (TILE_*); bn only with TILE_PAIR."""
+    return _check(lib.gemm_set_tile_policy(policy, bn), "gemm_set_tile_policy")
+
+
+def gemm_query_tile(M, N, K, ab_dtype, c_dtype):
+    """(kind, bn, units) of the tcgen05 path on the current device: kind 1 = one SM per
+    tile, 2 = SM pair; units = tiles in flight at once (CTAs or clusters)."""
+    kind, bn, units = _int(0), _int(0), _int(0)
+    _check(lib.gemm_query_tile(M, N, K, ab_dtype, c_dtype, ctypes.byref(kind), ctypes.byref(bn),
+                               ctypes.byref(units)), "gemm_query_tile")
+    return kind.value, bn.value, units.value
 
 
 def gemm_device_status(stream=None) -> int:

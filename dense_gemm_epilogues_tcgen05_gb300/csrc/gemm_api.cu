@@ -10,18 +10,13 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
 
 #include "../../include/gemm_gb300.h"
 #include "kernel_args.h"
-
-namespace gb300 {
-cudaError_t launch_tcgen05_f16(int, int, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int, cudaStream_t);
-cudaError_t launch_tcgen05_bf16(int, int, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int, cudaStream_t);
-cudaError_t launch_tcgen05_e4m3(int, int, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int, cudaStream_t);
-}  // namespace gb300
 
 // Device status word: kernels OR status bits into it; gemm_device_status reads
 // and clears it.
@@ -76,6 +71,7 @@ struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     unsigned int *status = nullptr;
+    int max_clusters[4][4];  // pair kernel, by (ab, out); -1 = not queried yet
 };
 
 std::mutex g_dev_mu;
@@ -95,6 +91,8 @@ gemm_status_t device_state(DeviceState **out) {
         if (cudaGetSymbolAddress(&p, g_gemm_status_word) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
         d.num_sms = sms;
         d.status = static_cast<unsigned int *>(p);
+        for (auto &row : d.max_clusters)
+            for (int &v : row) v = -1;
         d.ready = true;
     }
     *out = &d;
@@ -238,6 +236,93 @@ gemm_status_t encode_operand(CUtensorMap *map, int ab, const void *base, const O
     return encode_2d(map, ab, base, mn, k, s_k, swz, swz);
 }
 
+// ------------------------------------------------------------ tile choice --
+
+std::atomic<int> g_tile_policy{GEMM_TILE_AUTO};
+std::atomic<int> g_tile_policy_bn{0};
+
+int pair_max_clusters_for(int ab, int cd) {
+    switch (ab) {
+    case GEMM_F16: return pair_max_clusters_f16(cd);
+    case GEMM_BF16: return pair_max_clusters_bf16(cd);
+    case GEMM_E4M3: return pair_max_clusters_e4m3(cd);
+    default: return 0;
+    }
+}
+
+// Resident two-CTA clusters of the pair kernel on this device (cached).
+int device_max_clusters(DeviceState *d, int ab, int cd) {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    int &v = d->max_clusters[ab][cd];
+    if (v < 0) v = pair_max_clusters_for(ab, cd);
+    return v;
+}
+
+struct TileChoice {
+    int kind = 1;  // 1: one SM per 128 x bn tile; 2: a pair of SMs per 256 x bn tile
+    int bn = 256;
+};
+
+// Cost model.  Every SM computes 128 rows x bn columns per tile, so a tile
+// takes time ~ bn / eff, where eff is the tensor-pipe duty cycle that shared
+// memory bandwidth (~128 B/clk/SM) allows: per 16-deep k slice the MMA reads
+// A (4 KB) and its B columns and TMA writes the same bytes.
+//   one SM, 128 x bn:  (4096 + 32 bn) * 2 bytes per bn/2 clk
+//   pair, 256 x bn:    (4096 + 16 bn) * 2 bytes per bn/2 clk
+// Time = ceil(tiles / concurrent tiles) * bn / eff: wave quantisation over the
+// SMs (one-SM) or the resident clusters (pair) is the other term.  Pair widths
+// between 128 and 256 are not candidates: measured on GB300 they lose more
+// per tile (e.g. fp8 4096^3: 2314 TFLOP/s at 224 vs 2684 at 256) than wave
+// balance gains; they stay reachable through the tile policy.
+TileChoice choose_tile(int64_t M, int64_t N, int num_sms, int max_clusters, int policy, int policy_bn) {
+    auto cdiv = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
+    auto eff_of = [](int kind, int bn) {
+        const double bytes_per_clk = kind == 2 ? 4.0 * (4096.0 + 16.0 * bn) / bn : 4.0 * (4096.0 + 32.0 * bn) / bn;
+        return bytes_per_clk <= 128.0 ? 1.0 : 128.0 / bytes_per_clk;
+    };
+    TileChoice best;
+    double best_t = 1e300;
+    auto consider = [&](int kind, int bn) {
+        int64_t tiles, units;
+        if (kind == 2) {
+            if (max_clusters <= 0) return;
+            tiles = cdiv(M, 256) * cdiv(N, bn);
+            units = max_clusters;
+        } else {
+            tiles = cdiv(M, 128) * cdiv(N, bn);
+            units = num_sms;
+        }
+        const double t = static_cast<double>(cdiv(tiles, units)) * bn / eff_of(kind, bn);
+        if (t < best_t * (1.0 - 1e-9)) {
+            best_t = t;
+            best.kind = kind;
+            best.bn = bn;
+        }
+    };
+    static const int pair_widths[] = {256, 128};
+    if (policy == GEMM_TILE_1SM_256) return TileChoice{1, 256};
+    if (policy == GEMM_TILE_1SM_128) return TileChoice{1, 128};
+    if (policy == GEMM_TILE_PAIR && max_clusters > 0) {
+        if (policy_bn > 0) return TileChoice{2, policy_bn};
+        for (int bn : pair_widths) consider(2, bn);
+        return best;
+    }
+    for (int bn : pair_widths) consider(2, bn);
+    consider(1, 256);
+    consider(1, 128);
+    return best;
+}
+
+cudaError_t launch_pair(int ab, int cd, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
+                        int clusters, cudaStream_t s) {
+    switch (ab) {
+    case GEMM_F16: return launch_pair_f16(cd, ta, tb, args, clusters, s);
+    case GEMM_BF16: return launch_pair_bf16(cd, ta, tb, args, clusters, s);
+    case GEMM_E4M3: return launch_pair_e4m3(cd, ta, tb, args, clusters, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_tc(int ab, int cd, int bn, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
                       int grid, cudaStream_t s) {
     switch (ab) {
@@ -321,15 +406,19 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
         return launch_simt(ab_dtype, c_dtype, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
-    // tcgen05 path.  Tile width: 256 unless that leaves SMs idle.
-    const int64_t tiles_m = (M + 127) / 128;
-    int bn = 256;
-    if (tiles_m * ((N + 255) / 256) < dev->num_sms) bn = 128;
-    const int64_t tiles_n = (N + bn - 1) / bn;
+    // tcgen05 path: one SM or a pair of SMs per tile, by the cost model.
+    const int max_clusters = device_max_clusters(dev, ab_dtype, c_dtype);
+    const TileChoice tc = choose_tile(M, N, dev->num_sms, max_clusters, g_tile_policy.load(),
+                                      g_tile_policy_bn.load());
     const int bk = 128 / es;
+    const int64_t rows_per_tile = tc.kind == 2 ? 256 : 128;
+    const int64_t tiles_m = (M + rows_per_tile - 1) / rows_per_tile;
+    const int64_t tiles_n = (N + tc.bn - 1) / tc.bn;
+    // B's box covers this SM's columns: the whole tile (one SM) or half of it (pair).
+    const uint32_t b_box = static_cast<uint32_t>(tc.kind == 2 ? tc.bn / 2 : tc.bn);
     CUtensorMap ta, tb;
     if ((st = encode_operand(&ta, ab_dtype, A, plan.a, M, K, a_stride_m, a_stride_k, 128)) != GEMM_OK) return st;
-    if ((st = encode_operand(&tb, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, bn)) != GEMM_OK) return st;
+    if ((st = encode_operand(&tb, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, b_box)) != GEMM_OK) return st;
     TcArgs t;
     t.e = e;
     t.K = static_cast<int>(K);
@@ -341,8 +430,45 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     t.a_mn_major = plan.a.mn_major ? 1u : 0u;
     t.b_mn_major = plan.b.mn_major ? 1u : 0u;
     t.status = dev->status;
-    const int grid = static_cast<int>(t.num_tiles < dev->num_sms ? t.num_tiles : dev->num_sms);
-    return launch_tc(ab_dtype, c_dtype, bn, ta, tb, t, grid, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    t.bn = tc.bn;
+    const uint32_t swz = 128u / es;
+    const uint32_t b_bytes = plan.b.mn_major ? ((b_box + swz - 1) / swz) * 128u * bk : b_box * 128u;
+    t.stage_tx = 128u * 128u + b_bytes;
+    cudaError_t err;
+    if (tc.kind == 2) {
+        const int clusters = static_cast<int>(t.num_tiles < max_clusters ? t.num_tiles : max_clusters);
+        err = launch_pair(ab_dtype, c_dtype, ta, tb, t, clusters, s);
+    } else {
+        const int grid = static_cast<int>(t.num_tiles < dev->num_sms ? t.num_tiles : dev->num_sms);
+        err = launch_tc(ab_dtype, c_dtype, tc.bn, ta, tb, t, grid, s);
+    }
+    return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_set_tile_policy(gemm_tile_policy_t policy, int bn) {
+    if (policy < GEMM_TILE_AUTO || policy > GEMM_TILE_PAIR) return GEMM_ERR_INVALID_ARG;
+    if (bn != 0 && (policy != GEMM_TILE_PAIR || bn < 128 || bn > 256 || bn % 32 != 0)) return GEMM_ERR_INVALID_ARG;
+    g_tile_policy_bn.store(bn);
+    g_tile_policy.store(policy);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_query_tile(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, gemm_dtype_t c_dtype,
+                              int *kind, int *bn, int *units) {
+    (void)K;
+    if (kind == nullptr || bn == nullptr || units == nullptr || M < 0 || N < 0) return GEMM_ERR_INVALID_ARG;
+    if (!valid_dtype(ab_dtype) || !valid_dtype(c_dtype) || ab_dtype == GEMM_F32 || c_dtype == GEMM_E4M3)
+        return GEMM_ERR_UNSUPPORTED;
+    DeviceState *dev = nullptr;
+    gemm_status_t st = device_state(&dev);
+    if (st != GEMM_OK) return st;
+    const int max_clusters = device_max_clusters(dev, ab_dtype, c_dtype);
+    const TileChoice tc = choose_tile(M, N, dev->num_sms, max_clusters, g_tile_policy.load(),
+                                      g_tile_policy_bn.load());
+    *kind = tc.kind;
+    *bn = tc.bn;
+    *units = tc.kind == 2 ? max_clusters : dev->num_sms;
+    return GEMM_OK;
 }
 
 gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dtype_t c_dtype, const float *bias,

@@ -1,6 +1,8 @@
 // gemm_tcgen05_bf16.cu -- tcgen05 GEMM instantiations for bf16 A/B operands.
-// Tile widths: 256 (4-stage ring) and 128 (6-stage ring), both 192 KB of stages.
+// One-SM kernel: tile widths 256 (4-stage ring) and 128 (6-stage ring).
+// Pair kernel: 256 x BN tiles on two SMs, 6-stage ring of 32 KB per CTA.
 #include "gemm_tcgen05.cuh"
+#include "gemm_tcgen05_pair.cuh"
 
 namespace gb300 {
 
@@ -13,6 +15,21 @@ cudaError_t launch_tcgen05_bf16(int out, int bn, const CUtensorMap &ta, const CU
     if (out == kDtF16 && bn == 256) return launch_tcgen05_cfg<kDtBF16, kDtF16, 256, 4>(ta, tb, args, grid, stream);
     if (out == kDtF16 && bn == 128) return launch_tcgen05_cfg<kDtBF16, kDtF16, 128, 6>(ta, tb, args, grid, stream);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pair_bf16(int out, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
+                              int clusters, cudaStream_t stream) {
+    if (out == kDtBF16) return launch_pair_cfg<kDtBF16, kDtBF16, 6>(ta, tb, args, clusters, stream);
+    if (out == kDtF32) return launch_pair_cfg<kDtBF16, kDtF32, 6>(ta, tb, args, clusters, stream);
+    if (out == kDtF16) return launch_pair_cfg<kDtBF16, kDtF16, 6>(ta, tb, args, clusters, stream);
+    return cudaErrorInvalidValue;
+}
+
+int pair_max_clusters_bf16(int out) {
+    if (out == kDtBF16) return pair_max_clusters<kDtBF16, kDtBF16, 6>();
+    if (out == kDtF32) return pair_max_clusters<kDtBF16, kDtF32, 6>();
+    if (out == kDtF16) return pair_max_clusters<kDtBF16, kDtF16, 6>();
+    return 0;
 }
 
 }  // namespace gb300

@@ -1,0 +1,319 @@
+// gemm_tcgen05_pair.cuh -- the GEMM on pairs of SMs (tcgen05 cta_group::2).
+//
+// Same roles as the one-SM kernel (gemm_tcgen05.cuh), but a cluster of two
+// CTAs on two SMs computes one 256 x BN output tile with one MMA stream:
+//
+//   * each CTA's producer loads its own 128 rows of A and its own BN/2
+//     columns of B into its own shared memory, and counts the bytes on the
+//     LEADER CTA's full[s] barrier (TMA with cta_group::2);
+//   * the leader's MMA thread issues tcgen05.mma.cta_group::2 256 x BN x K;
+//     the hardware reads A rows 0-127 / B columns 0..BN/2-1 from the leader's
+//     shared memory and the rest from the peer's, and writes accumulator rows
+//     0-127 to the leader's tensor memory and 128-255 to the peer's;
+//   * tcgen05.commit multicasts to both CTAs: empty[s] frees both halves of a
+//     stage, tfull[acc] starts both CTAs' epilogues;
+//   * each CTA's eight epilogue warps drain their own tensor memory (two warps
+//     per 32-lane quadrant, each taking half of the columns) and arrive on the
+//     leader's tempty[acc].
+//
+// Per SM and per 16-deep k slice, the MMA reads 4 KB of A and 16*BN bytes of
+// B from shared memory and TMA writes as much: 128 B/clk at BN = 256, which
+// fits the shared-memory bandwidth, where the one-SM 128 x 256 tile needs
+// 192 B/clk.  BN is a runtime multiple of 32 up to 256, chosen by the host to
+// balance waves of tiles over the clusters.
+#pragma once
+
+#include "epilogue.cuh"
+#include "gemm_tcgen05.cuh"
+#include "kernel_args.h"
+#include "sm103_ptx.cuh"
+
+namespace gb300 {
+
+template <int AB, int STAGES_>
+struct PairConfig {
+    static constexpr int BM = 128;  // rows per CTA (256 per pair)
+    static constexpr int BN_MAX = 256;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int ES = TcTraits<AB>::kBytes;
+    static constexpr int SWZ = 128 / ES;
+    static constexpr int BK = SWZ;
+    static constexpr int UMMA_K = TcTraits<AB>::kUmmaK;
+    static constexpr int KSTEPS = BK / UMMA_K;
+    static constexpr int A_BYTES = BM * BK * ES;          // this CTA's rows of A
+    static constexpr int B_BYTES = (BN_MAX / 2) * BK * ES; // this CTA's columns of B (at most)
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int ACC_STRIDE = 256;                // TMEM columns between the two accumulators
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
+    static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the pair allocates all 512 TMEM columns");
+};
+
+// A bounded wait that, when it gives up, also raises the peer CTA's abort flag.
+__device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int *status, uint32_t peer_abort_addr) {
+    if (mbar_wait_bounded(bar, parity, abort_flag, status)) return true;
+    st_shared_cluster_u32(peer_abort_addr, 1u);
+    return false;
+}
+
+template <int AB, int OUT, int STAGES>
+__global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
+    gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const TcArgs args) {
+    using Cfg = PairConfig<AB, STAGES>;
+    using OutT = typename Elem<OUT>::T;
+    constexpr int BM = Cfg::BM, BK = Cfg::BK, SWZ = Cfg::SWZ;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: leader, 1: peer
+    const int cluster = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+    const int bn = args.bn;
+    const int bnh = bn >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);   // the leader's expect_tx arrive covers both CTAs' bytes
+            mbar_init(&empty[s], 1);  // one multicast commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 2 * Cfg::EPI_WARPS);  // both CTAs' epilogue warps (leader's copy is used)
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
+    const uint32_t tempty0_leader = mapa_shared(smem_u32(&tempty[0]), 0);
+    const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u);
+
+    const int M = args.e.M, N = args.e.N;
+    const int num_kb = args.num_kb;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer --
+            uint32_t stage = 0, phase = 0;
+            bool ok = true, issued = false;
+            for (int tile = cluster; ok && tile < args.num_tiles; tile += nclusters) {
+                int tm, tn;
+                tile_coords(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
+                const int m0 = tm * 2 * BM + static_cast<int>(rank) * BM;
+                const int n0 = tn * bn + static_cast<int>(rank) * bnh;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, args.status, peer_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    // Only the leader arms the phase, with both CTAs' bytes; the
+                    // peer's loads complete on the leader's barrier (a
+                    // completion may precede the arming within a phase: the
+                    // phase cannot end before the leader's arrive).  This keeps
+                    // cluster-scope fences off the per-k-block path.
+                    const uint32_t fbar = full0_leader + 8u * stage;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2u * args.stage_tx);
+                    issued = true;
+                    unsigned char *sA = smem + stage * Cfg::STAGE_BYTES;
+                    unsigned char *sB = sA + Cfg::A_BYTES;
+                    const int k0 = kb * BK;
+                    if (!args.a_mn_major) {
+                        tma_load_2d_pair(sA, &tmA, fbar, k0, m0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / SWZ; ++j)
+                            tma_load_2d_pair(sA + j * 128 * BK, &tmA, fbar, m0 + j * SWZ, k0);
+                    }
+                    if (!args.b_mn_major) {
+                        tma_load_2d_pair(sB, &tmB, fbar, k0, n0);
+                    } else {
+                        for (int j = 0; j * SWZ < bnh; ++j)
+                            tma_load_2d_pair(sB + j * 128 * BK, &tmB, fbar, n0 + j * SWZ, k0);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag && issued) {
+                // Unwinding: loads in flight complete within microseconds; give
+                // them time to land before this CTA's shared memory is released.
+                const unsigned long long t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) sleep_ns(10000);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // --------------------------------------------- MMA issuer (leader) --
+            const uint32_t idesc = mma_idesc(TcTraits<AB>::kFmt, TcTraits<AB>::kFmt, 2 * BM, bn) |
+                                   (args.a_mn_major << 15) | (args.b_mn_major << 16);
+            const uint32_t a_lbo = args.a_mn_major ? 128u * BK : 16u;
+            const uint32_t b_lbo = args.b_mn_major ? 128u * BK : 16u;
+            const uint32_t a_kstep = args.a_mn_major ? 128u * Cfg::UMMA_K : 32u;
+            const uint32_t b_kstep = args.b_mn_major ? 128u * Cfg::UMMA_K : 32u;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true, issued = false;
+            int local = 0;
+            for (int tile = cluster; ok && tile < args.num_tiles; tile += nclusters, ++local) {
+                const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
+                if (!pair_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, args.status, peer_abort)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * Cfg::ACC_STRIDE;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!pair_wait(&full[stage], phase, abort_flag, args.status, peer_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + Cfg::A_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
+                        const uint64_t ad = sw128_desc(a_addr + ks * a_kstep, a_lbo, 1024u);
+                        const uint64_t bd = sw128_desc(b_addr + ks * b_kstep, b_lbo, 1024u);
+                        tc_mma_pair<TcTraits<AB>::kKind>(d_tmem, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit_pair(&empty[stage], 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit_pair(&tfull[acc], 0x3);
+            }
+            if (*abort_flag && issued) {
+                tc_commit_pair(mma_done, 0x1);
+                mbar_drain_wait(mma_done, 0, 100000000ull);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- epilogue --
+        const int ew = warp - 2;           // 0..7
+        const int quad = warp & 3;         // TMEM lanes 32*quad .. 32*quad+31
+        const int half = ew >> 2;          // which half of the tile's columns
+        const int nchunks = bn >> 5;
+        const int c_begin = half ? (nchunks + 1) >> 1 : 0;
+        const int c_end = half ? nchunks : (nchunks + 1) >> 1;
+        const EpiParams &e = args.e;
+        int local = 0;
+        for (int tile = cluster; tile < args.num_tiles; tile += nclusters, ++local) {
+            const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
+            int tm, tn;
+            tile_coords(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
+            const int row = tm * 2 * BM + static_cast<int>(rank) * BM + quad * 32 + lane;
+            const int n_tile = tn * bn;
+            const bool got = pair_wait(&tfull[acc], acc_phase, abort_flag, args.status, peer_abort);
+            if (__any_sync(0xffffffffu, !got)) break;
+            tc_fence_after();
+            const bool row_ok = row < M;
+            OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
+            const uint32_t t_row =
+                tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * Cfg::ACC_STRIDE;
+#pragma unroll 1
+            for (int c = c_begin; c < c_end; ++c) {
+                const int col0 = n_tile + c * 32;
+                if (col0 >= N) break;  // warp-uniform
+                float v[32];
+                __syncwarp();
+                tmem_ld_32cols(t_row + c * 32, v);
+                if (row_ok) {
+                    if (e.c_vec && col0 + 32 <= N)
+                        epilogue_chunk32_fast<OUT>(v, crow + col0, e.bias + col0, e);
+                    else
+                        epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(tempty0_leader + 8u * acc);
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();  // no CTA leaves while its peer may still signal into it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int AB, int OUT, int STAGES>
+cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, int clusters,
+                            cudaStream_t stream) {
+    using Cfg = PairConfig<AB, STAGES>;
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+}
+
+// Largest number of two-CTA clusters of this kernel that can be resident at once.
+template <int AB, int OUT, int STAGES>
+int pair_max_clusters() {
+    using Cfg = PairConfig<AB, STAGES>;
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace gb300

@@ -31,6 +31,8 @@ struct TcArgs {
     int tiles_m, tiles_n, num_tiles, num_kb, group_m;
     uint32_t a_mn_major, b_mn_major;  // 1: the M (resp. N) index is the contiguous one
     unsigned int *status;             // device status word (timeouts)
+    int bn;                           // pair kernel: tile width (multiple of 32, <= 256)
+    uint32_t stage_tx;                // pair kernel: bytes one CTA's loads deliver per stage
 };
 
 // SIMT path: operands as (pointer, stride) views, any strides.
@@ -43,14 +45,27 @@ struct SimtArgs {
     long long sbk, sbn;
 };
 
-// Launchers (each returns the launch's cudaError_t).  `bn` is the tile width.
-cudaError_t launch_tcgen05(int ab, int out, int bn, const CUtensorMap &ta, const CUtensorMap &tb,
-                           const TcArgs &args, int grid, cudaStream_t stream);
+// Launchers (each returns the launch's cudaError_t), defined by the kernel files.
+//   one-SM tcgen05 kernel, `bn` = 256 or 128, `grid` CTAs:
+cudaError_t launch_tcgen05_f16(int out, int bn, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int grid,
+                               cudaStream_t);
+cudaError_t launch_tcgen05_bf16(int out, int bn, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int grid,
+                                cudaStream_t);
+cudaError_t launch_tcgen05_e4m3(int out, int bn, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int grid,
+                                cudaStream_t);
+//   pair kernel (tile width in args.bn), `clusters` two-CTA clusters:
+cudaError_t launch_pair_f16(int out, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
+                            cudaStream_t);
+cudaError_t launch_pair_bf16(int out, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
+                             cudaStream_t);
+cudaError_t launch_pair_e4m3(int out, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
+                             cudaStream_t);
+int pair_max_clusters_f16(int out);
+int pair_max_clusters_bf16(int out);
+int pair_max_clusters_e4m3(int out);
+//   CUDA-core kernels:
 cudaError_t launch_simt(int ab, int out, const SimtArgs &args, cudaStream_t stream);
 cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t stream);
 cudaError_t launch_bias_gelu(int out, const EpiParams &e, cudaStream_t stream);
-
-// Dynamic shared memory a tcgen05 configuration needs (host side, for checks).
-int tcgen05_smem_bytes(int ab, int bn);
 
 }  // namespace gb300

@@ -141,6 +141,34 @@ gemm_status_t gemm_query_path(int64_t M, int64_t N, int64_t K,
                               const float *bias, gemm_epilogue_t epilogue,
                               gemm_path_t *path);
 
+/* Tile policy of the tcgen05 path (process-wide; see gemm_set_tile_policy). */
+typedef enum {
+    GEMM_TILE_AUTO = 0,     /* cost model: wave balance over the SMs and shared-memory bandwidth */
+    GEMM_TILE_1SM_256 = 1,  /* one SM per 128 x 256 output tile */
+    GEMM_TILE_1SM_128 = 2,  /* one SM per 128 x 128 output tile */
+    GEMM_TILE_PAIR = 3      /* a cluster of two SMs per 256 x bn output tile (cta_group::2 MMA) */
+} gemm_tile_policy_t;
+
+/*
+ * gemm_set_tile_policy -- choose how later gemm() calls tile the output on the
+ * tcgen05 path, for every thread of the process.  `bn` is used with
+ * GEMM_TILE_PAIR only: a multiple of 32 in 128..256, or 0 to let the cost
+ * model pick the width.  Meant for tuning and tests; GEMM_TILE_AUTO (the
+ * default) is the right choice otherwise.  Returns GEMM_ERR_INVALID_ARG for an
+ * unknown policy or width; never touches the device.
+ */
+gemm_status_t gemm_set_tile_policy(gemm_tile_policy_t policy, int bn);
+
+/*
+ * gemm_query_tile -- the tile the tcgen05 path would use on the current device
+ * for an M x N x K problem: *kind = 1 for one SM per tile, 2 for a pair of SMs;
+ * *bn = tile width; *units = tiles in flight at once (CTAs, or two-CTA
+ * clusters).  All three are host pointers.  Reads device attributes; launches
+ * nothing.  GEMM_ERR_CUDA if the device cannot be queried.
+ */
+gemm_status_t gemm_query_tile(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, gemm_dtype_t c_dtype,
+                              int *kind, int *bn, int *units);
+
 /*
  * gemm_bias_gelu -- the UNFUSED second pass, for measuring what fusion saves
  * (Rigel abstract: fused GEMM + bias + GELU against the decomposed path):

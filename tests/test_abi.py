@@ -37,7 +37,7 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     assert {"gemm", "gemm_workspace_size", "gemm_query_path", "gemm_bias_gelu", "gemm_device_status",
-            "gemm_status_string", "gemm_version"} <= names
+            "gemm_status_string", "gemm_version", "gemm_set_tile_policy", "gemm_query_tile"} <= names
 
 
 def test_library_exports_every_declared_symbol(g):
@@ -116,3 +116,13 @@ def test_gemm_rejects_bad_arguments_before_any_cuda_call(g):
     assert ei.value.status == g.ERR_UNSUPPORTED
     # M == 0: a no-op that succeeds without touching anything
     assert g.gemm(0, 4, 4, g.BF16, None, 4, 1, None, 4, 1, None, 4, g.BF16, 1.0, 0.0, None, 0, stream=0) == 0
+
+
+def test_tile_policy_validation(g):
+    for policy, bn in [(0, 0), (1, 0), (2, 0), (3, 0), (3, 128), (3, 224), (3, 256)]:
+        assert g.gemm_set_tile_policy(policy, bn) == 0
+    for policy, bn in [(4, 0), (-1, 0), (3, 96), (3, 288), (3, 200), (1, 256)]:
+        with pytest.raises(g.GemmError) as ei:
+            g.gemm_set_tile_policy(policy, bn)
+        assert ei.value.status == g.ERR_INVALID_ARG
+    g.gemm_set_tile_policy(g.TILE_AUTO, 0)

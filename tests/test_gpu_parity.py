@@ -34,10 +34,23 @@ def _assert_exact(run):
                           f"want {y[tuple(bad[0])]}"
 
 
+# (policy, pair width): every tile variant of the tcgen05 path
+POLICIES = [(1, 0), (2, 0), (3, 0), (3, 224), (3, 160)]
+
+
+@pytest.fixture
+def tile_policy(cuda_lib, request):
+    policy, bn = request.param
+    cuda_lib.gemm_set_tile_policy(policy, bn)
+    yield request.param
+    cuda_lib.gemm_set_tile_policy(cuda_lib.TILE_AUTO, 0)
+
+
+@pytest.mark.parametrize("tile_policy", POLICIES, indirect=True, ids=lambda p: f"pol{p[0]}-{p[1]}")
 @pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("layout", ["NN", "NT", "TN", "TT"])
 @pytest.mark.parametrize("ab", [wl.F16, wl.BF16, wl.E4M3], ids=["f16", "bf16", "e4m3"])
-def test_integer_exact_tcgen05(cuda_lib, ab, layout, shape):
+def test_integer_exact_tcgen05(cuda_lib, ab, layout, shape, tile_policy):
     M, N, K = shape
     p = wl.random_problem(1000 + M + N + K, M, N, K, ab, wl.F32, layout=layout, alpha=2.0, beta=-1.0,
                           integer=True)
@@ -64,9 +77,10 @@ def test_integer_exact_misaligned_base(cuda_lib):
     _assert_exact(r)
 
 
+@pytest.mark.parametrize("tile_policy", [(1, 0), (3, 0), (3, 192)], indirect=True, ids=lambda p: f"pol{p[0]}-{p[1]}")
 @pytest.mark.parametrize("out", [wl.F16, wl.BF16, wl.F32], ids=["f16", "bf16", "f32"])
 @pytest.mark.parametrize("epi", [wl.EPI_NONE, wl.EPI_BIAS, wl.EPI_BIAS_GELU], ids=["none", "bias", "gelu"])
-def test_epilogues_and_outputs_ragged(cuda_lib, out, epi):
+def test_epilogues_and_outputs_ragged(cuda_lib, out, epi, tile_policy):
     for ab in (wl.F16, wl.BF16):
         p = wl.random_problem(31, 300, 200, 520, ab, out, alpha=0.75, beta=0.5 if epi == 0 else 0.0,
                               epilogue=epi)
@@ -223,3 +237,25 @@ def test_rejects_pageable_host_and_out_of_range_buffers(cuda_lib):
         g.gemm(64, 64, 64, g.BF16, A, 1 << 34, 1, B, 64, 1, C, 64, g.BF16, 1.0, 0.0, None, 0)
     assert ei.value.status == g.ERR_INVALID_ARG
     assert g.gemm_device_status() == 0
+
+
+def test_cost_model_choices(cuda_lib):
+    g = cuda_lib
+    g.gemm_set_tile_policy(g.TILE_AUTO, 0)
+    kind, bn, units = g.gemm_query_tile(4096, 4096, 4096, g.F16, g.F16)
+    assert kind == 2 and bn == 256 and units >= 70   # pair of SMs
+    kind, bn, _ = g.gemm_query_tile(8192, 8192, 8192, g.BF16, g.BF16)
+    assert kind == 2 and bn == 256
+    g.gemm_set_tile_policy(g.TILE_1SM_128, 0)
+    assert g.gemm_query_tile(4096, 4096, 4096, g.F16, g.F16)[:2] == (1, 128)
+    g.gemm_set_tile_policy(g.TILE_PAIR, 160)
+    assert g.gemm_query_tile(4096, 4096, 4096, g.F16, g.F16)[:2] == (2, 160)
+    g.gemm_set_tile_policy(g.TILE_AUTO, 0)
+
+
+@pytest.mark.parametrize("tile_policy", [(1, 0), (3, 256), (3, 224)], indirect=True, ids=lambda p: f"pol{p[0]}-{p[1]}")
+def test_fp16_alpha_beta_2048_each_tiling(cuda_lib, tile_policy):
+    r = run_gemm(cuda_lib, wl.fp16_alpha_beta(2048))
+    res = r.check()
+    assert res["pass"], res
+    assert cuda_lib.gemm_device_status() == 0
