@@ -20,6 +20,7 @@
 #include <cuda_fp8.h>
 
 #include "kernel_args.h"
+#include "sm103_ptx.cuh"
 
 namespace gb300 {
 
@@ -44,9 +45,100 @@ template <> struct Elem<kDtE4M3> {
     static __device__ __forceinline__ float load(const T *p) { return static_cast<float>(*p); }
 };
 
-// GELU, exact erf form: 0.5*z*(1 + erf(z/sqrt(2))).
+// GELU, erf form: 0.5*z*(1 + erf(z/sqrt(2))), with erf from the rational
+// approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26 (Hastings): for x >= 0,
+//     erfc(x) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2) + e(x),
+//     t = 1 / (1 + p x),  |e(x)| <= 1.5e-7,
+// p = 0.3275911, a1..a5 = 0.254829592, -0.284496736, 1.421413741,
+// -1.453152027, 1.061405429.  With x = |z|/sqrt(2) and q = erfc(x):
+//     erf(z/sqrt(2)) = copysign(1 - q, z),   GELU(z) = (z/2) * (1 + erf).
+// For z < 0 the sum 1 + erf is exact (Sterbenz) but inherits the rounding
+// of 1 - q (<= 2^-25), so the absolute error stays below 3e-8 |z| -- far
+// inside the normalised tolerances, whose scale is at least |z|.  The
+// reciprocal and 2^x are the hardware approximations (rcp.approx, ex2.approx,
+// relative error ~2^-22).  gelu_erf and gelu_erf2 perform the same operations
+// in the same order, so a value gets the same result from either.
+namespace gelu_c {
+constexpr float kRsqrt2 = 0.70710678118654752440f;
+constexpr float kP = 0.3275911f;
+constexpr float kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f, kA4 = -1.453152027f,
+                kA5 = 1.061405429f;
+constexpr float kNegLog2e = -1.44269504088896340736f;
+}  // namespace gelu_c
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ float gelu_erf(float z) {
-    return 0.5f * z * (1.0f + erff(z * 0.70710678118654752440f));
+    using namespace gelu_c;
+    const float x = fabsf(z) * kRsqrt2;
+    const float t = rcp_approx(fmaf(kP, x, 1.0f));
+    float poly = fmaf(kA5, t, kA4);
+    poly = fmaf(poly, t, kA3);
+    poly = fmaf(poly, t, kA2);
+    poly = fmaf(poly, t, kA1);
+    const float q = (poly * t) * ex2_approx((x * x) * kNegLog2e);
+    const float e = copysignf(fmaf(q, -1.0f, 1.0f), z);
+    return (0.5f * z) * (e + 1.0f);
+}
+
+// --- two fp32 lanes per instruction (Blackwell f32x2 arithmetic) -----------
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_splat(float c) { return f2_pack(c, c); }
+
+// GELU of two values at once; same operations as gelu_erf, lane by lane.
+__device__ __forceinline__ void gelu_erf2(float &z0, float &z1) {
+    using namespace gelu_c;
+    const uint64_t z = f2_pack(z0, z1);
+    const uint64_t x = f2_mul(z & 0x7FFFFFFF7FFFFFFFull, f2_splat(kRsqrt2));
+    const uint64_t d = f2_fma(f2_splat(kP), x, f2_splat(1.0f));
+    float d0, d1;
+    f2_unpack(d, d0, d1);
+    const uint64_t t = f2_pack(rcp_approx(d0), rcp_approx(d1));
+    uint64_t poly = f2_fma(f2_splat(kA5), t, f2_splat(kA4));
+    poly = f2_fma(poly, t, f2_splat(kA3));
+    poly = f2_fma(poly, t, f2_splat(kA2));
+    poly = f2_fma(poly, t, f2_splat(kA1));
+    const uint64_t u = f2_mul(f2_mul(x, x), f2_splat(kNegLog2e));
+    float u0, u1;
+    f2_unpack(u, u0, u1);
+    const uint64_t q = f2_mul(f2_mul(poly, t), f2_pack(ex2_approx(u0), ex2_approx(u1)));
+    const uint64_t omq = f2_fma(q, f2_splat(-1.0f), f2_splat(1.0f));
+    const uint64_t e = omq | (z & 0x8000000080000000ull);  // copysign(1 - q, z); 1 - q >= 0
+    const uint64_t y = f2_mul(f2_mul(f2_splat(0.5f), z), f2_add(e, f2_splat(1.0f)));
+    f2_unpack(y, z0, z1);
 }
 
 // Scalar epilogue of one element (used by the safe path and the SIMT kernel).
@@ -123,8 +215,12 @@ __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename E
                                                       const float *bias_chunk, const EpiParams &e) {
     constexpr int PV = Vec16<OUT>::kPerVec;
     constexpr int NV = 32 / PV;
+    const uint64_t alpha2 = f2_splat(e.alpha);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= e.alpha;
+    for (int j = 0; j < 32; j += 2) {
+        const uint64_t r = f2_mul(f2_pack(v[j], v[j + 1]), alpha2);
+        f2_unpack(r, v[j], v[j + 1]);
+    }
     if (e.beta != 0.0f) {
         const uint4 *src = reinterpret_cast<const uint4 *>(crow);
 #pragma unroll
@@ -144,7 +240,7 @@ __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename E
         }
         if (e.epilogue == kEpiBiasGelu) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+            for (int j = 0; j < 32; j += 2) gelu_erf2(v[j], v[j + 1]);
         }
     }
     uint4 *dst = reinterpret_cast<uint4 *>(crow);
@@ -162,6 +258,43 @@ __device__ __forceinline__ void epilogue_chunk32_safe(const float (&v)[32], type
             const float b = (e.epilogue != kEpiNone) ? e.bias[col0 + j] : 0.0f;
             epilogue_store_one<OUT>(v[j], crow + j, b, e);
         }
+    }
+}
+
+// One thread's share of a tile's epilogue: row `row` (its TMEM lane), chunks
+// 0 .. nvalid-1 of 32 columns starting at TMEM column address t_base and
+// output column col_base.  The TMEM load of chunk i+1 is in flight while chunk
+// i is processed.  Warp-collective (every lane calls it with the same t_base,
+// col_base and nvalid); nvalid <= MAXC.
+template <int OUT, int MAXC>
+__device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_base, int nvalid, int row, bool row_ok,
+                                                    const EpiParams &e) {
+    using OutT = typename Elem<OUT>::T;
+    if (nvalid <= 0) return;
+    OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
+    uint32_t ra[32], rb[32];
+    __syncwarp();
+    tmem_ld_issue(t_base, ra);
+    tmem_ld_wait(ra);
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+        if (i >= nvalid) break;  // warp-uniform
+        uint32_t(&cur)[32] = (i & 1) ? rb : ra;
+        uint32_t(&nxt)[32] = (i & 1) ? ra : rb;
+        const bool more = i + 1 < nvalid;
+        if (more) tmem_ld_issue(t_base + (i + 1) * 32, nxt);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(cur[j]);
+        const int col0 = col_base + i * 32;
+        if (row_ok) {
+            if (e.c_vec && col0 + 32 <= e.N)
+                epilogue_chunk32_fast<OUT>(v, crow + col0, e.bias + col0, e);
+            else
+                epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
+        }
+        __syncwarp();  // reconverge after the per-row store before the collective wait
+        if (more) tmem_ld_wait(nxt);
     }
 }
 

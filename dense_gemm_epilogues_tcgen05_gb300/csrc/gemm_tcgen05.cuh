@@ -95,7 +95,6 @@ __global__ void __launch_bounds__(TcConfig<AB, BN, STAGES>::THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const TcArgs args) {
     using Cfg = TcConfig<AB, BN, STAGES>;
-    using OutT = typename Elem<OUT>::T;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, SWZ = Cfg::SWZ;
 
     extern __shared__ unsigned char smem_raw[];
@@ -253,22 +252,11 @@ __global__ void __launch_bounds__(TcConfig<AB, BN, STAGES>::THREADS, 1)
             tc_fence_after();
             const int row = m0 + row_in_tile;
             const bool row_ok = row < M;
-            OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int col0 = n0 + c * 32;
-                if (col0 >= N) break;  // warp-uniform
-                float v[32];
-                __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the masked stores
-                tmem_ld_32cols(t_row + c * 32, v);
-                if (row_ok) {
-                    if (e.c_vec && col0 + 32 <= N)
-                        epilogue_chunk32_fast<OUT>(v, crow + col0, e.bias + col0, e);
-                    else
-                        epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
-                }
-            }
+            int nvalid = BN / 32;
+            const int left = (N - n0 + 31) >> 5;  // chunks that start inside the matrix
+            if (left < nvalid) nvalid = left;
+            epilogue_row_chunks<OUT, BN / 32>(t_row, n0, nvalid, row, row_ok, e);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);

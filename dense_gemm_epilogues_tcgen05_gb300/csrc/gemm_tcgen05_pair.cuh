@@ -66,7 +66,6 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const TcArgs args) {
     using Cfg = PairConfig<AB, STAGES>;
-    using OutT = typename Elem<OUT>::T;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, SWZ = Cfg::SWZ;
 
     extern __shared__ unsigned char smem_raw[];
@@ -236,23 +235,13 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
             if (__any_sync(0xffffffffu, !got)) break;
             tc_fence_after();
             const bool row_ok = row < M;
-            OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * Cfg::ACC_STRIDE;
-#pragma unroll 1
-            for (int c = c_begin; c < c_end; ++c) {
-                const int col0 = n_tile + c * 32;
-                if (col0 >= N) break;  // warp-uniform
-                float v[32];
-                __syncwarp();
-                tmem_ld_32cols(t_row + c * 32, v);
-                if (row_ok) {
-                    if (e.c_vec && col0 + 32 <= N)
-                        epilogue_chunk32_fast<OUT>(v, crow + col0, e.bias + col0, e);
-                    else
-                        epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
-                }
-            }
+            const int col_base = n_tile + c_begin * 32;
+            int nvalid = c_end - c_begin;
+            const int left = (N - col_base + 31) >> 5;  // chunks that start inside the matrix
+            if (left < nvalid) nvalid = left;
+            epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, e);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tempty0_leader + 8u * acc);

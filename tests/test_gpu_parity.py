@@ -259,3 +259,23 @@ def test_fp16_alpha_beta_2048_each_tiling(cuda_lib, tile_policy):
     res = r.check()
     assert res["pass"], res
     assert cuda_lib.gemm_device_status() == 0
+
+
+@pytest.mark.parametrize("ab", [wl.BF16, wl.F32], ids=["tcgen05", "simt"])
+def test_gelu_accuracy_over_range(cuda_lib, ab):
+    """z = bias exactly (the product is zero); fp32 output against float64 GELU."""
+    g = cuda_lib
+    M, N, K = 128, 4096, 64
+    a = torch.zeros(M, K)
+    b = torch.zeros(K, N)
+    bias = torch.linspace(-9.0, 9.0, N, dtype=torch.float32)
+    p = wl.make_problem("gelu_range", M, N, K, ab, wl.F32, a, b, alpha=1.0, beta=0.0, bias=bias,
+                        epilogue=wl.EPI_BIAS_GELU)
+    r = run_gemm(g, p)
+    assert r.path == (g.PATH_TCGEN05 if ab == wl.BF16 else g.PATH_SIMT)
+    got = r.values()
+    z = bias.double().numpy()
+    want = oracle.gelu(z)[None, :]
+    err = np.abs(got - want)
+    assert float(err.max()) <= 2e-7 * 9, float(err.max())
+    assert np.all(err <= 1e-7 + 4e-7 * np.abs(z)[None, :])
