@@ -152,6 +152,18 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm --
 
+_WS = {}
+
+
+def _workspace(g, device):
+    """The stream-K workspace (allocated once, outside any timed region)."""
+    import torch
+    key = str(device)
+    if key not in _WS:
+        _WS[key] = torch.empty(max(g.gemm_workspace_size(1, 1, 1, g.BF16), 256), dtype=torch.uint8, device=device)
+    return _WS[key]
+
+
 def _make_sets(problem, n_sets, device):
     sets = []
     for _ in range(n_sets):
@@ -162,8 +174,9 @@ def _make_sets(problem, n_sets, device):
 
 def _call(g, p, s, stream):
     A, B, C, bias = s
+    ws = _workspace(g, C.device)
     g.gemm(p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k, p.b_stride_n, C, p.ldc,
-           p.c_dtype, p.alpha, p.beta, bias, p.epilogue, stream=stream)
+           p.c_dtype, p.alpha, p.beta, bias, p.epilogue, workspace=ws, workspace_bytes=ws.numel(), stream=stream)
 
 
 def time_steps(g, p, sets, steps, warmup, stream, sampler=None, dist=None):
@@ -218,13 +231,15 @@ def e2e_measure(g, p, steps, stream):
     dA, dB, dC = torch.empty_like(hA, device=dev), torch.empty_like(hB, device=dev), torch.empty_like(hC, device=dev)
     hOut = torch.empty_like(hC).pin_memory()
     bias = None
+    ws = _workspace(g, dev)
 
     def step():
         dA.copy_(hA, non_blocking=True)
         dB.copy_(hB, non_blocking=True)
         dC.copy_(hC, non_blocking=True)
         g.gemm(p.M, p.N, p.K, p.ab_dtype, dA, p.a_stride_m, p.a_stride_k, dB, p.b_stride_k, p.b_stride_n, dC,
-               p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue, stream=stream)
+               p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue, workspace=ws, workspace_bytes=ws.numel(),
+               stream=stream)
         hOut.copy_(dC, non_blocking=True)
 
     with torch.cuda.stream(stream):

@@ -22,7 +22,8 @@ __all__ = [
     "PATH_NOOP", "PATH_EPILOGUE_ONLY", "PATH_TCGEN05", "PATH_SIMT",
     "TILE_AUTO", "TILE_1SM_256", "TILE_1SM_128", "TILE_PAIR",
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
-    "gemm_set_tile_policy", "gemm_query_tile",
+    "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K",
+    "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
 
@@ -34,6 +35,8 @@ EPI_NONE, EPI_BIAS, EPI_BIAS_GELU = 0, 1, 2
 PATH_NOOP, PATH_EPILOGUE_ONLY, PATH_TCGEN05, PATH_SIMT = 0, 1, 2, 3
 # gemm_tile_policy_t
 TILE_AUTO, TILE_1SM_256, TILE_1SM_128, TILE_PAIR = 0, 1, 2, 3
+# gemm_schedule_t
+SCHED_AUTO, SCHED_TILES, SCHED_STREAM_K = 0, 1, 2
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -62,6 +65,8 @@ lib.gemm_set_tile_policy.argtypes = [_int, _int]
 lib.gemm_query_tile.restype = _int
 lib.gemm_query_tile.argtypes = [_i64, _i64, _i64, _int, _int, ctypes.POINTER(_int), ctypes.POINTER(_int),
                                 ctypes.POINTER(_int)]
+lib.gemm_set_schedule.restype = _int
+lib.gemm_set_schedule.argtypes = [_int]
 lib.gemm_device_status.restype = _int
 lib.gemm_device_status.argtypes = [_vp]
 lib.gemm_status_string.restype = ctypes.c_char_p
@@ -139,6 +144,11 @@ def gemm_bias_gelu(M, N, C, ldc, c_dtype, bias, stream=None) -> int:
 def gemm_set_tile_policy(policy, bn=0) -> int:
     """Process-wide tile policy of the tcgen05 path (TILE_*); bn only with TILE_PAIR."""
     return _check(lib.gemm_set_tile_policy(policy, bn), "gemm_set_tile_policy")
+
+
+def gemm_set_schedule(schedule) -> int:
+    """Process-wide schedule of the pair kernel (SCHED_*)."""
+    return _check(lib.gemm_set_schedule(schedule), "gemm_set_schedule")
 
 
 def gemm_query_tile(M, N, K, ab_dtype, c_dtype):

@@ -240,6 +240,53 @@ gemm_status_t encode_operand(CUtensorMap *map, int ab, const void *base, const O
 
 std::atomic<int> g_tile_policy{GEMM_TILE_AUTO};
 std::atomic<int> g_tile_policy_bn{0};
+std::atomic<int> g_schedule{GEMM_SCHED_AUTO};
+std::atomic<unsigned int> g_epoch{0};
+
+// Stream-K workspace layout for `clusters` pairs: partial sums, then flags.
+size_t partial_bytes(int clusters) { return static_cast<size_t>(clusters) * 2 * kPartialFloatsPerCta * 4; }
+size_t workspace_bytes_for(int clusters) {
+    return partial_bytes(clusters) + ((static_cast<size_t>(clusters) * kFlagsPerCluster * 4 + 255) / 256) * 256;
+}
+
+unsigned int next_epoch() {
+    unsigned int e = g_epoch.fetch_add(1) + 1;
+    if (e == 0) e = g_epoch.fetch_add(1) + 1;  // 0 means "not ready"
+    return e;
+}
+
+// Schedule of the pair kernel: the tiles of the last one or two waves are
+// split over all clusters by k-block ranges (stream-K), the rest are whole
+// tiles, so every cluster ends at about the same time.  Measured on GB300 the
+// balance gain is small (the GPU runs near its power limit, so the SMs left
+// idle by a partial last wave let the busy ones clock up) and the fix-up
+// epilogues cost a fixed time per split tile, so the automatic mode uses it
+// only when (a) whole tiles alone would leave >= 10% of the cluster-time idle
+// in the last wave, (b) tiles are long (>= 48 k-blocks) and (c) at least one
+// wave of whole tiles remains for the fix-ups to hide behind.  Results:
+// bf16 / fp16 4096^3 +2%; fp8 4096^3 (32 k-blocks) and M=8192 bias+GELU
+// (3.8% idle) would lose 2-4% and keep whole tiles.  Stream-K always needs at
+// least 8 k-blocks per cluster.
+void choose_schedule(int64_t tiles, int num_kb, int max_clusters, bool have_ws, int mode, int *dp_tiles,
+                     long long *sk_units, int *clusters) {
+    *dp_tiles = static_cast<int>(tiles);
+    *sk_units = 0;
+    *clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
+    if (!have_ws || mode == GEMM_SCHED_TILES || max_clusters <= 0) return;
+    int64_t dp = 0;
+    if (mode != GEMM_SCHED_STREAM_K) {
+        if (tiles % max_clusters == 0) return;
+        const int64_t waves = tiles / max_clusters;
+        const double idle = 1.0 - static_cast<double>(tiles) / static_cast<double>((waves + 1) * max_clusters);
+        if (waves < 2 || num_kb < 48 || idle < 0.10) return;
+        dp = (waves - 1) * max_clusters;
+    }
+    const long long units = static_cast<long long>(tiles - dp) * num_kb;
+    if (units < 8LL * max_clusters) return;
+    *dp_tiles = static_cast<int>(dp);
+    *sk_units = units;
+    *clusters = max_clusters;
+}
 
 int pair_max_clusters_for(int ab, int cd) {
     switch (ab) {
@@ -368,15 +415,26 @@ gemm_status_t gemm_query_path(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_d
 }
 
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype) {
-    (void)M; (void)N; (void)K; (void)ab_dtype;
-    return 0;
+    (void)M; (void)N; (void)K;
+    if (ab_dtype != GEMM_F16 && ab_dtype != GEMM_BF16 && ab_dtype != GEMM_E4M3) return 0;
+    DeviceState *dev = nullptr;
+    if (device_state(&dev) != GEMM_OK) {
+        cudaGetLastError();
+        return 0;
+    }
+    return workspace_bytes_for(dev->num_sms / 2);
+}
+
+gemm_status_t gemm_set_schedule(gemm_schedule_t schedule) {
+    if (schedule < GEMM_SCHED_AUTO || schedule > GEMM_SCHED_STREAM_K) return GEMM_ERR_INVALID_ARG;
+    g_schedule.store(schedule);
+    return GEMM_OK;
 }
 
 gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const void *A, int64_t a_stride_m,
                    int64_t a_stride_k, const void *B, int64_t b_stride_k, int64_t b_stride_n, void *C, int64_t ldc,
                    gemm_dtype_t c_dtype, float alpha, float beta, const float *bias, gemm_epilogue_t epilogue,
                    void *workspace, size_t workspace_bytes, gemm_stream_t stream) {
-    (void)workspace; (void)workspace_bytes;
     Plan plan;
     gemm_status_t st = make_plan(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc,
                                  c_dtype, alpha, bias, epilogue, &plan);
@@ -434,9 +492,24 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     const uint32_t swz = 128u / es;
     const uint32_t b_bytes = plan.b.mn_major ? ((b_box + swz - 1) / swz) * 128u * bk : b_box * 128u;
     t.stage_tx = 128u * 128u + b_bytes;
+    t.dp_tiles = t.num_tiles;
+    t.sk_units = 0;
+    t.partial = nullptr;
+    t.flags = nullptr;
+    t.epoch = 0;
     cudaError_t err;
     if (tc.kind == 2) {
-        const int clusters = static_cast<int>(t.num_tiles < max_clusters ? t.num_tiles : max_clusters);
+        const bool have_ws = workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 &&
+                             workspace_bytes >= workspace_bytes_for(max_clusters);
+        int clusters = 0;
+        choose_schedule(t.num_tiles, t.num_kb, max_clusters, have_ws, g_schedule.load(), &t.dp_tiles,
+                        &t.sk_units, &clusters);
+        if (t.sk_units > 0) {
+            if ((st = check_range(workspace, workspace_bytes_for(max_clusters))) != GEMM_OK) return st;
+            t.partial = static_cast<float *>(workspace);
+            t.flags = reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + partial_bytes(max_clusters));
+            t.epoch = next_epoch();
+        }
         err = launch_pair(ab_dtype, c_dtype, ta, tb, t, clusters, s);
     } else {
         const int grid = static_cast<int>(t.num_tiles < dev->num_sms ? t.num_tiles : dev->num_sms);

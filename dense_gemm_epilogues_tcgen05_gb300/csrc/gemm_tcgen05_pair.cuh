@@ -61,6 +61,131 @@ __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, volati
     return false;
 }
 
+// ----------------------------------------------------------- schedule --
+// A cluster's work is a sequence of segments: (tile, k-blocks [kb_begin,
+// kb_end)).  First its piece [u0, u1) of the stream-K unit range (the k-blocks
+// of tiles dp_tiles .. num_tiles-1 in one line), cut at tile boundaries; then
+// whole tiles c, c + clusters, ... below dp_tiles.  Kinds: FULL (all k-blocks
+// of a tile), OWNER (starts at k-block 0 but stops early: later clusters hold
+// the rest), PART (starts inside a tile).  Since pieces are contiguous, only a
+// cluster's first segment can be a PART, so each cluster fills at most one
+// partial slot; the OWNER of a tile is the cluster whose piece holds its first
+// k-block (its last stream-K segment).  PARTs never wait on anything, OWNERs
+// wait only on PARTs of later clusters: no cycle.  Doing the stream-K piece
+// first lets the fix-up epilogues overlap the whole tiles' main loops, and
+// every cluster ends on an ordinary epilogue.
+enum SegKind { kSegFull = 0, kSegOwner = 1, kSegPart = 2 };
+
+struct Segment {
+    int tile, kb_begin, kb_end, kind;
+    long long sk_tile;  // index among the stream-K tiles (-1 for whole tiles)
+};
+
+struct SegmentIter {
+    int next_dp, nclusters, dp_tiles, num_kb;
+    long long u, u_end;
+    __device__ __forceinline__ SegmentIter(const TcArgs &a, int cluster, int nclusters_)
+        : next_dp(cluster), nclusters(nclusters_), dp_tiles(a.dp_tiles), num_kb(a.num_kb),
+          u(a.sk_units * cluster / nclusters_), u_end(a.sk_units * (cluster + 1) / nclusters_) {}
+    __device__ __forceinline__ bool next(Segment &s) {
+        if (u >= u_end) {
+            if (next_dp >= dp_tiles) return false;
+            s.tile = next_dp;
+            s.kb_begin = 0;
+            s.kb_end = num_kb;
+            s.kind = kSegFull;
+            s.sk_tile = -1;
+            next_dp += nclusters;
+            return true;
+        }
+        const long long t = u / num_kb;
+        const long long tile_end = (t + 1) * num_kb;
+        s.kb_begin = static_cast<int>(u - t * num_kb);
+        s.kb_end = static_cast<int>((u_end < tile_end ? u_end : tile_end) - t * num_kb);
+        s.tile = dp_tiles + static_cast<int>(t);
+        s.sk_tile = t;
+        s.kind = s.kb_begin != 0 ? kSegPart : (s.kb_end == num_kb ? kSegFull : kSegOwner);
+        u = t * num_kb + s.kb_end;
+        return true;
+    }
+};
+
+// Last cluster whose piece overlaps stream-K tile t: the one holding unit
+// (t + 1) * num_kb - 1, i.e. floor(((t+1)*num_kb*C - 1) / units).
+__device__ __forceinline__ int last_contributor(long long t, int num_kb, int nclusters, long long units) {
+    return static_cast<int>(((t + 1) * num_kb * nclusters - 1) / units);
+}
+
+// Index (in floats) of column group q (4 columns) of chunk ci, row r, inside
+// one CTA's partial slot: a warp's 32 rows of one group are 512 contiguous bytes.
+__device__ __forceinline__ long long partial_index(int ci, int q, int r) {
+    return ((static_cast<long long>(ci) * 8 + q) * 128 + r) * 4;
+}
+
+// PART epilogue: this thread's raw fp32 accumulators of chunks c0 .. c0+n-1 to
+// its cluster's partial slot (coalesced 16-byte stores, L2 only).
+__device__ __forceinline__ void store_partial_chunks(uint32_t t_base, int c0, int n, int r, float *slot) {
+    if (n <= 0) return;
+    uint32_t ra[32], rb[32];
+    __syncwarp();
+    tmem_ld_issue(t_base, ra);
+    tmem_ld_wait(ra);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (i >= n) break;
+        uint32_t(&cur)[32] = (i & 1) ? rb : ra;
+        uint32_t(&nxt)[32] = (i & 1) ? ra : rb;
+        const bool more = i + 1 < n;
+        if (more) tmem_ld_issue(t_base + (i + 1) * 32, nxt);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = make_float4(__uint_as_float(cur[4 * q]), __uint_as_float(cur[4 * q + 1]),
+                                         __uint_as_float(cur[4 * q + 2]), __uint_as_float(cur[4 * q + 3]));
+            __stcg(reinterpret_cast<float4 *>(slot + partial_index(c0 + i, q, r)), v);
+        }
+        __syncwarp();
+        if (more) tmem_ld_wait(nxt);
+    }
+}
+
+// OWNER epilogue: like epilogue_row_chunks, with the partial sums of
+// `ncontrib` later clusters (slots slot0, slot0 + slot_stride, ...) added to
+// the accumulators before alpha / beta / bias / GELU / cast.
+template <int OUT>
+__device__ __forceinline__ void owner_row_chunks(uint32_t t_base, int col_base, int c0, int nvalid, int row,
+                                                 bool row_ok, int r, const float *slot0, long long slot_stride,
+                                                 int ncontrib, const EpiParams &e) {
+    using OutT = typename Elem<OUT>::T;
+    OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
+#pragma unroll 1
+    for (int i = 0; i < nvalid; ++i) {
+        uint32_t raw[32];
+        __syncwarp();
+        tmem_ld_issue(t_base + i * 32, raw);
+        tmem_ld_wait(raw);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
+#pragma unroll 1
+        for (int k = 0; k < ncontrib; ++k) {
+            const float *src = slot0 + k * slot_stride;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + partial_index(c0 + i, q, r)));
+                v[4 * q] += p.x; v[4 * q + 1] += p.y; v[4 * q + 2] += p.z; v[4 * q + 3] += p.w;
+            }
+        }
+        const int col0 = col_base + i * 32;
+        if (row_ok) {
+            if (e.c_vec && col0 + 32 <= e.N)
+                epilogue_chunk32_fast<OUT>(v, crow + col0, e.bias + col0, e);
+            else
+                epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
+        }
+    }
+    __syncwarp();
+}
+
 template <int AB, int OUT, int STAGES>
 __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -123,12 +248,14 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
             // ------------------------------------------------ TMA producer --
             uint32_t stage = 0, phase = 0;
             bool ok = true, issued = false;
-            for (int tile = cluster; ok && tile < args.num_tiles; tile += nclusters) {
+            SegmentIter it(args, cluster, nclusters);
+            Segment seg;
+            while (ok && it.next(seg)) {
                 int tm, tn;
-                tile_coords(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
+                tile_coords(seg.tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
                 const int m0 = tm * 2 * BM + static_cast<int>(rank) * BM;
                 const int n0 = tn * bn + static_cast<int>(rank) * bnh;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
                     if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, args.status, peer_abort)) {
                         ok = false;
                         break;
@@ -182,12 +309,14 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true, issued = false;
             int local = 0;
-            for (int tile = cluster; ok && tile < args.num_tiles; tile += nclusters, ++local) {
+            SegmentIter it(args, cluster, nclusters);
+            Segment seg;
+            for (; ok && it.next(seg); ++local) {
                 const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
                 if (!pair_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, args.status, peer_abort)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * Cfg::ACC_STRIDE;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
                     if (!pair_wait(&full[stage], phase, abort_flag, args.status, peer_abort)) {
                         ok = false;
                         break;
@@ -199,7 +328,8 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
                     for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
                         const uint64_t ad = sw128_desc(a_addr + ks * a_kstep, a_lbo, 1024u);
                         const uint64_t bd = sw128_desc(b_addr + ks * b_kstep, b_lbo, 1024u);
-                        tc_mma_pair<TcTraits<AB>::kKind>(d_tmem, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+                        tc_mma_pair<TcTraits<AB>::kKind>(d_tmem, ad, bd, idesc,
+                                                          (kb != seg.kb_begin || ks != 0) ? 1u : 0u);
                     }
                     issued = true;
                     tc_commit_pair(&empty[stage], 0x3);
@@ -224,12 +354,15 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
         const int c_begin = half ? (nchunks + 1) >> 1 : 0;
         const int c_end = half ? nchunks : (nchunks + 1) >> 1;
         const EpiParams &e = args.e;
+        const int r = quad * 32 + lane;  // this thread's row inside the CTA's 128
         int local = 0;
-        for (int tile = cluster; tile < args.num_tiles; tile += nclusters, ++local) {
+        SegmentIter it(args, cluster, nclusters);
+        Segment seg;
+        for (; it.next(seg); ++local) {
             const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
             int tm, tn;
-            tile_coords(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
-            const int row = tm * 2 * BM + static_cast<int>(rank) * BM + quad * 32 + lane;
+            tile_coords(seg.tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
+            const int row = tm * 2 * BM + static_cast<int>(rank) * BM + r;
             const int n_tile = tn * bn;
             const bool got = pair_wait(&tfull[acc], acc_phase, abort_flag, args.status, peer_abort);
             if (__any_sync(0xffffffffu, !got)) break;
@@ -241,7 +374,34 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
             int nvalid = c_end - c_begin;
             const int left = (N - col_base + 31) >> 5;  // chunks that start inside the matrix
             if (left < nvalid) nvalid = left;
-            epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, e);
+            bool fail = false;
+            if (seg.kind == kSegFull) {
+                epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, e);
+            } else if (seg.kind == kSegPart) {
+                float *slot = args.partial + (static_cast<long long>(cluster) * 2 + rank) * kPartialFloatsPerCta;
+                store_partial_chunks(t_row + c_begin * 32, c_begin, nvalid, r, slot);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(&args.flags[(cluster * 2 + rank) * 8 + ew], args.epoch);
+            } else {
+                const int c_last = last_contributor(seg.sk_tile, num_kb, nclusters, args.sk_units);
+                const int ncontrib = c_last - cluster;
+                for (int k = 1; k <= ncontrib && !fail; ++k) {
+                    const unsigned int *f = &args.flags[((cluster + k) * 2 + rank) * 8 + ew];
+                    fail = !flag_wait_bounded(f, args.epoch, abort_flag, args.status);
+                }
+                if (__any_sync(0xffffffffu, fail)) {
+                    st_shared_cluster_u32(peer_abort, 1u);
+                    break;
+                }
+                const float *slot0 =
+                    args.partial + (static_cast<long long>(cluster + 1) * 2 + rank) * kPartialFloatsPerCta;
+                owner_row_chunks<OUT>(t_row + c_begin * 32, col_base, c_begin, nvalid, row, row_ok, r, slot0,
+                                      2 * kPartialFloatsPerCta, ncontrib, e);
+                __syncwarp();
+                if (lane == 0)
+                    for (int k = 1; k <= ncontrib; ++k) args.flags[((cluster + k) * 2 + rank) * 8 + ew] = 0u;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tempty0_leader + 8u * acc);

@@ -33,7 +33,20 @@ struct TcArgs {
     unsigned int *status;             // device status word (timeouts)
     int bn;                           // pair kernel: tile width (multiple of 32, <= 256)
     uint32_t stage_tx;                // pair kernel: bytes one CTA's loads deliver per stage
+    // Pair kernel schedule.  Tiles [0, dp_tiles) are computed whole, cluster c
+    // taking c, c + clusters, ...; the k-blocks of tiles [dp_tiles, num_tiles)
+    // form one range of sk_units = (num_tiles - dp_tiles) * num_kb units that
+    // is cut into `clusters` contiguous pieces (stream-K).
+    int dp_tiles;
+    long long sk_units;
+    float *partial;                   // stream-K: per cluster, 2 CTAs x 128 x 256 fp32 partial sums
+    unsigned int *flags;              // stream-K: per cluster, 2 CTAs x 8 epilogue warps
+    unsigned int epoch;               // stream-K: value a flag takes when its partial is ready (never 0)
 };
+
+// Floats of stream-K partial sums one CTA of a cluster writes, and flags per cluster.
+constexpr long long kPartialFloatsPerCta = 128LL * 256LL;
+constexpr int kFlagsPerCluster = 2 * 8;
 
 // SIMT path: operands as (pointer, stride) views, any strides.
 struct SimtArgs {

@@ -329,4 +329,36 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t cta_mask)
         : "memory");
 }
 
+
+// ------------------------------------------- flags between clusters (gpu) --
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned int *p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until *p == want (acquire).  Gives up like mbar_wait_bounded.
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned int *p, unsigned int want, volatile int *abort_flag,
+                                                  unsigned int *status) {
+    if (ld_acquire_gpu(p) == want) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        sleep_ns(64);
+        if (ld_acquire_gpu(p) == want) return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 }  // namespace gb300

@@ -103,9 +103,13 @@ typedef enum {
  *   epilogue       GEMM_EPI_NONE, GEMM_EPI_BIAS or GEMM_EPI_BIAS_GELU; the
  *                  order is z = alpha*AB + beta*C + bias, then GELU, then cast
  *                  (round to nearest even).
- *   workspace      device scratch of at least gemm_workspace_size(...) bytes,
- *   workspace_bytes  or NULL / 0 when that size is 0 (it is 0 for every
- *                  configuration today).
+ *   workspace      optional device scratch, 256-byte aligned, owned by the
+ *   workspace_bytes  caller: with at least gemm_workspace_size(...) bytes the
+ *                  last waves of output tiles are split along K over all SM
+ *                  pairs (stream-K: partial sums go through the workspace);
+ *                  with less, or NULL / 0, whole tiles only.  Calls that share
+ *                  a workspace must not run concurrently.  Its contents need no
+ *                  initialisation (each call tags its flags with a fresh value).
  *   stream         CUDA stream the work is enqueued on.
  *
  * Aliasing: C must not overlap A, B or bias.  Returns GEMM_OK once enqueued.
@@ -121,10 +125,28 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K,
                    gemm_stream_t stream);
 
 /*
- * gemm_workspace_size -- bytes of device scratch gemm() needs for this shape
- * and input type (0 today for every configuration).  Never fails.
+ * gemm_workspace_size -- bytes of device scratch that let gemm() use the
+ * stream-K schedule on the current device: 256 KB of partial sums and 64
+ * bytes of flags per pair of SMs (about 19 MB on a 152-SM GB300), 0 for fp32
+ * inputs or when the device cannot be queried.  The size does not depend on
+ * M, N, K.  Never fails.
  */
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype);
+
+/* How the tcgen05 pair kernel distributes tiles (process-wide). */
+typedef enum {
+    GEMM_SCHED_AUTO = 0,     /* stream-K for the last waves when the tiles do not divide evenly */
+    GEMM_SCHED_TILES = 1,    /* whole tiles only */
+    GEMM_SCHED_STREAM_K = 2  /* every tile's k-blocks in one range split over all SM pairs */
+} gemm_schedule_t;
+
+/*
+ * gemm_set_schedule -- schedule of later gemm() calls on the pair kernel, for
+ * every thread of the process (stream-K still needs a large enough
+ * workspace).  Meant for tuning and tests.  GEMM_ERR_INVALID_ARG for an
+ * unknown value; never touches the device.
+ */
+gemm_status_t gemm_set_schedule(gemm_schedule_t schedule);
 
 /*
  * gemm_query_path -- validate the same arguments gemm() takes and report, in

@@ -37,7 +37,8 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     assert {"gemm", "gemm_workspace_size", "gemm_query_path", "gemm_bias_gelu", "gemm_device_status",
-            "gemm_status_string", "gemm_version", "gemm_set_tile_policy", "gemm_query_tile"} <= names
+            "gemm_status_string", "gemm_version", "gemm_set_tile_policy", "gemm_query_tile",
+            "gemm_set_schedule"} <= names
 
 
 def test_library_exports_every_declared_symbol(g):
@@ -53,9 +54,19 @@ def test_status_strings_and_version(g):
     assert "sm_103a" in g.gemm_version()
 
 
-def test_workspace_is_zero(g):
+def test_workspace_size_without_gpu(g):
+    # fp32 inputs never need one; without a device the size cannot be known: 0
     assert g.gemm_workspace_size(4096, 4096, 4096, g.F32) == 0
-    assert g.gemm_workspace_size(4096, 4096, 4096, g.BF16) == 0
+    assert g.gemm_workspace_size(4096, 4096, 4096, g.BF16) >= 0
+
+
+def test_schedule_validation(g):
+    for v in (0, 1, 2):
+        assert g.gemm_set_schedule(v) == 0
+    for v in (-1, 3):
+        with pytest.raises(g.GemmError):
+            g.gemm_set_schedule(v)
+    g.gemm_set_schedule(g.SCHED_AUTO)
 
 
 # Fake, aligned device addresses: query_path never dereferences them.

@@ -279,3 +279,63 @@ def test_gelu_accuracy_over_range(cuda_lib, ab):
     err = np.abs(got - want)
     assert float(err.max()) <= 2e-7 * 9, float(err.max())
     assert np.all(err <= 1e-7 + 4e-7 * np.abs(z)[None, :])
+
+
+# ---------------------------------------------------------------- stream-K --
+
+@pytest.fixture
+def schedule(cuda_lib, request):
+    cuda_lib.gemm_set_schedule(request.param)
+    yield request.param
+    cuda_lib.gemm_set_schedule(cuda_lib.SCHED_AUTO)
+
+
+SK_SHAPES = [(256, 256, 1024), (512, 768, 4096), (336, 208, 3008), (1024, 1024, 2048), (128, 4096, 1024)]
+
+
+@pytest.mark.parametrize("schedule", [2], indirect=True, ids=["streamk"])
+@pytest.mark.parametrize("shape", SK_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layout", ["NN", "TT"])
+@pytest.mark.parametrize("ab", [wl.BF16, wl.E4M3], ids=["bf16", "e4m3"])
+def test_integer_exact_stream_k(cuda_lib, ab, layout, shape, schedule):
+    """Every tile's k-blocks split over all SM pairs: partial sums through the
+    workspace must reproduce the exact integer result (sums < 2^24)."""
+    M, N, K = shape
+    p = wl.random_problem(500 + M + K, M, N, K, ab, wl.F32, layout=layout, alpha=2.0, beta=-1.0,
+                          integer=True)
+    r = run_gemm(cuda_lib, p)
+    assert r.status == 0 and r.path == cuda_lib.PATH_TCGEN05
+    _assert_exact(r)
+
+
+@pytest.mark.parametrize("schedule", [0, 1, 2], indirect=True, ids=["auto", "tiles", "streamk"])
+@pytest.mark.parametrize("epi", [wl.EPI_NONE, wl.EPI_BIAS_GELU], ids=["none", "gelu"])
+def test_schedules_agree(cuda_lib, epi, schedule):
+    """Random data, every schedule within tolerance; whole-tile vs stream-K sums
+    differ only in the order of fp32 additions."""
+    p = wl.random_problem(77, 1536, 1280, 2048, wl.BF16, wl.F32, alpha=0.5, beta=0.0, epilogue=epi)
+    r = run_gemm(cuda_lib, p)
+    res = r.check()
+    assert res["pass"], res
+
+
+def test_stream_k_repeated_calls_and_no_workspace(cuda_lib):
+    """Flags reset after use: back-to-back stream-K calls on one workspace stay
+    correct, and a call without workspace falls back to whole tiles."""
+    g = cuda_lib
+    g.gemm_set_schedule(g.SCHED_STREAM_K)
+    try:
+        p = wl.random_problem(88, 640, 512, 1536, wl.F16, wl.F32, alpha=1.0, beta=1.0, integer=True)
+        for _ in range(3):
+            _assert_exact(run_gemm(g, p))
+        _assert_exact(run_gemm(g, p, use_workspace=False))
+    finally:
+        g.gemm_set_schedule(g.SCHED_AUTO)
+
+
+def test_workspace_size(cuda_lib):
+    g = cuda_lib
+    n = g.gemm_workspace_size(4096, 4096, 4096, g.F16)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert n >= (sms // 2) * 2 * 128 * 256 * 4
+    assert g.gemm_workspace_size(4096, 4096, 4096, g.F32) == 0
