@@ -23,7 +23,7 @@ __all__ = [
     "TILE_AUTO", "TILE_1SM_256", "TILE_1SM_128", "TILE_PAIR",
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K",
-    "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule",
+    "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
 
@@ -65,6 +65,9 @@ lib.gemm_set_tile_policy.argtypes = [_int, _int]
 lib.gemm_query_tile.restype = _int
 lib.gemm_query_tile.argtypes = [_i64, _i64, _i64, _int, _int, ctypes.POINTER(_int), ctypes.POINTER(_int),
                                 ctypes.POINTER(_int)]
+lib.gemm_builtin_scratch.restype = _int
+lib.gemm_builtin_scratch.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _int,
+                                     _f32, _f32, _vp, _int, _vp]
 lib.gemm_set_schedule.restype = _int
 lib.gemm_set_schedule.argtypes = [_int]
 lib.gemm_device_status.restype = _int
@@ -118,6 +121,17 @@ def gemm(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n
                   _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue, _ptr(workspace), workspace_bytes,
                   _stream(stream))
     return _check(st, "gemm")
+
+
+def gemm_builtin_scratch(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc,
+                         c_dtype, alpha, beta, bias, epilogue, stream=None) -> int:
+    """gemm() without a workspace argument, for callers that cannot allocate device
+    memory: the stream-K scratch comes from the library's fixed device array (see
+    include/gemm_gb300.h for its size and the rules on overlapping calls)."""
+    st = lib.gemm_builtin_scratch(M, N, K, ab_dtype, _ptr(A), a_stride_m, a_stride_k, _ptr(B), b_stride_k,
+                                  b_stride_n, _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue,
+                                  _stream(stream))
+    return _check(st, "gemm_builtin_scratch")
 
 
 def gemm_query_path(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc, c_dtype,

@@ -192,6 +192,42 @@ gemm_status_t gemm_query_tile(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_d
                               int *kind, int *bn, int *units);
 
 /*
+ * gemm_builtin_scratch -- gemm() for callers that cannot allocate device
+ * memory.  (The pages have no counterpart: this is a deployment convenience
+ * of this library, not part of the method.)
+ *
+ * gemm() takes the stream-K scratch (partial sums and ready flags) from a
+ * workspace the caller allocates.  Code that cannot call cudaMalloc or any
+ * allocating routine where it multiplies -- inside CUDA stream capture, on
+ * real-time paths, or in processes whose device memory belongs to another
+ * allocator -- calls this instead: same arguments and result as gemm()
+ * without the workspace pair, with the scratch taken from a fixed array of
+ * 20,976,640 bytes (enough for 80 pairs of SMs) that the library reserves in
+ * device memory on every device that loads it, for as long as it is loaded.
+ * It allocates nothing.
+ *
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; nothing
+ *     in it needs clearing between calls.  Calls that overlap on the GPU (on
+ *     different streams, or from different threads) race on it: serialise
+ *     them.
+ *   - A device with more than 80 pairs of SMs needs a larger stream-K
+ *     workspace than the array holds: such calls return GEMM_ERR_WORKSPACE
+ *     (use gemm() with a workspace there).
+ *   - Other errors as gemm().
+ */
+gemm_status_t gemm_builtin_scratch(int64_t M, int64_t N, int64_t K,
+                                   gemm_dtype_t ab_dtype,
+                                   const void *A, int64_t a_stride_m, int64_t a_stride_k,
+                                   const void *B, int64_t b_stride_k, int64_t b_stride_n,
+                                   void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                                   float alpha, float beta,
+                                   const float *bias, gemm_epilogue_t epilogue,
+                                   gemm_stream_t stream);
+
+/*
  * gemm_bias_gelu -- the UNFUSED second pass, for measuring what fusion saves
  * (Rigel abstract: fused GEMM + bias + GELU against the decomposed path):
  * C[i][j] = cast(GELU(C[i][j] + bias[j])) in place, for an M x N block of an
