@@ -319,6 +319,9 @@ def run_ours(a):
     peaks = measured_peaks()
     avg_ms = sum(per) / len(per)
     achieved = p.flops / (avg_ms * 1e-3) / 1e12
+    kind, bn, units = g.gemm_query_tile(p.M, p.N, p.K, p.ab_dtype, p.c_dtype)
+    kernel = (f"gemm_tcgen05_pair_kernel<f16,f16> 256x{bn} tiles on {units} SM pairs" if kind == 2 else
+              f"gemm_tcgen05_kernel<f16,f16,{bn}> 128x{bn} tiles on {units} SMs")
     traffic = recorded_traffic("tcgen05_f16_4096")
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
@@ -332,7 +335,7 @@ def run_ours(a):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 burst (fp16 runs at the bf16 rate)",
-                     "kernel": "gemm_tcgen05_kernel<f16,f16,256,4>"},
+                     "kernel": kernel},
         "clocks": sampler.summary(),
         "gpu_launches": a.steps,
     }
@@ -360,7 +363,8 @@ def extra_cells(g, stream):
     cells["fp8_over_fp16"] = round(cells["fp8_4096_bf16out"]["median_tflops"] /
                                    cells["fp16_twin_4096_bf16out"]["median_tflops"], 3)
     cells["bf16_8192_nn"] = cell(g, wl.bf16_nn_large(8192), 10, 3, stream, n_sets=2)
-    for M in (2048, 8192):
+    cells["fp32_4096_NN_simt"] = cell(g, wl.fp32_layout("NN", 4096), 5, 2, stream, n_sets=2)
+    for M in (512, 2048, 8192):
         fused = cell(g, wl.bf16_bias_gelu(M), 30, 5, stream)
         plain = cell(g, wl.bf16_bias_gelu(M, epilogue=wl.EPI_NONE), 30, 5, stream)
         cells[f"gelu_M{M}"] = {"fused": fused, "none": plain,
