@@ -94,6 +94,20 @@ def recorded_traffic(kernel_tag):
     return None
 
 
+def aggregate(local_seconds, flops_per_step, steps, dist=None, device="cpu"):
+    """Whole-job throughput: every rank ran `steps` steps of `flops_per_step`;
+    the job's time is the slowest rank's.  Returns (TFLOP/s, max seconds)."""
+    import torch
+    world = 1
+    t = float(local_seconds)
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        x = torch.tensor([t], dtype=torch.float64, device=device)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        t = float(x.item())
+    return flops_per_step * steps * world / t / 1e12, t
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -131,8 +145,14 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.tmp.flush()
         with open(self.tmp.name) as f:
-            rows = [r.split(",") for r in f.read().strip().splitlines() if r.strip()]
+            text = f.read()
         os.unlink(self.tmp.name)
+        return self.parse(text)
+
+    @staticmethod
+    def parse(text):
+        """Summary of nvidia-smi CSV rows (the FIELDS order, no header, no units)."""
+        rows = [r.split(",") for r in text.strip().splitlines() if r.strip()]
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -308,12 +328,7 @@ def run_ours(a):
     st = g.gemm_device_status()
     if st != 0:
         raise RuntimeError(f"device status after timing: {g.gemm_status_string(st)}")
-    total_s = total * 1e-3
-    if dist is not None:
-        t = torch.tensor([total_s], device=dev)
-        dist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = p.flops * a.steps * world / total_s / 1e12
+    value, total_s = aggregate(total * 1e-3, p.flops, a.steps, dist, dev)
     tf = [p.flops / (t * 1e-3) / 1e12 for t in per]
     med, ci = bootstrap_ci(tf)
     peaks = measured_peaks()

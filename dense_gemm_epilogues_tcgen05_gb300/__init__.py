@@ -23,7 +23,7 @@ __all__ = [
     "TILE_AUTO", "TILE_1SM_256", "TILE_1SM_128", "TILE_PAIR",
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K",
-    "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch",
+    "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
 
@@ -68,6 +68,8 @@ lib.gemm_query_tile.argtypes = [_i64, _i64, _i64, _int, _int, ctypes.POINTER(_in
 lib.gemm_builtin_scratch.restype = _int
 lib.gemm_builtin_scratch.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _int,
                                      _f32, _f32, _vp, _int, _vp]
+lib.gemm_wait_selftest.restype = _int
+lib.gemm_wait_selftest.argtypes = [_vp, ctypes.c_uint64, _vp]
 lib.gemm_set_schedule.restype = _int
 lib.gemm_set_schedule.argtypes = [_int]
 lib.gemm_device_status.restype = _int
@@ -177,6 +179,11 @@ def gemm_query_tile(M, N, K, ab_dtype, c_dtype):
 def gemm_device_status(stream=None) -> int:
     """Synchronise the stream; return (and clear) the device status as a gemm_status_t code."""
     return int(lib.gemm_device_status(_stream(stream)))
+
+
+def gemm_wait_selftest(never_set, limit_ns, stream=None) -> int:
+    """Run the bounded-wait self-test (see include/gemm_gb300.h); then gemm_device_status()."""
+    return _check(lib.gemm_wait_selftest(_ptr(never_set), limit_ns, _stream(stream)), "gemm_wait_selftest")
 
 
 def gemm_status_string(status: int) -> str:

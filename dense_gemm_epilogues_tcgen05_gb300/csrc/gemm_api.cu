@@ -559,6 +559,19 @@ gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dt
                                                                                                 : GEMM_ERR_CUDA;
 }
 
+gemm_status_t gemm_wait_selftest(const unsigned int *never_set, uint64_t limit_ns, gemm_stream_t stream) {
+    if (never_set == nullptr || limit_ns == 0 || limit_ns > 1000000000ull) return GEMM_ERR_INVALID_ARG;
+    if (!driver_fns().ok) return GEMM_ERR_CUDA;
+    DeviceState *dev = nullptr;
+    gemm_status_t st = device_state(&dev);
+    if (st != GEMM_OK) return st;
+    if ((st = check_range(never_set, sizeof(unsigned int))) != GEMM_OK) return st;
+    return launch_wait_selftest(never_set, limit_ns, dev->status, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_CUDA;
+}
+
 gemm_status_t gemm_device_status(gemm_stream_t stream) {
     DeviceState *dev = nullptr;
     gemm_status_t st = device_state(&dev);

@@ -9,8 +9,11 @@
 //   * epilogue_only_kernel: K == 0 or alpha == 0 (C = epilogue(beta*C + bias)).
 //   * bias_gelu_kernel: the unfused bias+GELU pass over a finished GEMM output,
 //     used only to measure what fusing saves (Rigel, abstract and section 1).
+//   * wait_selftest_kernel: runs the bounded waits of the GEMM kernels against
+//     events that never happen, so tests can see them give up and report.
 #include "epilogue.cuh"
 #include "kernel_args.h"
+#include "sm103_ptx.cuh"
 
 namespace gb300 {
 
@@ -116,6 +119,27 @@ __global__ void bias_gelu_kernel(const EpiParams e) {
     }
 }
 
+// One warp: lane 0 waits on an mbarrier that nobody arrives at, then on a
+// global flag that nobody sets, each for at most limit_ns; each wait that gives
+// up records a timeout in the status word.  Returns in about 2 * limit_ns.
+__global__ void wait_selftest_kernel(const unsigned int *never_set, unsigned long long limit_ns,
+                                     unsigned int *status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile int *ab = &abort_flag;
+        mbar_wait_bounded(&bar, 0, ab, status, limit_ns);
+        *ab = 0;
+        flag_wait_bounded(never_set, 0xFFFFFFFFu, ab, status, limit_ns);
+    }
+}
+
 int elementwise_grid(long long total, int threads) {
     long long blocks = (total + threads - 1) / threads;
     const long long cap = 152LL * 16;  // a few waves over the SMs; the loops are grid-stride
@@ -158,6 +182,12 @@ cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t s) {
     case kDtBF16: epilogue_only_kernel<kDtBF16><<<grid, threads, 0, s>>>(e); break;
     default: return cudaErrorInvalidValue;
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(const unsigned int *never_set, unsigned long long limit_ns, unsigned int *status,
+                                 cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(never_set, limit_ns, status);
     return cudaGetLastError();
 }
 

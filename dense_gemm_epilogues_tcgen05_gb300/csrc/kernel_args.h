@@ -80,5 +80,7 @@ int pair_max_clusters_e4m3(int out);
 cudaError_t launch_simt(int ab, int out, const SimtArgs &args, cudaStream_t stream);
 cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t stream);
 cudaError_t launch_bias_gelu(int out, const EpiParams &e, cudaStream_t stream);
+cudaError_t launch_wait_selftest(const unsigned int *never_set, unsigned long long limit_ns, unsigned int *status,
+                                 cudaStream_t stream);
 
 }  // namespace gb300

@@ -69,7 +69,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 // role of the CTA has raised `abort_flag`, or after kWaitLimitNs, in which
 // case it raises the flag itself and records a timeout in `status`.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                                  unsigned int *status) {
+                                                  unsigned int *status,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     const uint32_t addr = smem_u32(bar);
     if (mbar_try_wait(addr, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
@@ -77,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (mbar_try_wait(addr, parity)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(status, kStatusTimeout);
                 return false;
@@ -344,7 +345,8 @@ __device__ __forceinline__ void st_release_gpu(unsigned int *p, unsigned int v) 
 
 // Bounded wait until *p == want (acquire).  Gives up like mbar_wait_bounded.
 __device__ __forceinline__ bool flag_wait_bounded(const unsigned int *p, unsigned int want, volatile int *abort_flag,
-                                                  unsigned int *status) {
+                                                  unsigned int *status,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (ld_acquire_gpu(p) == want) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -352,7 +354,7 @@ __device__ __forceinline__ bool flag_wait_bounded(const unsigned int *p, unsigne
         if (ld_acquire_gpu(p) == want) return true;
         if ((it & 15u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(status, kStatusTimeout);
                 return false;

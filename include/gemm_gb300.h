@@ -245,6 +245,17 @@ gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dt
  */
 gemm_status_t gemm_device_status(gemm_stream_t stream);
 
+/*
+ * gemm_wait_selftest -- exercise the bounded waits the GEMM kernels rely on
+ * instead of hanging.  Enqueues on `stream` a one-warp kernel that waits on an
+ * mbarrier nobody arrives at and then on *never_set (a device word the caller
+ * guarantees nobody sets to 0xFFFFFFFF during the call), each for at most
+ * limit_ns nanoseconds (1 .. 1e9).  Each wait that gives up records a timeout,
+ * so the next gemm_device_status() returns GEMM_ERR_TIMEOUT; the CUDA context
+ * stays usable.  (Failure-detection aid; the pages have no counterpart.)
+ */
+gemm_status_t gemm_wait_selftest(const unsigned int *never_set, uint64_t limit_ns, gemm_stream_t stream);
+
 /* gemm_status_string -- static, NUL-terminated description of a status code. */
 const char *gemm_status_string(gemm_status_t status);
 

@@ -38,7 +38,7 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     assert {"gemm", "gemm_workspace_size", "gemm_query_path", "gemm_bias_gelu", "gemm_device_status",
             "gemm_status_string", "gemm_version", "gemm_set_tile_policy", "gemm_query_tile",
-            "gemm_set_schedule"} <= names
+            "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest"} <= names
 
 
 def test_library_exports_every_declared_symbol(g):

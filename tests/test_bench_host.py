@@ -1,0 +1,108 @@
+"""bench.py host logic (CPU only): statistics, clock records, traffic lookup,
+the reference arm's JSON line, and the multi-rank aggregation under gloo."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+from conftest import REPO
+
+sys.path.insert(0, REPO)
+import bench  # noqa: E402
+
+
+def test_bootstrap_ci_brackets_the_median():
+    rng = np.random.default_rng(1)
+    x = rng.normal(100.0, 1.0, size=300)
+    med, (lo, hi) = bench.bootstrap_ci(x)
+    assert med == pytest.approx(float(np.median(x)))
+    assert lo <= med <= hi and hi - lo < 0.5
+    # fixed seed: the same samples give the same interval
+    assert bench.bootstrap_ci(x) == (med, [lo, hi])
+
+
+def test_bootstrap_ci_bimodal_is_wide():
+    x = np.concatenate([np.full(145, 4.65), np.full(155, 6.5)])
+    med, (lo, hi) = bench.bootstrap_ci(x)
+    assert lo < 5.0 < hi or (lo == hi == 6.5)
+
+
+def test_clock_record_parsing():
+    text = "\n".join([
+        "2070, 2070, 120.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "1890, 2070, 1200.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "1900, 2070, 1250.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+    ])
+    s = bench.ClockSampler.parse(text)
+    assert s["sm_max_mhz"] == 2070.0
+    assert s["sm_mhz"] == pytest.approx(1895.0)   # median of the samples under load
+    assert s["reasons"] == ["sw_power_cap"]
+    bad = bench.ClockSampler.parse("1500, 2070, 900, 0x8, Active, Not Active, Not Active, Not Active")
+    assert "hw_slowdown" in bad["reasons"]
+
+
+def test_measured_peaks_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "REPO", str(tmp_path))
+    p = bench.measured_peaks()
+    assert p["source"] == "fallback" and p["bf16_tflops"] == 1900.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"bf16_tflops": 1954.3, "bf16_tflops_sustained": 1749.8, "hbm_gbs": 6655.6}))
+    p = bench.measured_peaks()
+    assert p["source"] == "measured" and p["bf16_tflops"] == 1954.3
+
+
+def test_traffic_record_matches_only_current_sources(tmp_path, monkeypatch):
+    import __graft_entry__
+    fp = __graft_entry__.build_module().source_fingerprint()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.tsv").write_text(
+        f"# comment\n0000000000000000\ttagA\t1\told kernel\n{fp}\ttagA\t12345\tnow\n")
+    monkeypatch.setattr(bench, "REPO", str(tmp_path))
+    assert bench.recorded_traffic("tagA") == 12345.0
+    assert bench.recorded_traffic("tagB") is None
+
+
+def test_aggregate_single_rank():
+    v, t = bench.aggregate(2.0, 1e12, 10)
+    assert t == 2.0 and v == pytest.approx(5.0)
+
+
+def _agg_worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    v, t = bench.aggregate(1.0 + rank, 1e12, 4, dist)
+    out[rank] = (v, t)
+    dist.destroy_process_group()
+
+
+def test_aggregate_two_ranks_takes_the_slowest():
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_agg_worker, args=(2, port, out), nprocs=2, join=True)
+    for r in range(2):
+        v, t = out[r]
+        assert t == 2.0                       # max over ranks
+        assert v == pytest.approx(2 * 4 * 1e12 / 2.0 / 1e12)  # both ranks' work over that time
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(REPO, "bench.py"), "--impl", "reference", "--steps", "2",
+                        "--warmup", "1", "--size", "256", "--cpu-seconds", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=REPO)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "config", "cpu_baseline", "e2e", "impl"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0

@@ -224,6 +224,24 @@ def test_deterministic(cuda_lib):
     assert np.array_equal(a, b)
 
 
+def test_bounded_waits_give_up_and_report(cuda_lib):
+    """A wait that can never complete ends after its limit with a timeout status;
+    the context stays usable and the status clears once read."""
+    import time
+    g = cuda_lib
+    assert g.gemm_device_status() == g.OK
+    flag = torch.zeros(4, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    g.gemm_wait_selftest(flag, 20_000_000)  # 20 ms per wait
+    assert g.gemm_device_status() == g.ERR_TIMEOUT
+    assert 0.03 < time.perf_counter() - t0 < 5.0
+    assert g.gemm_device_status() == g.OK
+    r = run_gemm(g, wl.random_problem(5, 256, 256, 256, wl.BF16, wl.F32, integer=True))
+    _assert_exact(r)
+    with pytest.raises(g.GemmError):
+        g.gemm_wait_selftest(flag, 2_000_000_000)
+
+
 def test_rejects_pageable_host_and_out_of_range_buffers(cuda_lib):
     g = cuda_lib
     A = torch.zeros(64 * 64, dtype=torch.bfloat16, device="cuda")
