@@ -71,7 +71,7 @@ struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     unsigned int *status = nullptr;
-    int max_clusters[4][4];  // pair kernel, by (ab, out); -1 = not queried yet
+    int max_clusters[5][4];  // pair kernel, by (ab incl. 3xTF32, out); -1 = not queried yet
 };
 
 std::mutex g_dev_mu;
@@ -226,6 +226,19 @@ gemm_status_t encode_2d(CUtensorMap *map, int ab, const void *base, int64_t inne
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// 2-D map with an explicit data type (3xTF32 arrays are plain fp32).
+gemm_status_t encode_2d_dt(CUtensorMap *map, CUtensorMapDataType dt, int es, const void *base, int64_t inner,
+                           int64_t outer, int64_t outer_stride_elems, uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(outer_stride_elems * es)};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = driver_fns().encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 // Map for an operand of logical shape (mn x k): K-major boxes are
 // (k-block x tile rows); MN-major boxes are (one 128-byte swizzle row of MN x
 // k-block), several per tile.
@@ -234,6 +247,19 @@ gemm_status_t encode_operand(CUtensorMap *map, int ab, const void *base, const O
     const uint32_t swz = 128u / elem_bytes(ab);
     if (!o.mn_major) return encode_2d(map, ab, base, k, mn, s_mn, swz, tile_mn);
     return encode_2d(map, ab, base, mn, k, s_k, swz, swz);
+}
+
+// ------------------------------------------------------------------ 3xTF32 --
+
+// Stacked K-major hi/lo arrays of A (2M x pitch) and B (2N x pitch), pitch = K
+// rounded up to 4 floats (16-byte rows for TMA), each array 256-byte aligned.
+int64_t tf32x3_pitch(int64_t K) { return (K + 3) / 4 * 4; }
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || M >= (int64_t(1) << 30) || N >= (int64_t(1) << 30) || K > INT32_MAX)
+        return 0;
+    const size_t p = static_cast<size_t>(tf32x3_pitch(K));
+    return round256(2 * static_cast<size_t>(M) * p * 4) + round256(2 * static_cast<size_t>(N) * p * 4);
 }
 
 // ------------------------------------------------------------ tile choice --
@@ -293,6 +319,7 @@ int pair_max_clusters_for(int ab, int cd) {
     case GEMM_F16: return pair_max_clusters_f16(cd);
     case GEMM_BF16: return pair_max_clusters_bf16(cd);
     case GEMM_E4M3: return pair_max_clusters_e4m3(cd);
+    case kDtTF32x3: return pair_max_clusters_tf32x3(cd);
     default: return 0;
     }
 }
@@ -397,6 +424,50 @@ EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alp
     return e;
 }
 
+// fp32 GEMM as 3xTF32: split A and B into the workspace, then the pair kernel
+// on the stacked hi/lo arrays (whole tiles, 256 x 256).
+gemm_status_t gemm_tf32x3(int64_t M, int64_t N, int64_t K, const void *A, int64_t sam, int64_t sak, const void *B,
+                          int64_t sbk, int64_t sbn, const EpiParams &e, void *workspace, int max_clusters,
+                          DeviceState *dev, cudaStream_t s) {
+    const int64_t pitch = tf32x3_pitch(K);
+    float *a2 = static_cast<float *>(workspace);
+    float *b2 = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                          round256(2 * static_cast<size_t>(M) * pitch * 4));
+    if (launch_tf32_split(static_cast<const float *>(A), M, K, sam, sak, a2, pitch, s) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (launch_tf32_split(static_cast<const float *>(B), N, K, sbn, sbk, b2, pitch, s) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const int bn = 256;
+    CUtensorMap ta, tb;
+    gemm_status_t st;
+    if ((st = encode_2d_dt(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a2, K, 2 * M, pitch, 32, 128)) != GEMM_OK)
+        return st;
+    if ((st = encode_2d_dt(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, b2, K, 2 * N, pitch, 32, bn / 2)) != GEMM_OK)
+        return st;
+    TcArgs t;
+    t.e = e;
+    t.K = static_cast<int>(K);
+    t.tiles_m = static_cast<int>((M + 255) / 256);
+    t.tiles_n = static_cast<int>((N + bn - 1) / bn);
+    t.num_tiles = t.tiles_m * t.tiles_n;
+    t.num_kb = static_cast<int>((K + 31) / 32);
+    t.group_m = 8;
+    t.a_mn_major = 0;
+    t.b_mn_major = 0;
+    t.status = dev->status;
+    t.bn = bn;
+    t.stage_tx = 2u * (128u * 128u + static_cast<uint32_t>(bn / 2) * 128u);
+    t.dp_tiles = t.num_tiles;
+    t.sk_units = 0;
+    t.partial = nullptr;
+    t.flags = nullptr;
+    t.epoch = 0;
+    t.lo_row_a = static_cast<int>(M);
+    t.lo_row_b = static_cast<int>(N);
+    const int clusters = t.num_tiles < max_clusters ? t.num_tiles : max_clusters;
+    return launch_pair_tf32x3(GEMM_F32, ta, tb, t, clusters, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -415,7 +486,7 @@ gemm_status_t gemm_query_path(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_d
 }
 
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype) {
-    (void)M; (void)N; (void)K;
+    if (ab_dtype == GEMM_F32) return tf32x3_workspace_bytes(M, N, K);
     if (ab_dtype != GEMM_F16 && ab_dtype != GEMM_BF16 && ab_dtype != GEMM_E4M3) return 0;
     DeviceState *dev = nullptr;
     if (device_state(&dev) != GEMM_OK) {
@@ -455,6 +526,18 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     if ((st = check_range(A, span_bytes(M, K, a_stride_m, a_stride_k, es))) != GEMM_OK) return st;
     if ((st = check_range(B, span_bytes(K, N, b_stride_k, b_stride_n, es))) != GEMM_OK) return st;
 
+    if (plan.path == GEMM_PATH_SIMT && ab_dtype == GEMM_F32) {
+        // fp32 inputs: 3xTF32 on the tensor cores when the caller's workspace
+        // holds the split operands; otherwise the FFMA kernel below.
+        const size_t need = tf32x3_workspace_bytes(M, N, K);
+        const int max_clusters = device_max_clusters(dev, kDtTF32x3, GEMM_F32);
+        if (need > 0 && workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 &&
+            workspace_bytes >= need && max_clusters > 0) {
+            if ((st = check_range(workspace, need)) != GEMM_OK) return st;
+            return gemm_tf32x3(M, N, K, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, e, workspace,
+                               max_clusters, dev, s);
+        }
+    }
     if (plan.path == GEMM_PATH_SIMT) {
         SimtArgs a;
         a.e = e;

@@ -52,6 +52,10 @@ template <> struct TcTraits<kDtE4M3> {
     static constexpr int kBytes = 1, kUmmaK = 32, kKind = kKindF8F6F4;
     static constexpr uint32_t kFmt = 0;
 };
+template <> struct TcTraits<kDtTF32x3> {
+    static constexpr int kBytes = 4, kUmmaK = 8, kKind = kKindTF32;
+    static constexpr uint32_t kFmt = 2;
+};
 
 template <int AB, int BN_, int STAGES_>
 struct TcConfig {

@@ -42,7 +42,13 @@ struct PairConfig {
     static constexpr int KSTEPS = BK / UMMA_K;
     static constexpr int A_BYTES = BM * BK * ES;          // this CTA's rows of A
     static constexpr int B_BYTES = (BN_MAX / 2) * BK * ES; // this CTA's columns of B (at most)
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // 3xTF32 keeps a hi and a lo copy of both tiles: [A hi][A lo][B hi][B lo].
+    static constexpr bool X3 = (AB == kDtTF32x3);
+    static constexpr int COPIES = X3 ? 2 : 1;
+    static constexpr int A_LO = A_BYTES;                  // offset of A lo (3xTF32)
+    static constexpr int B_OFF = COPIES * A_BYTES;        // offset of B (hi)
+    static constexpr int B_LO = B_OFF + B_BYTES;          // offset of B lo (3xTF32)
+    static constexpr int STAGE_BYTES = COPIES * (A_BYTES + B_BYTES);
     static constexpr int ACC_STRIDE = 256;                // TMEM columns between the two accumulators
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_WARPS = 8;
@@ -269,20 +275,28 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2u * args.stage_tx);
                     issued = true;
                     unsigned char *sA = smem + stage * Cfg::STAGE_BYTES;
-                    unsigned char *sB = sA + Cfg::A_BYTES;
+                    unsigned char *sB = sA + Cfg::B_OFF;
                     const int k0 = kb * BK;
-                    if (!args.a_mn_major) {
+                    if constexpr (Cfg::X3) {
+                        // hi and lo halves of the stacked K-major arrays
+                        tma_load_2d_pair(sA, &tmA, fbar, k0, m0);
+                        tma_load_2d_pair(sA + Cfg::A_LO, &tmA, fbar, k0, m0 + args.lo_row_a);
+                        tma_load_2d_pair(sB, &tmB, fbar, k0, n0);
+                        tma_load_2d_pair(sA + Cfg::B_LO, &tmB, fbar, k0, n0 + args.lo_row_b);
+                    } else if (!args.a_mn_major) {
                         tma_load_2d_pair(sA, &tmA, fbar, k0, m0);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / SWZ; ++j)
                             tma_load_2d_pair(sA + j * 128 * BK, &tmA, fbar, m0 + j * SWZ, k0);
                     }
-                    if (!args.b_mn_major) {
-                        tma_load_2d_pair(sB, &tmB, fbar, k0, n0);
-                    } else {
-                        for (int j = 0; j * SWZ < bnh; ++j)
-                            tma_load_2d_pair(sB + j * 128 * BK, &tmB, fbar, n0 + j * SWZ, k0);
+                    if constexpr (!Cfg::X3) {
+                        if (!args.b_mn_major) {
+                            tma_load_2d_pair(sB, &tmB, fbar, k0, n0);
+                        } else {
+                            for (int j = 0; j * SWZ < bnh; ++j)
+                                tma_load_2d_pair(sB + j * 128 * BK, &tmB, fbar, n0 + j * SWZ, k0);
+                        }
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -323,13 +337,22 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + Cfg::A_BYTES;
+                    const uint32_t b_addr = a_addr + Cfg::B_OFF;
 #pragma unroll
                     for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
+                        const uint32_t acc_in = (kb != seg.kb_begin || ks != 0) ? 1u : 0u;
                         const uint64_t ad = sw128_desc(a_addr + ks * a_kstep, a_lbo, 1024u);
                         const uint64_t bd = sw128_desc(b_addr + ks * b_kstep, b_lbo, 1024u);
-                        tc_mma_pair<TcTraits<AB>::kKind>(d_tmem, ad, bd, idesc,
-                                                          (kb != seg.kb_begin || ks != 0) ? 1u : 0u);
+                        if constexpr (Cfg::X3) {
+                            // 3xTF32: A*B ~ A_lo*B_hi + A_hi*B_lo + A_hi*B_hi, small terms first
+                            const uint64_t ad_lo = sw128_desc(a_addr + Cfg::A_LO + ks * a_kstep, a_lbo, 1024u);
+                            const uint64_t bd_lo = sw128_desc(a_addr + Cfg::B_LO + ks * b_kstep, b_lbo, 1024u);
+                            tc_mma_pair<TcTraits<AB>::kKind>(d_tmem, ad_lo, bd, idesc, acc_in);
+                            tc_mma_pair<TcTraits<AB>::kKind>(d_tmem, ad, bd_lo, idesc, 1u);
+                            tc_mma_pair<TcTraits<AB>::kKind>(d_tmem, ad, bd, idesc, 1u);
+                        } else {
+                            tc_mma_pair<TcTraits<AB>::kKind>(d_tmem, ad, bd, idesc, acc_in);
+                        }
                     }
                     issued = true;
                     tc_commit_pair(&empty[stage], 0x3);

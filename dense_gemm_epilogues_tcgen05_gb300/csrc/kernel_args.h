@@ -11,6 +11,9 @@ namespace gb300 {
 
 // Element type and epilogue codes, numbered like gemm_dtype_t / gemm_epilogue_t.
 enum : int { kDtF32 = 0, kDtF16 = 1, kDtBF16 = 2, kDtE4M3 = 3 };
+// Internal operand format of the tensor-core fp32 path: each operand split into
+// a tf32 "hi" and an fp32 "lo" part, stacked in one K-major array (3xTF32).
+enum : int { kDtTF32x3 = 4 };
 enum : int { kEpiNone = 0, kEpiBias = 1, kEpiBiasGelu = 2 };
 
 // Everything the epilogue needs: output geometry and the scalars.
@@ -42,6 +45,7 @@ struct TcArgs {
     float *partial;                   // stream-K: per cluster, 2 CTAs x 128 x 256 fp32 partial sums
     unsigned int *flags;              // stream-K: per cluster, 2 CTAs x 8 epilogue warps
     unsigned int epoch;               // stream-K: value a flag takes when its partial is ready (never 0)
+    int lo_row_a, lo_row_b;           // 3xTF32: first row of the "lo" half in the stacked A / B arrays
 };
 
 // Floats of stream-K partial sums one CTA of a cluster writes, and flags per cluster.
@@ -76,6 +80,12 @@ cudaError_t launch_pair_e4m3(int out, const CUtensorMap &, const CUtensorMap &, 
 int pair_max_clusters_f16(int out);
 int pair_max_clusters_bf16(int out);
 int pair_max_clusters_e4m3(int out);
+//   3xTF32 pair kernel (fp32 output) and the hi/lo split pre-pass:
+cudaError_t launch_pair_tf32x3(int out, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
+                               cudaStream_t);
+int pair_max_clusters_tf32x3(int out);
+cudaError_t launch_tf32_split(const float *src, long long rows, long long cols, long long s_row, long long s_col,
+                              float *dst, long long pitch, cudaStream_t stream);
 //   CUDA-core kernels:
 cudaError_t launch_simt(int ab, int out, const SimtArgs &args, cudaStream_t stream);
 cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t stream);

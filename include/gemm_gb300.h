@@ -68,7 +68,9 @@ typedef enum {
     GEMM_ERR_TIMEOUT = 6        /* a device-side wait gave up (reported by gemm_device_status) */
 } gemm_status_t;
 
-/* Which kernel family a call runs on (see gemm_query_path). */
+/* Which kernel family a call runs on (see gemm_query_path).  fp32 inputs report
+ * GEMM_PATH_SIMT, the path without a workspace; given a workspace of
+ * gemm_workspace_size() bytes they run as 3xTF32 on the tensor cores. */
 typedef enum {
     GEMM_PATH_NOOP = 0,           /* M == 0 or N == 0: nothing to do */
     GEMM_PATH_EPILOGUE_ONLY = 1,  /* K == 0 or alpha == 0: C = cast(epilogue(beta*C + bias)) */
@@ -125,11 +127,14 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K,
                    gemm_stream_t stream);
 
 /*
- * gemm_workspace_size -- bytes of device scratch that let gemm() use the
- * stream-K schedule on the current device: 256 KB of partial sums and 64
- * bytes of flags per pair of SMs (about 19 MB on a 152-SM GB300), 0 for fp32
- * inputs or when the device cannot be queried.  The size does not depend on
- * M, N, K.  Never fails.
+ * gemm_workspace_size -- bytes of device scratch that let gemm() use its
+ * fastest path.  fp16 / bf16 / fp8 inputs: the stream-K schedule on the
+ * current device, 256 KB of partial sums and 64 bytes of flags per pair of SMs
+ * (about 19 MB on a 152-SM GB300), independent of M, N, K; 0 when the device
+ * cannot be queried.  fp32 inputs: the 3xTF32 split of both operands, hi and
+ * lo copies in K-major rows padded to 16 bytes, 2*(M+N)*ceil4(K)*4 bytes
+ * (each half rounded up to 256); with it gemm() runs fp32 on the tensor
+ * cores, without it on the FFMA kernel.  Never fails.
  */
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype);
 

@@ -34,11 +34,12 @@ def sample_rows(M, n_random=256, seed=23):
 _WORKSPACE = {}
 
 
-def workspace(g, device="cuda"):
-    """One stream-K workspace per device (256-byte aligned), reused by every call."""
-    if device not in _WORKSPACE:
-        n = g.gemm_workspace_size(1, 1, 1, g.BF16)
-        _WORKSPACE[device] = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+def workspace(g, device="cuda", nbytes=0):
+    """A workspace of at least `nbytes` (and the stream-K size), reused across calls."""
+    need = max(nbytes, g.gemm_workspace_size(1, 1, 1, g.BF16), 256)
+    if device not in _WORKSPACE or _WORKSPACE[device].numel() < need:
+        _WORKSPACE.pop(device, None)
+        _WORKSPACE[device] = torch.empty(need, dtype=torch.uint8, device=device)
     return _WORKSPACE[device]
 
 
@@ -71,7 +72,7 @@ def run_gemm(g, p, *, nan_c=False, stream=None, a_elem_offset=0, b_elem_offset=0
     path = g.gemm_query_path(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr,
                              p.b_stride_k, p.b_stride_n, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta,
                              bias, p.epilogue)
-    ws = workspace(g, device) if use_workspace else None
+    ws = workspace(g, device, g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype)) if use_workspace else None
     g.gemm(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr, p.b_stride_k, p.b_stride_n,
            c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue,
            workspace=ws, workspace_bytes=0 if ws is None else ws.numel(), stream=stream)

@@ -55,8 +55,10 @@ def test_status_strings_and_version(g):
 
 
 def test_workspace_size_without_gpu(g):
-    # fp32 inputs never need one; without a device the size cannot be known: 0
-    assert g.gemm_workspace_size(4096, 4096, 4096, g.F32) == 0
+    # fp32: the 3xTF32 split buffers, a pure function of the sizes
+    assert g.gemm_workspace_size(4096, 4096, 4096, g.F32) == 2 * (4096 + 4096) * 4096 * 4
+    assert g.gemm_workspace_size(0, 4096, 4096, g.F32) == 0
+    # 16-bit / fp8: stream-K scratch per SM pair; without a device it is unknown: 0
     assert g.gemm_workspace_size(4096, 4096, 4096, g.BF16) >= 0
 
 

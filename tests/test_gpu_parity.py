@@ -356,4 +356,33 @@ def test_workspace_size(cuda_lib):
     n = g.gemm_workspace_size(4096, 4096, 4096, g.F16)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert n >= (sms // 2) * 2 * 128 * 256 * 4
-    assert g.gemm_workspace_size(4096, 4096, 4096, g.F32) == 0
+    # fp32 inputs: the 3xTF32 split of A and B (hi + lo, K-major, 16-byte rows)
+    assert g.gemm_workspace_size(4096, 4096, 4096, g.F32) == 2 * (4096 + 4096) * 4096 * 4
+    assert g.gemm_workspace_size(100, 50, 9, g.F32) == 256 * ((2 * 100 * 12 * 4 + 255) // 256) + 256 * (
+        (2 * 50 * 12 * 4 + 255) // 256)
+
+
+# ------------------------------------------------------------------- 3xTF32 --
+
+@pytest.mark.parametrize("shape", [(256, 256, 128), (336, 200, 1000), (1024, 768, 4096), (5, 300, 77)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layout", ["NN", "NT", "TN", "TT"])
+def test_fp32_3xtf32_integer_exact(cuda_lib, layout, shape):
+    """Small integers are exact in tf32 (lo = 0): the split path must be exact."""
+    M, N, K = shape
+    p = wl.random_problem(900 + M + K, M, N, K, wl.F32, wl.F32, layout=layout, alpha=2.0, beta=-1.0,
+                          integer=True, ldc_pad=3)
+    r = run_gemm(cuda_lib, p)
+    assert r.status == 0
+    _assert_exact(r)
+
+
+def test_fp32_workspace_selects_tensor_core_path(cuda_lib):
+    """With a workspace fp32 runs as 3xTF32 (tensor cores), without it on the FFMA
+    kernel; both meet 1e-5 and their roundings differ."""
+    p = wl.random_problem(123, 768, 640, 2048, wl.F32, wl.F32, alpha=1.0, beta=0.5)
+    a = run_gemm(cuda_lib, p, use_workspace=True)
+    b = run_gemm(cuda_lib, p, use_workspace=False)
+    ra, rb = a.check(), b.check()
+    assert ra["pass"] and rb["pass"], (ra, rb)
+    assert not np.array_equal(a.out_codes, b.out_codes)
