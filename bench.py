@@ -175,12 +175,15 @@ class ClockSampler:
 _WS = {}
 
 
-def _workspace(g, device):
-    """The stream-K workspace (allocated once, outside any timed region)."""
+def _workspace(g, device, nbytes=0):
+    """The library's workspace (stream-K scratch, or the 3xTF32 split of fp32
+    operands), allocated outside any timed region and reused."""
     import torch
     key = str(device)
-    if key not in _WS:
-        _WS[key] = torch.empty(max(g.gemm_workspace_size(1, 1, 1, g.BF16), 256), dtype=torch.uint8, device=device)
+    need = max(nbytes, g.gemm_workspace_size(1, 1, 1, g.BF16), 256)
+    if key not in _WS or _WS[key].numel() < need:
+        _WS.pop(key, None)
+        _WS[key] = torch.empty(need, dtype=torch.uint8, device=device)
     return _WS[key]
 
 
@@ -194,7 +197,7 @@ def _make_sets(problem, n_sets, device):
 
 def _call(g, p, s, stream):
     A, B, C, bias = s
-    ws = _workspace(g, C.device)
+    ws = _workspace(g, C.device, g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype))
     g.gemm(p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k, p.b_stride_n, C, p.ldc,
            p.c_dtype, p.alpha, p.beta, bias, p.epilogue, workspace=ws, workspace_bytes=ws.numel(), stream=stream)
 
@@ -378,7 +381,8 @@ def extra_cells(g, stream):
     cells["fp8_over_fp16"] = round(cells["fp8_4096_bf16out"]["median_tflops"] /
                                    cells["fp16_twin_4096_bf16out"]["median_tflops"], 3)
     cells["bf16_8192_nn"] = cell(g, wl.bf16_nn_large(8192), 10, 3, stream, n_sets=2)
-    cells["fp32_4096_NN_simt"] = cell(g, wl.fp32_layout("NN", 4096), 5, 2, stream, n_sets=2)
+    cells["fp32_4096_NN_3xtf32"] = cell(g, wl.fp32_layout("NN", 4096), 20, 3, stream, n_sets=2)
+    cells["fp32_4096_TT_3xtf32"] = cell(g, wl.fp32_layout("TT", 4096), 20, 3, stream, n_sets=2)
     for M in (512, 2048, 8192):
         fused = cell(g, wl.bf16_bias_gelu(M), 30, 5, stream)
         plain = cell(g, wl.bf16_bias_gelu(M, epilogue=wl.EPI_NONE), 30, 5, stream)
