@@ -210,6 +210,7 @@ template <> struct Vec16<kDtBF16> {
 };
 
 // Fast path: 32 in-range columns of one row, C and bias 16-byte aligned.
+// `bias_chunk` may point to global or shared memory (generic loads).
 template <int OUT>
 __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename Elem<OUT>::T *crow,
                                                       const float *bias_chunk, const EpiParams &e) {
@@ -235,7 +236,7 @@ __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename E
         const float4 *b4 = reinterpret_cast<const float4 *>(bias_chunk);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const float4 b = __ldg(b4 + q);
+            const float4 b = b4[q];
             v[4 * q] += b.x; v[4 * q + 1] += b.y; v[4 * q + 2] += b.z; v[4 * q + 3] += b.w;
         }
         if (e.epilogue == kEpiBiasGelu) {
@@ -263,12 +264,13 @@ __device__ __forceinline__ void epilogue_chunk32_safe(const float (&v)[32], type
 
 // One thread's share of a tile's epilogue: row `row` (its TMEM lane), chunks
 // 0 .. nvalid-1 of 32 columns starting at TMEM column address t_base and
-// output column col_base.  The TMEM load of chunk i+1 is in flight while chunk
-// i is processed.  Warp-collective (every lane calls it with the same t_base,
-// col_base and nvalid); nvalid <= MAXC.
+// output column col_base; bias_base[c] is the bias of column col_base + c (in
+// global memory, or staged in shared memory).  The TMEM load of chunk i+1 is
+// in flight while chunk i is processed.  Warp-collective (every lane calls it
+// with the same t_base, col_base and nvalid); nvalid <= MAXC.
 template <int OUT, int MAXC>
 __device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_base, int nvalid, int row, bool row_ok,
-                                                    const EpiParams &e) {
+                                                    const float *bias_base, const EpiParams &e) {
     using OutT = typename Elem<OUT>::T;
     if (nvalid <= 0) return;
     OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
@@ -289,13 +291,38 @@ __device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_bas
         const int col0 = col_base + i * 32;
         if (row_ok) {
             if (e.c_vec && col0 + 32 <= e.N)
-                epilogue_chunk32_fast<OUT>(v, crow + col0, e.bias + col0, e);
+                epilogue_chunk32_fast<OUT>(v, crow + col0, bias_base + i * 32, e);
             else
                 epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
         }
         __syncwarp();  // reconverge after the per-row store before the collective wait
         if (more) tmem_ld_wait(nxt);
     }
+}
+
+// Epilogue inputs of one warp's columns, fetched before the accumulator is
+// ready so their latency overlaps the main loop: the 32*nchunk bias values
+// go to shared memory (bias_s, 16-byte aligned), and this thread's row of C
+// (when beta != 0) is prefetched into L2.  Warp-collective.
+template <int OUT>
+__device__ __forceinline__ void epilogue_prefetch(float *bias_s, int col_base, int nchunk, int row, bool row_ok,
+                                                  const EpiParams &e) {
+    using OutT = typename Elem<OUT>::T;
+    const int lane = threadIdx.x & 31;
+    if (e.epilogue != kEpiNone) {
+        for (int c = lane; c < nchunk * 32; c += 32) {
+            const int col = col_base + c;
+            bias_s[c] = col < e.N ? e.bias[col] : 0.0f;
+        }
+    }
+    const int ncols = min(nchunk * 32, e.N - col_base);  // only columns inside the matrix
+    if (e.beta != 0.0f && row_ok && ncols > 0) {
+        const OutT *crow = reinterpret_cast<const OutT *>(e.C) + (long long)row * e.ldc + col_base;
+        const int bytes = ncols * static_cast<int>(sizeof(OutT));
+        const char *p = reinterpret_cast<const char *>(crow);
+        for (int off = 0; off < bytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+    }
+    __syncwarp();
 }
 
 }  // namespace gb300

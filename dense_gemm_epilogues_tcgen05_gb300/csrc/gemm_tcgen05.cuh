@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(TcConfig<AB, BN, STAGES>::THREADS, 1)
             int nvalid = BN / 32;
             const int left = (N - n0 + 31) >> 5;  // chunks that start inside the matrix
             if (left < nvalid) nvalid = left;
-            epilogue_row_chunks<OUT, BN / 32>(t_row, n0, nvalid, row, row_ok, e);
+            epilogue_row_chunks<OUT, BN / 32>(t_row, n0, nvalid, row, row_ok, e.bias + n0, e);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);

@@ -54,7 +54,9 @@ struct PairConfig {
     static constexpr int EPI_WARPS = 8;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    // Bias staged per epilogue warp (up to 4 chunks of 32 columns), per accumulator.
+    static constexpr int BIAS_BYTES = 2 * EPI_WARPS * 128 * 4;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + BIAS_BYTES;
     static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
     static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the pair allocates all 512 TMEM columns");
 };
@@ -160,7 +162,7 @@ __device__ __forceinline__ void store_partial_chunks(uint32_t t_base, int c0, in
 template <int OUT>
 __device__ __forceinline__ void owner_row_chunks(uint32_t t_base, int col_base, int c0, int nvalid, int row,
                                                  bool row_ok, int r, const float *slot0, long long slot_stride,
-                                                 int ncontrib, const EpiParams &e) {
+                                                 int ncontrib, const float *bias_base, const EpiParams &e) {
     using OutT = typename Elem<OUT>::T;
     OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
 #pragma unroll 1
@@ -184,7 +186,7 @@ __device__ __forceinline__ void owner_row_chunks(uint32_t t_base, int col_base, 
         const int col0 = col_base + i * 32;
         if (row_ok) {
             if (e.c_vec && col0 + 32 <= e.N)
-                epilogue_chunk32_fast<OUT>(v, crow + col0, e.bias + col0, e);
+                epilogue_chunk32_fast<OUT>(v, crow + col0, bias_base + i * 32, e);
             else
                 epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
         }
@@ -209,6 +211,7 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
     uint64_t *mma_done = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *bias_stage = reinterpret_cast<float *>(smem + STAGES * Cfg::STAGE_BYTES + Cfg::BAR_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -387,6 +390,9 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
             tile_coords(seg.tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
             const int row = tm * 2 * BM + static_cast<int>(rank) * BM + r;
             const int n_tile = tn * bn;
+            float *bias_s = bias_stage + (acc * Cfg::EPI_WARPS + ew) * 128;
+            if (seg.kind != kSegPart)
+                epilogue_prefetch<OUT>(bias_s, n_tile + c_begin * 32, c_end - c_begin, row, row < M, e);
             const bool got = pair_wait(&tfull[acc], acc_phase, abort_flag, args.status, peer_abort);
             if (__any_sync(0xffffffffu, !got)) break;
             tc_fence_after();
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
             if (left < nvalid) nvalid = left;
             bool fail = false;
             if (seg.kind == kSegFull) {
-                epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, e);
+                epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, bias_s, e);
             } else if (seg.kind == kSegPart) {
                 float *slot = args.partial + (static_cast<long long>(cluster) * 2 + rank) * kPartialFloatsPerCta;
                 store_partial_chunks(t_row + c_begin * 32, c_begin, nvalid, r, slot);
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
                 const float *slot0 =
                     args.partial + (static_cast<long long>(cluster + 1) * 2 + rank) * kPartialFloatsPerCta;
                 owner_row_chunks<OUT>(t_row + c_begin * 32, col_base, c_begin, nvalid, row, row_ok, r, slot0,
-                                      2 * kPartialFloatsPerCta, ncontrib, e);
+                                      2 * kPartialFloatsPerCta, ncontrib, bias_s, e);
                 __syncwarp();
                 if (lane == 0)
                     for (int k = 1; k <= ncontrib; ++k) args.flags[((cluster + k) * 2 + rank) * 8 + ew] = 0u;
