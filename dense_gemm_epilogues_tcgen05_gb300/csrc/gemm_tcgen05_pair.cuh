@@ -30,7 +30,11 @@
 
 namespace gb300 {
 
-template <int AB, int STAGES_>
+// BNH: B columns one CTA stages per k-block (half the widest tile it runs).
+// All instantiations use 128 (6 stages of 32 KB); a 64-column, 8-stage ring
+// for 128-wide tiles measured no faster on GB300 (M=512, N=K=4096: 28.7 us
+// either way), so it is not built.
+template <int AB, int STAGES_, int BNH = 128>
 struct PairConfig {
     static constexpr int BM = 128;  // rows per CTA (256 per pair)
     static constexpr int BN_MAX = 256;
@@ -41,7 +45,10 @@ struct PairConfig {
     static constexpr int UMMA_K = TcTraits<AB>::kUmmaK;
     static constexpr int KSTEPS = BK / UMMA_K;
     static constexpr int A_BYTES = BM * BK * ES;          // this CTA's rows of A
-    static constexpr int B_BYTES = (BN_MAX / 2) * BK * ES; // this CTA's columns of B (at most)
+    // This CTA's columns of B (at most).  An N-contiguous B is loaded in whole
+    // 128-byte swizzle rows (SWZ columns), so the slot is never narrower.
+    static constexpr int B_COLS = BNH > SWZ ? BNH : SWZ;
+    static constexpr int B_BYTES = B_COLS * BK * ES;
     // 3xTF32 keeps a hi and a lo copy of both tiles: [A hi][A lo][B hi][B lo].
     static constexpr bool X3 = (AB == kDtTF32x3);
     static constexpr int COPIES = X3 ? 2 : 1;
@@ -194,11 +201,11 @@ __device__ __forceinline__ void owner_row_chunks(uint32_t t_base, int col_base, 
     __syncwarp();
 }
 
-template <int AB, int OUT, int STAGES>
-__global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
+template <int AB, int OUT, int STAGES, int BNH>
+__global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const TcArgs args) {
-    using Cfg = PairConfig<AB, STAGES>;
+    using Cfg = PairConfig<AB, STAGES, BNH>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, SWZ = Cfg::SWZ;
 
     extern __shared__ unsigned char smem_raw[];
@@ -446,11 +453,14 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES>::THREADS, 1)
     }
 }
 
-template <int AB, int OUT, int STAGES>
+template <int AB, int OUT, int STAGES, int BNH = 128>
 cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, int clusters,
                             cudaStream_t stream) {
-    using Cfg = PairConfig<AB, STAGES>;
-    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES>;
+    using Cfg = PairConfig<AB, STAGES, BNH>;
+    // What one CTA's loads of a stage occupy must fit its slots.
+    if (args.bn > 2 * BNH) return cudaErrorInvalidValue;
+    if (args.stage_tx > static_cast<uint32_t>(Cfg::STAGE_BYTES)) return cudaErrorInvalidValue;
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -469,10 +479,10 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
 }
 
 // Largest number of two-CTA clusters of this kernel that can be resident at once.
-template <int AB, int OUT, int STAGES>
+template <int AB, int OUT, int STAGES, int BNH = 128>
 int pair_max_clusters() {
-    using Cfg = PairConfig<AB, STAGES>;
-    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES>;
+    using Cfg = PairConfig<AB, STAGES, BNH>;
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
