@@ -300,6 +300,118 @@ __device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_bas
     }
 }
 
+// ------------------------------------------- staged epilogue (C by TMA) --
+// With one row per thread, direct loads and stores touch 32 rows per warp
+// instruction.  The staged form moves C as 32-row x 64-byte boxes between
+// global memory and a per-warp 2 KB shared-memory buffer with TMA (coalesced,
+// no L1 traffic), and the threads only read and write their own row of the
+// buffer.  The box uses the 64-byte TMA swizzle: 16-byte unit q of row r sits
+// at unit q ^ ((r >> 1) & 3) of that row, so the eight rows of a quarter-warp
+// fall in eight different bank groups.  Elements of a box outside the matrix
+// (ragged M or N, the ldc padding) are zero on load and never stored.
+
+constexpr int kStageBoxBytes = 32 * 64;  // one warp's staged box
+
+__device__ __forceinline__ uint32_t sw64_offset(int r, int q) {
+    return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+}
+
+// Epilogue of one 32-column chunk of the warp's 32 rows (this thread: row
+// row0 + lane, accumulators v), output columns col0 .. col0+31, bias of those
+// columns at bias_chunk (16-byte aligned, shared memory).  Warp-collective;
+// row0 < M and col0 < N.  Stores stay in flight when it returns; the buffer is
+// reused only after the previous store has read it.  Returns false if a wait
+// for C gave up.
+template <int OUT>
+__device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, int row0, const float *bias_chunk,
+                                                     const EpiParams &e, const CUtensorMap *tmC, unsigned char *buf,
+                                                     uint64_t *cbar, uint32_t &cphase, volatile int *abort_flag,
+                                                     unsigned int *status) {
+    constexpr int ES = static_cast<int>(sizeof(typename Elem<OUT>::T));
+    constexpr int PER = 64 / ES;  // columns per box row
+    constexpr int NSUB = 32 / PER;
+    constexpr int PV = Vec16<OUT>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const uint64_t alpha2 = f2_splat(e.alpha);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const uint64_t r = f2_mul(f2_pack(v[j], v[j + 1]), alpha2);
+        f2_unpack(r, v[j], v[j + 1]);
+    }
+#pragma unroll
+    for (int h = 0; h < NSUB; ++h) {
+        const int x = col0 + h * PER;
+        if (x >= e.N) break;  // warp-uniform
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        if (e.beta != 0.0f) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(cbar, kStageBoxBytes);
+                tma_load_2d(buf, tmC, cbar, x, row0);
+            }
+            const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
+            if (!__all_sync(0xffffffffu, got)) return false;
+            cphase ^= 1u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float c[PV];
+                Vec16<OUT>::unpack(*reinterpret_cast<const uint4 *>(buf + sw64_offset(lane, q)), c);
+#pragma unroll
+                for (int t = 0; t < PV; ++t) v[h * PER + q * PV + t] = fmaf(e.beta, c[t], v[h * PER + q * PV + t]);
+            }
+        }
+        if (e.epilogue != kEpiNone) {
+            const float4 *b4 = reinterpret_cast<const float4 *>(bias_chunk + h * PER);
+#pragma unroll
+            for (int q = 0; q < PER / 4; ++q) {
+                const float4 b = b4[q];
+                v[h * PER + 4 * q] += b.x; v[h * PER + 4 * q + 1] += b.y;
+                v[h * PER + 4 * q + 2] += b.z; v[h * PER + 4 * q + 3] += b.w;
+            }
+            if (e.epilogue == kEpiBiasGelu) {
+#pragma unroll
+                for (int j = 0; j < PER; j += 2) gelu_erf2(v[h * PER + j], v[h * PER + j + 1]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4 *>(buf + sw64_offset(lane, q)) = Vec16<OUT>::pack(&v[h * PER + q * PV]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, buf, x, row0);
+            bulk_commit();
+        }
+    }
+    return true;
+}
+
+// Staged epilogue of one warp's rows row0 .. row0+31 and chunks 0 .. nvalid-1
+// of 32 columns from TMEM column address t_base / output column col_base (the
+// TMEM load of chunk i+1 in flight while chunk i is processed).  Warp-collective.
+template <int OUT, int MAXC>
+__device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base, int nvalid, int row0,
+                                                  const float *bias_base, const EpiParams &e, const CUtensorMap *tmC,
+                                                  unsigned char *buf, uint64_t *cbar, uint32_t &cphase,
+                                                  volatile int *abort_flag, unsigned int *status) {
+    bool ok = true;
+#pragma unroll 1
+    for (int i = 0; i < nvalid; ++i) {
+        uint32_t raw[32];
+        __syncwarp();
+        tmem_ld_issue(t_base + i * 32, raw);
+        tmem_ld_wait(raw);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
+        if (ok)
+            ok = epilogue_chunk32_tma<OUT>(v, col_base + i * 32, row0, bias_base + i * 32, e, tmC, buf, cbar,
+                                           cphase, abort_flag, status);
+    }
+    __syncwarp();
+    return ok;
+}
+
 // Epilogue inputs of one warp's columns, fetched before the accumulator is
 // ready so their latency overlaps the main loop: the 32*nchunk bias values
 // go to shared memory (bias_s, 16-byte aligned), and this thread's row of C

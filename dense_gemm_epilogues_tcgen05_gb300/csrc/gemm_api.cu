@@ -249,6 +249,27 @@ gemm_status_t encode_operand(CUtensorMap *map, int ab, const void *base, const O
     return encode_2d(map, ab, base, mn, k, s_k, swz, swz);
 }
 
+// Map of the output C (N x M, row pitch ldc) for the pair kernel's staged
+// epilogue: boxes of 32 rows x 64 bytes with the 64-byte swizzle.  Returns
+// false (and the kernel stores C directly) when C's base or row pitch rules
+// out TMA.
+bool encode_c(CUtensorMap *map, int cd, void *C, int64_t M, int64_t N, int64_t ldc) {
+    const int es = elem_bytes(cd);
+    const int64_t pitch = ldc * es;
+    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || pitch % 16 != 0 || pitch <= 0 || pitch >= (int64_t(1) << 40))
+        return false;
+    const CUtensorMapDataType dt = cd == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : cd == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / es), 32u};
+    cuuint32_t estr[2] = {1, 1};
+    return driver_fns().encode(map, dt, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ 3xTF32 --
 
 // Stacked K-major hi/lo arrays of A (2M x pitch) and B (2N x pitch), pitch = K
@@ -387,12 +408,12 @@ TileChoice choose_tile(int64_t M, int64_t N, int num_sms, int max_clusters, int 
     return best;
 }
 
-cudaError_t launch_pair(int ab, int cd, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
-                        int clusters, cudaStream_t s) {
+cudaError_t launch_pair(int ab, int cd, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                        const TcArgs &args, int clusters, cudaStream_t s) {
     switch (ab) {
-    case GEMM_F16: return launch_pair_f16(cd, ta, tb, args, clusters, s);
-    case GEMM_BF16: return launch_pair_bf16(cd, ta, tb, args, clusters, s);
-    case GEMM_E4M3: return launch_pair_e4m3(cd, ta, tb, args, clusters, s);
+    case GEMM_F16: return launch_pair_f16(cd, ta, tb, tc, args, clusters, s);
+    case GEMM_BF16: return launch_pair_bf16(cd, ta, tb, tc, args, clusters, s);
+    case GEMM_E4M3: return launch_pair_e4m3(cd, ta, tb, tc, args, clusters, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -421,6 +442,7 @@ EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alp
     const bool c_al = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (ldc * elem_bytes(cd)) % 16 == 0;
     const bool b_al = epi == GEMM_EPI_NONE || (reinterpret_cast<uintptr_t>(bias) & 15u) == 0;
     e.c_vec = (c_al && b_al) ? 1 : 0;
+    e.c_tma = 0;  // set by the pair-kernel launch once C's tensor map is encoded
     return e;
 }
 
@@ -464,8 +486,11 @@ gemm_status_t gemm_tf32x3(int64_t M, int64_t N, int64_t K, const void *A, int64_
     t.epoch = 0;
     t.lo_row_a = static_cast<int>(M);
     t.lo_row_b = static_cast<int>(N);
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof(tc));
+    t.e.c_tma = encode_c(&tc, GEMM_F32, e.C, M, N, e.ldc) ? 1 : 0;
     const int clusters = t.num_tiles < max_clusters ? t.num_tiles : max_clusters;
-    return launch_pair_tf32x3(GEMM_F32, ta, tb, t, clusters, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    return launch_pair_tf32x3(GEMM_F32, ta, tb, tc, t, clusters, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 }  // namespace
@@ -593,7 +618,10 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
             t.flags = reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + partial_bytes(max_clusters));
             t.epoch = next_epoch();
         }
-        err = launch_pair(ab_dtype, c_dtype, ta, tb, t, clusters, s);
+        CUtensorMap tcm;
+        std::memset(&tcm, 0, sizeof(tcm));
+        t.e.c_tma = encode_c(&tcm, c_dtype, C, M, N, ldc) ? 1 : 0;
+        err = launch_pair(ab_dtype, c_dtype, ta, tb, tcm, t, clusters, s);
     } else {
         const int grid = static_cast<int>(t.num_tiles < dev->num_sms ? t.num_tiles : dev->num_sms);
         err = launch_tc(ab_dtype, c_dtype, tc.bn, ta, tb, t, grid, s);

@@ -17,11 +17,11 @@ cudaError_t launch_tcgen05_bf16(int out, int bn, const CUtensorMap &ta, const CU
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_pair_bf16(int out, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
+cudaError_t launch_pair_bf16(int out, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const TcArgs &args,
                               int clusters, cudaStream_t stream) {
-    if (out == kDtBF16) return launch_pair_cfg<kDtBF16, kDtBF16, 6>(ta, tb, args, clusters, stream);
-    if (out == kDtF32) return launch_pair_cfg<kDtBF16, kDtF32, 6>(ta, tb, args, clusters, stream);
-    if (out == kDtF16) return launch_pair_cfg<kDtBF16, kDtF16, 6>(ta, tb, args, clusters, stream);
+    if (out == kDtBF16) return launch_pair_cfg<kDtBF16, kDtBF16, 6>(ta, tb, tc, args, clusters, stream);
+    if (out == kDtF32) return launch_pair_cfg<kDtBF16, kDtF32, 6>(ta, tb, tc, args, clusters, stream);
+    if (out == kDtF16) return launch_pair_cfg<kDtBF16, kDtF16, 6>(ta, tb, tc, args, clusters, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -15,10 +15,10 @@ cudaError_t launch_tcgen05_e4m3(int out, int bn, const CUtensorMap &ta, const CU
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_pair_e4m3(int out, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
+cudaError_t launch_pair_e4m3(int out, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const TcArgs &args,
                               int clusters, cudaStream_t stream) {
-    if (out == kDtBF16) return launch_pair_cfg<kDtE4M3, kDtBF16, 6>(ta, tb, args, clusters, stream);
-    if (out == kDtF32) return launch_pair_cfg<kDtE4M3, kDtF32, 6>(ta, tb, args, clusters, stream);
+    if (out == kDtBF16) return launch_pair_cfg<kDtE4M3, kDtBF16, 6>(ta, tb, tc, args, clusters, stream);
+    if (out == kDtF32) return launch_pair_cfg<kDtE4M3, kDtF32, 6>(ta, tb, tc, args, clusters, stream);
     return cudaErrorInvalidValue;
 }
 

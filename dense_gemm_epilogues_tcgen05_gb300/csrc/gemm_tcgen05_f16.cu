@@ -17,11 +17,11 @@ cudaError_t launch_tcgen05_f16(int out, int bn, const CUtensorMap &ta, const CUt
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_pair_f16(int out, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
+cudaError_t launch_pair_f16(int out, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const TcArgs &args,
                               int clusters, cudaStream_t stream) {
-    if (out == kDtF16) return launch_pair_cfg<kDtF16, kDtF16, 6>(ta, tb, args, clusters, stream);
-    if (out == kDtF32) return launch_pair_cfg<kDtF16, kDtF32, 6>(ta, tb, args, clusters, stream);
-    if (out == kDtBF16) return launch_pair_cfg<kDtF16, kDtBF16, 6>(ta, tb, args, clusters, stream);
+    if (out == kDtF16) return launch_pair_cfg<kDtF16, kDtF16, 6>(ta, tb, tc, args, clusters, stream);
+    if (out == kDtF32) return launch_pair_cfg<kDtF16, kDtF32, 6>(ta, tb, tc, args, clusters, stream);
+    if (out == kDtBF16) return launch_pair_cfg<kDtF16, kDtBF16, 6>(ta, tb, tc, args, clusters, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -60,10 +60,17 @@ struct PairConfig {
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_WARPS = 8;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    // Per epilogue warp: one staged 32-row x 64-byte box of C (TMA in and out).
+    static constexpr int CSTAGE_BYTES = EPI_WARPS * kStageBoxBytes;
     static constexpr int BAR_BYTES = 256;
     // Bias staged per epilogue warp (up to 4 chunks of 32 columns), per accumulator.
     static constexpr int BIAS_BYTES = 2 * EPI_WARPS * 128 * 4;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + BIAS_BYTES;
+    // Layout: [stages][C boxes][barriers][bias]; stages and boxes stay 1024-byte aligned.
+    static constexpr int CSTAGE_OFF = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = CSTAGE_OFF + CSTAGE_BYTES;
+    static constexpr int BIAS_OFF = BAR_OFF + BAR_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + BIAS_OFF + BIAS_BYTES;
+    static_assert((2 * STAGES + 5 + EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barriers fit their slot");
     static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
     static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the pair allocates all 512 TMEM columns");
 };
@@ -166,12 +173,18 @@ __device__ __forceinline__ void store_partial_chunks(uint32_t t_base, int c0, in
 // OWNER epilogue: like epilogue_row_chunks, with the partial sums of
 // `ncontrib` later clusters (slots slot0, slot0 + slot_stride, ...) added to
 // the accumulators before alpha / beta / bias / GELU / cast.
+// With e.c_tma the chunks go through the warp's staged C box (rows row0 ..
+// row0+31, row0 < M) instead.  Returns false if a wait for C gave up.
 template <int OUT>
-__device__ __forceinline__ void owner_row_chunks(uint32_t t_base, int col_base, int c0, int nvalid, int row,
+__device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, int c0, int nvalid, int row,
                                                  bool row_ok, int r, const float *slot0, long long slot_stride,
-                                                 int ncontrib, const float *bias_base, const EpiParams &e) {
+                                                 int ncontrib, const float *bias_base, const EpiParams &e,
+                                                 int row0, const CUtensorMap *tmC, unsigned char *cbuf,
+                                                 uint64_t *cbar, uint32_t &cphase, volatile int *abort_flag,
+                                                 unsigned int *status) {
     using OutT = typename Elem<OUT>::T;
     OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
+    bool ok = true;
 #pragma unroll 1
     for (int i = 0; i < nvalid; ++i) {
         uint32_t raw[32];
@@ -191,7 +204,11 @@ __device__ __forceinline__ void owner_row_chunks(uint32_t t_base, int col_base, 
             }
         }
         const int col0 = col_base + i * 32;
-        if (row_ok) {
+        if (e.c_tma) {
+            if (ok && row0 < e.M)
+                ok = epilogue_chunk32_tma<OUT>(v, col0, row0, bias_base + i * 32, e, tmC, cbuf, cbar, cphase,
+                                               abort_flag, status);
+        } else if (row_ok) {
             if (e.c_vec && col0 + 32 <= e.N)
                 epilogue_chunk32_fast<OUT>(v, crow + col0, bias_base + i * 32, e);
             else
@@ -199,26 +216,28 @@ __device__ __forceinline__ void owner_row_chunks(uint32_t t_base, int col_base, 
         }
     }
     __syncwarp();
+    return ok;
 }
 
 template <int AB, int OUT, int STAGES, int BNH>
 __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const TcArgs args) {
+                             const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
     using Cfg = PairConfig<AB, STAGES, BNH>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, SWZ = Cfg::SWZ;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFF);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *mma_done = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *cbar = mma_done + 1;  // one per epilogue warp: its C box has landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cbar + Cfg::EPI_WARPS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *bias_stage = reinterpret_cast<float *>(smem + STAGES * Cfg::STAGE_BYTES + Cfg::BAR_BYTES);
+    float *bias_stage = reinterpret_cast<float *>(smem + Cfg::BIAS_OFF);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -238,10 +257,12 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             mbar_init(&tempty[b], 2 * Cfg::EPI_WARPS);  // both CTAs' epilogue warps (leader's copy is used)
         }
         mbar_init(mma_done, 1);
+        for (int w = 0; w < Cfg::EPI_WARPS; ++w) mbar_init(&cbar[w], 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (args.e.c_tma) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
@@ -388,6 +409,8 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
         const int c_end = half ? nchunks : (nchunks + 1) >> 1;
         const EpiParams &e = args.e;
         const int r = quad * 32 + lane;  // this thread's row inside the CTA's 128
+        unsigned char *cbuf = smem + Cfg::CSTAGE_OFF + ew * kStageBoxBytes;
+        uint32_t cphase = 0;
         int local = 0;
         SegmentIter it(args, cluster, nclusters);
         Segment seg;
@@ -395,7 +418,8 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
             int tm, tn;
             tile_coords(seg.tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
-            const int row = tm * 2 * BM + static_cast<int>(rank) * BM + r;
+            const int row0 = tm * 2 * BM + static_cast<int>(rank) * BM + quad * 32;  // the warp's first row
+            const int row = row0 + lane;
             const int n_tile = tn * bn;
             float *bias_s = bias_stage + (acc * Cfg::EPI_WARPS + ew) * 128;
             if (seg.kind != kSegPart)
@@ -412,7 +436,11 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             if (left < nvalid) nvalid = left;
             bool fail = false;
             if (seg.kind == kSegFull) {
-                epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, bias_s, e);
+                if (!e.c_tma)
+                    epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, bias_s, e);
+                else if (row0 < M)
+                    fail = !epilogue_rows_tma<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, e, &tmC,
+                                                      cbuf, &cbar[ew], cphase, abort_flag, args.status);
             } else if (seg.kind == kSegPart) {
                 float *slot = args.partial + (static_cast<long long>(cluster) * 2 + rank) * kPartialFloatsPerCta;
                 store_partial_chunks(t_row + c_begin * 32, c_begin, nvalid, r, slot);
@@ -432,8 +460,9 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                 }
                 const float *slot0 =
                     args.partial + (static_cast<long long>(cluster + 1) * 2 + rank) * kPartialFloatsPerCta;
-                owner_row_chunks<OUT>(t_row + c_begin * 32, col_base, c_begin, nvalid, row, row_ok, r, slot0,
-                                      2 * kPartialFloatsPerCta, ncontrib, bias_s, e);
+                fail = !owner_row_chunks<OUT>(t_row + c_begin * 32, col_base, c_begin, nvalid, row, row_ok, r, slot0,
+                                              2 * kPartialFloatsPerCta, ncontrib, bias_s, e, row0, &tmC, cbuf,
+                                              &cbar[ew], cphase, abort_flag, args.status);
                 __syncwarp();
                 if (lane == 0)
                     for (int k = 1; k <= ncontrib; ++k) args.flags[((cluster + k) * 2 + rank) * 8 + ew] = 0u;
@@ -441,7 +470,14 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tempty0_leader + 8u * acc);
+            if (__any_sync(0xffffffffu, fail)) {
+                st_shared_cluster_u32(peer_abort, 1u);
+                break;
+            }
         }
+        // Staged stores still in flight must finish before the CTA's shared memory goes.
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
     }
 
     __syncwarp();
@@ -454,7 +490,8 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
 }
 
 template <int AB, int OUT, int STAGES, int BNH = 128>
-cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, int clusters,
+cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const TcArgs &args,
+                            int clusters,
                             cudaStream_t stream) {
     using Cfg = PairConfig<AB, STAGES, BNH>;
     // What one CTA's loads of a stage occupy must fit its slots.
@@ -475,7 +512,7 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args);
 }
 
 // Largest number of two-CTA clusters of this kernel that can be resident at once.

@@ -68,9 +68,9 @@ cudaError_t launch_tf32_split(const float *src, long long rows, long long cols, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_pair_tf32x3(int out, const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args,
+cudaError_t launch_pair_tf32x3(int out, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const TcArgs &args,
                                int clusters, cudaStream_t stream) {
-    if (out == kDtF32) return launch_pair_cfg<kDtTF32x3, kDtF32, 3>(ta, tb, args, clusters, stream);
+    if (out == kDtF32) return launch_pair_cfg<kDtTF32x3, kDtF32, 3>(ta, tb, tc, args, clusters, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -25,6 +25,7 @@ struct EpiParams {
     float alpha, beta;
     int epilogue;
     int c_vec;        // C base and row pitch allow 16-byte vector access
+    int c_tma;        // pair kernel: C moves through shared memory by TMA (the kernel's C map is valid)
 };
 
 // tcgen05 path: operands come through the two tensor maps.
@@ -70,18 +71,19 @@ cudaError_t launch_tcgen05_bf16(int out, int bn, const CUtensorMap &, const CUte
                                 cudaStream_t);
 cudaError_t launch_tcgen05_e4m3(int out, int bn, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int grid,
                                 cudaStream_t);
-//   pair kernel (tile width in args.bn), `clusters` two-CTA clusters:
-cudaError_t launch_pair_f16(int out, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
+//   pair kernel (tile width in args.bn), `clusters` two-CTA clusters; the third map
+//   describes C (read only when args.e.c_tma != 0):
+cudaError_t launch_pair_f16(int out, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
                             cudaStream_t);
-cudaError_t launch_pair_bf16(int out, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
+cudaError_t launch_pair_bf16(int out, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
                              cudaStream_t);
-cudaError_t launch_pair_e4m3(int out, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
+cudaError_t launch_pair_e4m3(int out, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
                              cudaStream_t);
 int pair_max_clusters_f16(int out);
 int pair_max_clusters_bf16(int out);
 int pair_max_clusters_e4m3(int out);
 //   3xTF32 pair kernel (fp32 output) and the hi/lo split pre-pass:
-cudaError_t launch_pair_tf32x3(int out, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
+cudaError_t launch_pair_tf32x3(int out, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
                                cudaStream_t);
 int pair_max_clusters_tf32x3(int out);
 cudaError_t launch_tf32_split(const float *src, long long rows, long long cols, long long s_row, long long s_col,
