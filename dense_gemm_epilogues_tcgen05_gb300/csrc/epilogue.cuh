@@ -316,28 +316,67 @@ __device__ __forceinline__ uint32_t sw64_offset(int r, int q) {
     return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
 }
 
-// Epilogue of one 32-column chunk of the warp's 32 rows (this thread: row
-// row0 + lane, accumulators v), output columns col0 .. col0+31, bias of those
-// columns at bias_chunk (16-byte aligned, shared memory).  Warp-collective;
-// row0 < M and col0 < N.  Stores stay in flight when it returns; the buffer is
-// reused only after the previous store has read it.  Returns false if a wait
-// for C gave up.
+// Columns h*PER .. h*PER+PER-1 of one 32-column chunk (PER = 64 bytes of
+// output): beta*C with C read from this thread's row of the staged box,
+// bias, GELU, and the result packed back into the same row of the box.
+// v holds alpha*acc on entry.
 template <int OUT>
-__device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, int row0, const float *bias_chunk,
-                                                     const EpiParams &e, const CUtensorMap *tmC, unsigned char *buf,
-                                                     uint64_t *cbar, uint32_t &cphase, volatile int *abort_flag,
-                                                     unsigned int *status) {
-    constexpr int ES = static_cast<int>(sizeof(typename Elem<OUT>::T));
-    constexpr int PER = 64 / ES;  // columns per box row
-    constexpr int NSUB = 32 / PER;
+__device__ __forceinline__ void box_math(float (&v)[32], int h, unsigned char *box, const float *bias_chunk,
+                                         const EpiParams &e) {
+    constexpr int PER = 64 / static_cast<int>(sizeof(typename Elem<OUT>::T));
     constexpr int PV = Vec16<OUT>::kPerVec;
     const int lane = threadIdx.x & 31;
-    const uint64_t alpha2 = f2_splat(e.alpha);
+    if (e.beta != 0.0f) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float c[PV];
+            Vec16<OUT>::unpack(*reinterpret_cast<const uint4 *>(box + sw64_offset(lane, q)), c);
+#pragma unroll
+            for (int t = 0; t < PV; ++t) v[h * PER + q * PV + t] = fmaf(e.beta, c[t], v[h * PER + q * PV + t]);
+        }
+    }
+    if (e.epilogue != kEpiNone) {
+        const float4 *b4 = reinterpret_cast<const float4 *>(bias_chunk + h * PER);
+#pragma unroll
+        for (int q = 0; q < PER / 4; ++q) {
+            const float4 b = b4[q];
+            v[h * PER + 4 * q] += b.x; v[h * PER + 4 * q + 1] += b.y;
+            v[h * PER + 4 * q + 2] += b.z; v[h * PER + 4 * q + 3] += b.w;
+        }
+        if (e.epilogue == kEpiBiasGelu) {
+#pragma unroll
+            for (int j = 0; j < PER; j += 2) gelu_erf2(v[h * PER + j], v[h * PER + j + 1]);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(box + sw64_offset(lane, q)) = Vec16<OUT>::pack(&v[h * PER + q * PV]);
+}
+
+__device__ __forceinline__ void scale_alpha(float (&v)[32], float alpha) {
+    const uint64_t alpha2 = f2_splat(alpha);
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         const uint64_t r = f2_mul(f2_pack(v[j], v[j + 1]), alpha2);
         f2_unpack(r, v[j], v[j + 1]);
     }
+}
+
+// Epilogue of one 32-column chunk of the warp's 32 rows (this thread: row
+// row0 + lane, accumulators v), output columns col0 .. col0+31, bias of those
+// columns at bias_chunk (16-byte aligned, shared memory), through the warp's
+// one staged box.  Warp-collective; row0 < M and col0 < N.  Stores stay in
+// flight when it returns; the box is reused only after the previous store has
+// read it.  Returns false if a wait for C gave up.
+template <int OUT>
+__device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, int row0, const float *bias_chunk,
+                                                     const EpiParams &e, const CUtensorMap *tmC, unsigned char *buf,
+                                                     uint64_t *cbar, uint32_t &cphase, volatile int *abort_flag,
+                                                     unsigned int *status) {
+    constexpr int PER = 64 / static_cast<int>(sizeof(typename Elem<OUT>::T));
+    constexpr int NSUB = 32 / PER;
+    const int lane = threadIdx.x & 31;
+    scale_alpha(v, e.alpha);
 #pragma unroll
     for (int h = 0; h < NSUB; ++h) {
         const int x = col0 + h * PER;
@@ -352,30 +391,8 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
             const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
             if (!__all_sync(0xffffffffu, got)) return false;
             cphase ^= 1u;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float c[PV];
-                Vec16<OUT>::unpack(*reinterpret_cast<const uint4 *>(buf + sw64_offset(lane, q)), c);
-#pragma unroll
-                for (int t = 0; t < PV; ++t) v[h * PER + q * PV + t] = fmaf(e.beta, c[t], v[h * PER + q * PV + t]);
-            }
         }
-        if (e.epilogue != kEpiNone) {
-            const float4 *b4 = reinterpret_cast<const float4 *>(bias_chunk + h * PER);
-#pragma unroll
-            for (int q = 0; q < PER / 4; ++q) {
-                const float4 b = b4[q];
-                v[h * PER + 4 * q] += b.x; v[h * PER + 4 * q + 1] += b.y;
-                v[h * PER + 4 * q + 2] += b.z; v[h * PER + 4 * q + 3] += b.w;
-            }
-            if (e.epilogue == kEpiBiasGelu) {
-#pragma unroll
-                for (int j = 0; j < PER; j += 2) gelu_erf2(v[h * PER + j], v[h * PER + j + 1]);
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4 *>(buf + sw64_offset(lane, q)) = Vec16<OUT>::pack(&v[h * PER + q * PV]);
+        box_math<OUT>(v, h, buf, bias_chunk, e);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -387,9 +404,9 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
 }
 
 // Staged epilogue of one warp's rows row0 .. row0+31 and chunks 0 .. nvalid-1
-// of 32 columns from TMEM column address t_base / output column col_base (the
-// TMEM load of chunk i+1 in flight while chunk i is processed).  Warp-collective.
-template <int OUT, int MAXC>
+// of 32 columns from TMEM column address t_base / output column col_base,
+// through the warp's one box.  Warp-collective.
+template <int OUT>
 __device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base, int nvalid, int row0,
                                                   const float *bias_base, const EpiParams &e, const CUtensorMap *tmC,
                                                   unsigned char *buf, uint64_t *cbar, uint32_t &cphase,
@@ -410,6 +427,67 @@ __device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base,
     }
     __syncwarp();
     return ok;
+}
+
+// The same for a CTA's last tile, when its operand ring is idle: every box of
+// the warp gets its own slot in `area` (box b of chunk i, part h at slot
+// i*NSUB + h), all C boxes are requested at once and no store waits for a
+// slot to be read, so the tail of the kernel is not a chain of round trips.
+template <int OUT>
+__device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col_base, int nvalid, int row0,
+                                                        const float *bias_base, const EpiParams &e,
+                                                        const CUtensorMap *tmC, unsigned char *area, uint64_t *cbar,
+                                                        uint32_t &cphase, volatile int *abort_flag,
+                                                        unsigned int *status) {
+    constexpr int PER = 64 / static_cast<int>(sizeof(typename Elem<OUT>::T));
+    constexpr int NSUB = 32 / PER;
+    const int lane = threadIdx.x & 31;
+    if (nvalid <= 0) return true;
+    if (e.beta != 0.0f) {
+        if (lane == 0) {
+            uint32_t nbox = 0;
+            for (int i = 0; i < nvalid; ++i)
+                for (int h = 0; h < NSUB; ++h)
+                    if (col_base + i * 32 + h * PER < e.N) ++nbox;
+            mbar_arrive_expect_tx(cbar, nbox * kStageBoxBytes);
+            for (int i = 0; i < nvalid; ++i)
+                for (int h = 0; h < NSUB; ++h) {
+                    const int x = col_base + i * 32 + h * PER;
+                    if (x < e.N) tma_load_2d(area + (i * NSUB + h) * kStageBoxBytes, tmC, cbar, x, row0);
+                }
+        }
+        const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
+        if (!__all_sync(0xffffffffu, got)) return false;
+        cphase ^= 1u;
+    }
+#pragma unroll 1
+    for (int i = 0; i < nvalid; ++i) {
+        uint32_t raw[32];
+        __syncwarp();
+        tmem_ld_issue(t_base + i * 32, raw);
+        tmem_ld_wait(raw);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
+        scale_alpha(v, e.alpha);
+#pragma unroll
+        for (int h = 0; h < NSUB; ++h) {
+            const int x = col_base + i * 32 + h * PER;
+            if (x < e.N) box_math<OUT>(v, h, area + (i * NSUB + h) * kStageBoxBytes, bias_base + i * 32, e);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < NSUB; ++h) {
+                const int x = col_base + i * 32 + h * PER;
+                if (x < e.N) tma_store_2d(tmC, area + (i * NSUB + h) * kStageBoxBytes, x, row0);
+            }
+            bulk_commit();
+        }
+    }
+    __syncwarp();
+    return true;
 }
 
 // Epilogue inputs of one warp's columns, fetched before the accumulator is

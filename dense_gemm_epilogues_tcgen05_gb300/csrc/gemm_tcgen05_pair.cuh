@@ -71,6 +71,10 @@ struct PairConfig {
     static constexpr int BIAS_OFF = BAR_OFF + BAR_BYTES;
     static constexpr int SMEM_BYTES = 1024 + BIAS_OFF + BIAS_BYTES;
     static_assert((2 * STAGES + 5 + EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barriers fit their slot");
+    // A CTA's last tile stages its C boxes in the idle ring: per warp up to 4
+    // chunks x 2 boxes (fp32 output) of 2 KB.
+    static constexpr int BURST_BYTES_PER_WARP = 4 * 2 * kStageBoxBytes;
+    static_assert(EPI_WARPS * BURST_BYTES_PER_WARP <= STAGES * STAGE_BYTES, "last-tile boxes fit the ring");
     static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
     static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the pair allocates all 512 TMEM columns");
 };
@@ -272,6 +276,10 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
     tc_fence_before();
     cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
     tc_fence_after();
+    // Everything above touches only this CTA's own resources, so it may overlap
+    // the previous grid in the stream; every global-memory access below waits.
+    grid_dep_wait();
+    grid_dep_launch();
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
     const uint32_t tempty0_leader = mapa_shared(smem_u32(&tempty[0]), 0);
@@ -416,6 +424,11 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
         Segment seg;
         for (; it.next(seg); ++local) {
             const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
+            SegmentIter peek = it;
+            Segment after;
+            // After the last segment's accumulator is ready, every MMA has
+            // completed and no load is pending: the operand ring is idle.
+            const bool last = !peek.next(after);
             int tm, tn;
             tile_coords(seg.tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
             const int row0 = tm * 2 * BM + static_cast<int>(rank) * BM + quad * 32;  // the warp's first row
@@ -438,9 +451,13 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             if (seg.kind == kSegFull) {
                 if (!e.c_tma)
                     epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, bias_s, e);
+                else if (row0 < M && last)
+                    fail = !epilogue_rows_tma_burst<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, e,
+                                                         &tmC, smem + ew * Cfg::BURST_BYTES_PER_WARP, &cbar[ew],
+                                                         cphase, abort_flag, args.status);
                 else if (row0 < M)
-                    fail = !epilogue_rows_tma<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, e, &tmC,
-                                                      cbuf, &cbar[ew], cphase, abort_flag, args.status);
+                    fail = !epilogue_rows_tma<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, e, &tmC,
+                                                   cbuf, &cbar[ew], cphase, abort_flag, args.status);
             } else if (seg.kind == kSegPart) {
                 float *slot = args.partial + (static_cast<long long>(cluster) * 2 + rank) * kPartialFloatsPerCta;
                 store_partial_chunks(t_row + c_begin * 32, c_begin, nvalid, r, slot);
@@ -505,13 +522,17 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // The prologue may start while the previous grid drains (the kernel waits
+    // for it before its first global-memory access).
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args);
 }
 

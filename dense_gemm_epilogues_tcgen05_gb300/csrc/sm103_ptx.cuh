@@ -299,6 +299,13 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// Programmatic dependent launch.  grid_dep_wait blocks until the grids this
+// one depends on have completed and their memory is visible (a no-op when the
+// launch had no such dependency); grid_dep_launch lets the next grid in the
+// stream start launching (its own grid_dep_wait still waits for this grid).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void sleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
 // TMA load into this CTA's shared memory whose completion is counted on an
