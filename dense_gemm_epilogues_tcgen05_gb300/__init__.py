@@ -22,7 +22,8 @@ __all__ = [
     "PATH_NOOP", "PATH_EPILOGUE_ONLY", "PATH_TCGEN05", "PATH_SIMT",
     "TILE_AUTO", "TILE_1SM_256", "TILE_1SM_128", "TILE_PAIR",
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
-    "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K",
+    "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K", "ORDER_AUTO", "ORDER_AS_GIVEN", "ORDER_TRANSPOSED",
+    "gemm_set_operand_order",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
@@ -37,6 +38,8 @@ PATH_NOOP, PATH_EPILOGUE_ONLY, PATH_TCGEN05, PATH_SIMT = 0, 1, 2, 3
 TILE_AUTO, TILE_1SM_256, TILE_1SM_128, TILE_PAIR = 0, 1, 2, 3
 # gemm_schedule_t
 SCHED_AUTO, SCHED_TILES, SCHED_STREAM_K = 0, 1, 2
+# gemm_operand_order_t
+ORDER_AUTO, ORDER_AS_GIVEN, ORDER_TRANSPOSED = 0, 1, 2
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -72,6 +75,8 @@ lib.gemm_wait_selftest.restype = _int
 lib.gemm_wait_selftest.argtypes = [_vp, ctypes.c_uint64, _vp]
 lib.gemm_set_schedule.restype = _int
 lib.gemm_set_schedule.argtypes = [_int]
+lib.gemm_set_operand_order.restype = _int
+lib.gemm_set_operand_order.argtypes = [_int]
 lib.gemm_device_status.restype = _int
 lib.gemm_device_status.argtypes = [_vp]
 lib.gemm_status_string.restype = ctypes.c_char_p
@@ -165,6 +170,11 @@ def gemm_set_tile_policy(policy, bn=0) -> int:
 def gemm_set_schedule(schedule) -> int:
     """Process-wide schedule of the pair kernel (SCHED_*)."""
     return _check(lib.gemm_set_schedule(schedule), "gemm_set_schedule")
+
+
+def gemm_set_operand_order(order) -> int:
+    """Process-wide operand order of the pair kernel (ORDER_*): whether it may compute C^T = B^T A^T."""
+    return _check(lib.gemm_set_operand_order(order), "gemm_set_operand_order")
 
 
 def gemm_query_tile(M, N, K, ab_dtype, c_dtype):

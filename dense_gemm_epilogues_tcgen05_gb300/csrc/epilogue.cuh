@@ -362,21 +362,122 @@ __device__ __forceinline__ void scale_alpha(float (&v)[32], float alpha) {
     }
 }
 
+// ------------------------------------------------ transposed accumulators --
+// When the kernel computes C^T = B^T A^T (so that an N-contiguous B becomes
+// the MMA's A operand), TMEM lane l of a warp holds output column n0 + l and
+// its 32 accumulator columns are output rows m0 .. m0+31: the warp holds the
+// 32 x 32 block C[m0.., n0..] transposed.  The staged box is still C's own
+// 32-row x 64-byte box (16-bit output only): lanes 2p and 2p+1 trade values
+// with one shuffle per row pair so that each writes whole 32-bit words
+// (columns 2p, 2p+1) of alternate rows, two rows per warp instruction.
+
+// Byte offset of a 32-bit word inside a 64-byte-swizzled box.
+__device__ __forceinline__ uint32_t sw64_word(uint32_t byte) { return byte ^ (((byte >> 7) & 3u) << 4); }
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2_out(float lo, float hi) {
+    uint32_t w;
+    if constexpr (OUT == kDtF16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        w = *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        w = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return w;
+}
+
+template <int OUT>
+__device__ __forceinline__ float2 unpack2_out(uint32_t w) {
+    if constexpr (OUT == kDtF16) {
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    } else {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+    }
+}
+
+// Transposed counterpart of box_math for one whole chunk (v = alpha*acc of
+// output column n0+lane, rows m0 .. m0+31): beta*C from the box, the column's
+// bias, GELU, and the result written back into the box.
+template <int OUT>
+__device__ __forceinline__ void box_math_t(float (&v)[32], unsigned char *box, float bias_lane, const EpiParams &e) {
+    static_assert(OUT == kDtF16 || OUT == kDtBF16, "transposed staging is for 16-bit outputs");
+    const int lane = threadIdx.x & 31;
+    const uint32_t odd = lane & 1u;
+    const uint32_t col_bytes = (lane >> 1) * 4u;
+    if (e.beta != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t own = *reinterpret_cast<const uint32_t *>(box + sw64_word((2 * i + odd) * 64u + col_bytes));
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, own, 1);
+            const float2 a = unpack2_out<OUT>(own), b = unpack2_out<OUT>(other);
+            // even lane: own word is row 2i, partner's row 2i+1, low halves are its column
+            const float c_even = odd ? b.y : a.x;  // row 2i
+            const float c_odd = odd ? a.y : b.x;   // row 2i+1
+            v[2 * i] = fmaf(e.beta, c_even, v[2 * i]);
+            v[2 * i + 1] = fmaf(e.beta, c_odd, v[2 * i + 1]);
+        }
+    }
+    if (e.epilogue != kEpiNone) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += bias_lane;
+        if (e.epilogue == kEpiBiasGelu) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) gelu_erf2(v[j], v[j + 1]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        // send the row the partner writes, keep the row this lane writes
+        const float send = odd ? v[2 * i] : v[2 * i + 1];
+        const float keep = odd ? v[2 * i + 1] : v[2 * i];
+        const float got = __shfl_xor_sync(0xffffffffu, send, 1);
+        const uint32_t w = odd ? pack2_out<OUT>(got, keep) : pack2_out<OUT>(keep, got);
+        *reinterpret_cast<uint32_t *>(box + sw64_word((2 * i + odd) * 64u + col_bytes)) = w;
+    }
+}
+
 // Epilogue of one 32-column chunk of the warp's 32 rows (this thread: row
 // row0 + lane, accumulators v), output columns col0 .. col0+31, bias of those
 // columns at bias_chunk (16-byte aligned, shared memory), through the warp's
 // one staged box.  Warp-collective; row0 < M and col0 < N.  Stores stay in
 // flight when it returns; the box is reused only after the previous store has
 // read it.  Returns false if a wait for C gave up.
+// With e.swap the accumulators are transposed (TMEM lanes are output columns
+// row0 + lane, chunk columns are output rows col0 ..; bias_lane is the
+// lane's column bias); see box_math_t.
 template <int OUT>
 __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, int row0, const float *bias_chunk,
-                                                     const EpiParams &e, const CUtensorMap *tmC, unsigned char *buf,
-                                                     uint64_t *cbar, uint32_t &cphase, volatile int *abort_flag,
-                                                     unsigned int *status) {
+                                                     float bias_lane, const EpiParams &e, const CUtensorMap *tmC,
+                                                     unsigned char *buf, uint64_t *cbar, uint32_t &cphase,
+                                                     volatile int *abort_flag, unsigned int *status) {
     constexpr int PER = 64 / static_cast<int>(sizeof(typename Elem<OUT>::T));
     constexpr int NSUB = 32 / PER;
     const int lane = threadIdx.x & 31;
     scale_alpha(v, e.alpha);
+    if constexpr (OUT != kDtF32) {
+        if (e.swap) {
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            if (e.beta != 0.0f) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(cbar, kStageBoxBytes);
+                    tma_load_2d(buf, tmC, cbar, row0, col0);
+                }
+                const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
+                if (!__all_sync(0xffffffffu, got)) return false;
+                cphase ^= 1u;
+            }
+            box_math_t<OUT>(v, buf, bias_lane, e);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tmC, buf, row0, col0);
+                bulk_commit();
+            }
+            return true;
+        }
+    }
 #pragma unroll
     for (int h = 0; h < NSUB; ++h) {
         const int x = col0 + h * PER;
@@ -408,9 +509,9 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
 // through the warp's one box.  Warp-collective.
 template <int OUT>
 __device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base, int nvalid, int row0,
-                                                  const float *bias_base, const EpiParams &e, const CUtensorMap *tmC,
-                                                  unsigned char *buf, uint64_t *cbar, uint32_t &cphase,
-                                                  volatile int *abort_flag, unsigned int *status) {
+                                                  const float *bias_base, float bias_lane, const EpiParams &e,
+                                                  const CUtensorMap *tmC, unsigned char *buf, uint64_t *cbar,
+                                                  uint32_t &cphase, volatile int *abort_flag, unsigned int *status) {
     bool ok = true;
 #pragma unroll 1
     for (int i = 0; i < nvalid; ++i) {
@@ -422,8 +523,8 @@ __device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base,
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
         if (ok)
-            ok = epilogue_chunk32_tma<OUT>(v, col_base + i * 32, row0, bias_base + i * 32, e, tmC, buf, cbar,
-                                           cphase, abort_flag, status);
+            ok = epilogue_chunk32_tma<OUT>(v, col_base + i * 32, row0, bias_base + i * 32, bias_lane, e, tmC, buf,
+                                           cbar, cphase, abort_flag, status);
     }
     __syncwarp();
     return ok;
@@ -435,7 +536,7 @@ __device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base,
 // slot to be read, so the tail of the kernel is not a chain of round trips.
 template <int OUT>
 __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col_base, int nvalid, int row0,
-                                                        const float *bias_base, const EpiParams &e,
+                                                        const float *bias_base, float bias_lane, const EpiParams &e,
                                                         const CUtensorMap *tmC, unsigned char *area, uint64_t *cbar,
                                                         uint32_t &cphase, volatile int *abort_flag,
                                                         unsigned int *status) {
@@ -443,6 +544,41 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
     constexpr int NSUB = 32 / PER;
     const int lane = threadIdx.x & 31;
     if (nvalid <= 0) return true;
+    if constexpr (OUT != kDtF32) {
+        if (e.swap) {
+            // transposed: chunk i is the box at (x = row0, y = col_base + 32 i), slot i
+            if (e.beta != 0.0f) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(cbar, static_cast<uint32_t>(nvalid) * kStageBoxBytes);
+                    for (int i = 0; i < nvalid; ++i)
+                        tma_load_2d(area + i * kStageBoxBytes, tmC, cbar, row0, col_base + i * 32);
+                }
+                const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
+                if (!__all_sync(0xffffffffu, got)) return false;
+                cphase ^= 1u;
+            }
+#pragma unroll 1
+            for (int i = 0; i < nvalid; ++i) {
+                uint32_t raw[32];
+                __syncwarp();
+                tmem_ld_issue(t_base + i * 32, raw);
+                tmem_ld_wait(raw);
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
+                scale_alpha(v, e.alpha);
+                box_math_t<OUT>(v, area + i * kStageBoxBytes, bias_lane, e);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmC, area + i * kStageBoxBytes, row0, col_base + i * 32);
+                    bulk_commit();
+                }
+            }
+            __syncwarp();
+            return true;
+        }
+    }
     if (e.beta != 0.0f) {
         if (lane == 0) {
             uint32_t nbox = 0;
@@ -488,6 +624,27 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
     }
     __syncwarp();
     return true;
+}
+
+// Transposed counterpart of epilogue_prefetch: the warp's block of C is rows
+// col_base .. col_base + 32*nchunk - 1 (within M) by columns row0 .. row0+31
+// (within N); each of those rows' 64 bytes is prefetched into L2 when beta
+// != 0.  Returns this lane's column bias.  Warp-collective.
+template <int OUT>
+__device__ __forceinline__ float epilogue_prefetch_t(int col_base, int nchunk, int row0, const EpiParams &e) {
+    using OutT = typename Elem<OUT>::T;
+    const int lane = threadIdx.x & 31;
+    const int n = row0 + lane;
+    const float b = (e.epilogue != kEpiNone && n < e.N) ? e.bias[n] : 0.0f;
+    if (e.beta != 0.0f && row0 < e.N) {
+        const int m_end = min(col_base + nchunk * 32, e.M);
+        for (int m = col_base + lane; m < m_end; m += 32) {
+            const OutT *p = reinterpret_cast<const OutT *>(e.C) + (long long)m * e.ldc + row0;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        }
+    }
+    __syncwarp();
+    return b;
 }
 
 // Epilogue inputs of one warp's columns, fetched before the accumulator is

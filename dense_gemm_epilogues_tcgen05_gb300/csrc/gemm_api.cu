@@ -288,6 +288,7 @@ size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 std::atomic<int> g_tile_policy{GEMM_TILE_AUTO};
 std::atomic<int> g_tile_policy_bn{0};
 std::atomic<int> g_schedule{GEMM_SCHED_AUTO};
+std::atomic<int> g_operand_order{GEMM_ORDER_AUTO};
 std::atomic<unsigned int> g_epoch{0};
 
 // Stream-K workspace layout for `clusters` pairs: partial sums, then flags.
@@ -443,6 +444,7 @@ EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alp
     const bool b_al = epi == GEMM_EPI_NONE || (reinterpret_cast<uintptr_t>(bias) & 15u) == 0;
     e.c_vec = (c_al && b_al) ? 1 : 0;
     e.c_tma = 0;  // set by the pair-kernel launch once C's tensor map is encoded
+    e.swap = 0;   // set by the pair-kernel launch when it computes C^T = B^T A^T
     return e;
 }
 
@@ -572,19 +574,42 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
         return launch_simt(ab_dtype, c_dtype, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
-    // tcgen05 path: one SM or a pair of SMs per tile, by the cost model.
+    // tcgen05 path: one SM or a pair of SMs per tile, by the cost model.  The
+    // pair kernel may run the transposed problem C^T = B^T A^T (kernel rows =
+    // output columns), see gemm_operand_order_t.
     const int max_clusters = device_max_clusters(dev, ab_dtype, c_dtype);
-    const TileChoice tc = choose_tile(M, N, dev->num_sms, max_clusters, g_tile_policy.load(),
-                                      g_tile_policy_bn.load());
+    CUtensorMap tcm;
+    std::memset(&tcm, 0, sizeof(tcm));
+    const bool c_tma = encode_c(&tcm, c_dtype, C, M, N, ldc);
+    const int order = g_operand_order.load();
+    bool swap = c_tma && c_dtype != GEMM_F32 && order != GEMM_ORDER_AS_GIVEN &&
+                (order == GEMM_ORDER_TRANSPOSED ||
+                 (plan.b.mn_major && !plan.a.mn_major && ab_dtype != GEMM_E4M3));
+    TileChoice tc;
+    if (swap) {
+        tc = choose_tile(N, M, dev->num_sms, max_clusters, g_tile_policy.load(), g_tile_policy_bn.load());
+        if (tc.kind != 2) swap = false;  // the one-SM kernel runs the problem as given
+    }
+    if (!swap) tc = choose_tile(M, N, dev->num_sms, max_clusters, g_tile_policy.load(), g_tile_policy_bn.load());
+    // The kernel's problem: Mk x Nk, first operand (Mk x K), second (Nk x K).
+    const int64_t Mk = swap ? N : M, Nk = swap ? M : N;
+    const Operand &op1 = swap ? plan.b : plan.a, &op2 = swap ? plan.a : plan.b;
     const int bk = 128 / es;
     const int64_t rows_per_tile = tc.kind == 2 ? 256 : 128;
-    const int64_t tiles_m = (M + rows_per_tile - 1) / rows_per_tile;
-    const int64_t tiles_n = (N + tc.bn - 1) / tc.bn;
-    // B's box covers this SM's columns: the whole tile (one SM) or half of it (pair).
+    const int64_t tiles_m = (Mk + rows_per_tile - 1) / rows_per_tile;
+    const int64_t tiles_n = (Nk + tc.bn - 1) / tc.bn;
+    // The second operand's box covers this SM's columns: the whole tile (one SM) or half of it (pair).
     const uint32_t b_box = static_cast<uint32_t>(tc.kind == 2 ? tc.bn / 2 : tc.bn);
     CUtensorMap ta, tb;
-    if ((st = encode_operand(&ta, ab_dtype, A, plan.a, M, K, a_stride_m, a_stride_k, 128)) != GEMM_OK) return st;
-    if ((st = encode_operand(&tb, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, b_box)) != GEMM_OK) return st;
+    if (swap) {
+        if ((st = encode_operand(&ta, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, 128)) != GEMM_OK) return st;
+        if ((st = encode_operand(&tb, ab_dtype, A, plan.a, M, K, a_stride_m, a_stride_k, b_box)) != GEMM_OK)
+            return st;
+    } else {
+        if ((st = encode_operand(&ta, ab_dtype, A, plan.a, M, K, a_stride_m, a_stride_k, 128)) != GEMM_OK) return st;
+        if ((st = encode_operand(&tb, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, b_box)) != GEMM_OK)
+            return st;
+    }
     TcArgs t;
     t.e = e;
     t.K = static_cast<int>(K);
@@ -593,12 +618,12 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     t.num_tiles = static_cast<int>(tiles_m * tiles_n);
     t.num_kb = static_cast<int>((K + bk - 1) / bk);
     t.group_m = 8;
-    t.a_mn_major = plan.a.mn_major ? 1u : 0u;
-    t.b_mn_major = plan.b.mn_major ? 1u : 0u;
+    t.a_mn_major = op1.mn_major ? 1u : 0u;
+    t.b_mn_major = op2.mn_major ? 1u : 0u;
     t.status = dev->status;
     t.bn = tc.bn;
     const uint32_t swz = 128u / es;
-    const uint32_t b_bytes = plan.b.mn_major ? ((b_box + swz - 1) / swz) * 128u * bk : b_box * 128u;
+    const uint32_t b_bytes = op2.mn_major ? ((b_box + swz - 1) / swz) * 128u * bk : b_box * 128u;
     t.stage_tx = 128u * 128u + b_bytes;
     t.dp_tiles = t.num_tiles;
     t.sk_units = 0;
@@ -618,15 +643,20 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
             t.flags = reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + partial_bytes(max_clusters));
             t.epoch = next_epoch();
         }
-        CUtensorMap tcm;
-        std::memset(&tcm, 0, sizeof(tcm));
-        t.e.c_tma = encode_c(&tcm, c_dtype, C, M, N, ldc) ? 1 : 0;
+        t.e.c_tma = c_tma ? 1 : 0;
+        t.e.swap = swap ? 1 : 0;
         err = launch_pair(ab_dtype, c_dtype, ta, tb, tcm, t, clusters, s);
     } else {
         const int grid = static_cast<int>(t.num_tiles < dev->num_sms ? t.num_tiles : dev->num_sms);
         err = launch_tc(ab_dtype, c_dtype, tc.bn, ta, tb, t, grid, s);
     }
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_set_operand_order(gemm_operand_order_t order) {
+    if (order < GEMM_ORDER_AUTO || order > GEMM_ORDER_TRANSPOSED) return GEMM_ERR_INVALID_ARG;
+    g_operand_order.store(order);
+    return GEMM_OK;
 }
 
 gemm_status_t gemm_set_tile_policy(gemm_tile_policy_t policy, int bn) {

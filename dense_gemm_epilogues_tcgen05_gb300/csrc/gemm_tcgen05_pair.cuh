@@ -185,7 +185,7 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
                                                  int ncontrib, const float *bias_base, const EpiParams &e,
                                                  int row0, const CUtensorMap *tmC, unsigned char *cbuf,
                                                  uint64_t *cbar, uint32_t &cphase, volatile int *abort_flag,
-                                                 unsigned int *status) {
+                                                 unsigned int *status, float bias_lane) {
     using OutT = typename Elem<OUT>::T;
     OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
     bool ok = true;
@@ -209,9 +209,9 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
         }
         const int col0 = col_base + i * 32;
         if (e.c_tma) {
-            if (ok && row0 < e.M)
-                ok = epilogue_chunk32_tma<OUT>(v, col0, row0, bias_base + i * 32, e, tmC, cbuf, cbar, cphase,
-                                               abort_flag, status);
+            if (ok && row0 < (e.swap ? e.N : e.M))
+                ok = epilogue_chunk32_tma<OUT>(v, col0, row0, bias_base + i * 32, bias_lane, e, tmC, cbuf, cbar,
+                                               cphase, abort_flag, status);
         } else if (row_ok) {
             if (e.c_vec && col0 + 32 <= e.N)
                 epilogue_chunk32_fast<OUT>(v, crow + col0, bias_base + i * 32, e);
@@ -431,33 +431,41 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             const bool last = !peek.next(after);
             int tm, tn;
             tile_coords(seg.tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
-            const int row0 = tm * 2 * BM + static_cast<int>(rank) * BM + quad * 32;  // the warp's first row
+            // Accumulator rows (TMEM lanes) and columns: output rows and columns,
+            // or output columns and rows when the kernel computes C^T (e.swap).
+            const int row0 = tm * 2 * BM + static_cast<int>(rank) * BM + quad * 32;  // the warp's first lane row
             const int row = row0 + lane;
             const int n_tile = tn * bn;
             float *bias_s = bias_stage + (acc * Cfg::EPI_WARPS + ew) * 128;
-            if (seg.kind != kSegPart)
-                epilogue_prefetch<OUT>(bias_s, n_tile + c_begin * 32, c_end - c_begin, row, row < M, e);
+            float bias_lane = 0.0f;
+            if (seg.kind != kSegPart) {
+                if (e.swap)
+                    bias_lane = epilogue_prefetch_t<OUT>(n_tile + c_begin * 32, c_end - c_begin, row0, e);
+                else
+                    epilogue_prefetch<OUT>(bias_s, n_tile + c_begin * 32, c_end - c_begin, row, row < M, e);
+            }
             const bool got = pair_wait(&tfull[acc], acc_phase, abort_flag, args.status, peer_abort);
             if (__any_sync(0xffffffffu, !got)) break;
             tc_fence_after();
-            const bool row_ok = row < M;
+            const int lane_extent = e.swap ? N : M, col_extent = e.swap ? M : N;
+            const bool row_ok = row < lane_extent;
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * Cfg::ACC_STRIDE;
             const int col_base = n_tile + c_begin * 32;
             int nvalid = c_end - c_begin;
-            const int left = (N - col_base + 31) >> 5;  // chunks that start inside the matrix
+            const int left = (col_extent - col_base + 31) >> 5;  // chunks that start inside the matrix
             if (left < nvalid) nvalid = left;
             bool fail = false;
             if (seg.kind == kSegFull) {
                 if (!e.c_tma)
                     epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, bias_s, e);
-                else if (row0 < M && last)
-                    fail = !epilogue_rows_tma_burst<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, e,
-                                                         &tmC, smem + ew * Cfg::BURST_BYTES_PER_WARP, &cbar[ew],
-                                                         cphase, abort_flag, args.status);
-                else if (row0 < M)
-                    fail = !epilogue_rows_tma<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, e, &tmC,
-                                                   cbuf, &cbar[ew], cphase, abort_flag, args.status);
+                else if (row0 < lane_extent && last)
+                    fail = !epilogue_rows_tma_burst<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s,
+                                                         bias_lane, e, &tmC, smem + ew * Cfg::BURST_BYTES_PER_WARP,
+                                                         &cbar[ew], cphase, abort_flag, args.status);
+                else if (row0 < lane_extent)
+                    fail = !epilogue_rows_tma<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, bias_lane, e,
+                                                   &tmC, cbuf, &cbar[ew], cphase, abort_flag, args.status);
             } else if (seg.kind == kSegPart) {
                 float *slot = args.partial + (static_cast<long long>(cluster) * 2 + rank) * kPartialFloatsPerCta;
                 store_partial_chunks(t_row + c_begin * 32, c_begin, nvalid, r, slot);
@@ -479,7 +487,7 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                     args.partial + (static_cast<long long>(cluster + 1) * 2 + rank) * kPartialFloatsPerCta;
                 fail = !owner_row_chunks<OUT>(t_row + c_begin * 32, col_base, c_begin, nvalid, row, row_ok, r, slot0,
                                               2 * kPartialFloatsPerCta, ncontrib, bias_s, e, row0, &tmC, cbuf,
-                                              &cbar[ew], cphase, abort_flag, args.status);
+                                              &cbar[ew], cphase, abort_flag, args.status, bias_lane);
                 __syncwarp();
                 if (lane == 0)
                     for (int k = 1; k <= ncontrib; ++k) args.flags[((cluster + k) * 2 + rank) * 8 + ew] = 0u;

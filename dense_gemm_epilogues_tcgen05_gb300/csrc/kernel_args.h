@@ -26,6 +26,7 @@ struct EpiParams {
     int epilogue;
     int c_vec;        // C base and row pitch allow 16-byte vector access
     int c_tma;        // pair kernel: C moves through shared memory by TMA (the kernel's C map is valid)
+    int swap;         // pair kernel: the MMA computes C^T = B^T A^T (TMEM lanes are output columns)
 };
 
 // tcgen05 path: operands come through the two tensor maps.

@@ -154,6 +154,31 @@ typedef enum {
 gemm_status_t gemm_set_schedule(gemm_schedule_t schedule);
 
 /*
+ * Operand order of the pair kernel.  The kernel can compute C = A*B as
+ * C^T = B^T * A^T, with B's transpose as the MMA's first operand and C^T's
+ * rows written as C's columns.  On GB300 a second MMA operand that is
+ * N-contiguous (B stored K x N row-major) keeps the tensor pipe measurably
+ * less busy than a K-contiguous one (79.5 % vs 86.5 % of cycles, bf16
+ * 8192^3), so AUTO transposes exactly that case for fp16 / bf16 inputs: A
+ * K-contiguous, B N-contiguous, 16-bit output, C base and pitch usable by
+ * TMA (fp8 inputs measured no faster transposed and keep the given order).
+ * The result is the same product; only the summation order inside fp32
+ * accumulation may differ.
+ */
+typedef enum {
+    GEMM_ORDER_AUTO = 0,        /* transpose when it is the faster orientation (above) */
+    GEMM_ORDER_AS_GIVEN = 1,    /* never transpose */
+    GEMM_ORDER_TRANSPOSED = 2   /* transpose whenever the output allows (16-bit, TMA-able C) */
+} gemm_operand_order_t;
+
+/*
+ * gemm_set_operand_order -- operand order of later gemm() calls on the pair
+ * kernel, for every thread of the process.  Meant for tuning and tests.
+ * GEMM_ERR_INVALID_ARG for an unknown value; never touches the device.
+ */
+gemm_status_t gemm_set_operand_order(gemm_operand_order_t order);
+
+/*
  * gemm_query_path -- validate the same arguments gemm() takes and report, in
  * *path (host pointer), which kernel family gemm() would launch.  Launches
  * nothing and touches no device memory.  Returns the status gemm() would

@@ -71,6 +71,15 @@ def test_schedule_validation(g):
     g.gemm_set_schedule(g.SCHED_AUTO)
 
 
+def test_operand_order_validation(g):
+    for v in (g.ORDER_AUTO, g.ORDER_AS_GIVEN, g.ORDER_TRANSPOSED):
+        assert g.gemm_set_operand_order(v) == 0
+    for v in (-1, 3):
+        with pytest.raises(g.GemmError):
+            g.gemm_set_operand_order(v)
+    g.gemm_set_operand_order(g.ORDER_AUTO)
+
+
 # Fake, aligned device addresses: query_path never dereferences them.
 PA, PB, PC, PBIAS = 0x7F0000000000, 0x7F1000000000, 0x7F2000000000, 0x7F3000000000
 
