@@ -9,7 +9,9 @@ What it computes (the plain definition the kernels reach up to rounding order):
     a_ik = decode(A bytes at i*a_stride_m + k*a_stride_k)        exact in float64
     b_kj = decode(B bytes at k*b_stride_k + j*b_stride_n)
     z_ij = alpha*sum_k a_ik*b_kj + beta*c_ij + bias_j
-    y_ij = GELU(z_ij) = 0.5*z*(1 + erf(z/sqrt(2)))   (bias+GELU epilogue only)
+    y_ij = act(z_ij)                      (bias + activation epilogues)
+
+with act one of GELU (exact erf form), GELU (tanh form), SiLU and ReLU.
 
 Sources on the pages:
   * C = alpha*A*B + beta*C with the epilogue applied to the accumulator before
@@ -27,6 +29,11 @@ Sources on the pages:
   * GELU of bias-added accumulators -- Rigel abstract and section 1
     (GEMM + bias + GELU fusion).  The pages say only "GELU"; the exact erf form
     is the reading taken here.
+  * Other activations in the same place -- "Case Study: Steel's BlockMMA"
+    (the Epilogue is a pluggable functor applied to every accumulator before
+    the store).  Their formulas are the standard definitions: the tanh form of
+    GELU (Hendrycks & Gimpel, "Gaussian Error Linear Units", section 2),
+    SiLU z*sigmoid(z) (Elfwing, Uchibe & Doya 2018) and ReLU max(z, 0).
 
 The sum over k is taken with a float64 library matmul (a library primitive used
 as one step); its rounding error (~K * 2^-53 relative) is nine orders of
@@ -41,10 +48,13 @@ from typing import Optional, Sequence
 
 import numpy as np
 from scipy.special import erf as _erf
+from scipy.special import expit as _expit
 
 # Element type and epilogue codes of the C ABI (restated, not imported).
 F32, F16, BF16, E4M3 = 0, 1, 2, 3
 EPI_NONE, EPI_BIAS, EPI_BIAS_GELU = 0, 1, 2
+EPI_BIAS_GELU_TANH, EPI_BIAS_SILU, EPI_BIAS_RELU = 3, 4, 5
+EPILOGUES = (EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_GELU_TANH, EPI_BIAS_SILU, EPI_BIAS_RELU)
 
 # max_z |d/dz GELU(z)|, attained at z = sqrt(2): Phi(sqrt2) + sqrt2*phi(sqrt2).
 GELU_LIPSCHITZ = 0.5 * (1.0 + math.erf(1.0)) + math.sqrt(2.0) * math.exp(-1.0) / math.sqrt(2.0 * math.pi)
@@ -154,6 +164,44 @@ def gelu(z: np.ndarray) -> np.ndarray:
     return 0.5 * z * (1.0 + _erf(z / math.sqrt(2.0)))
 
 
+def gelu_tanh(z: np.ndarray) -> np.ndarray:
+    """GELU, tanh form: 0.5*z*(1 + tanh(sqrt(2/pi)*(z + 0.044715*z^3)))."""
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        return 0.5 * z * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (z + 0.044715 * z * z * z)))
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU (swish with beta = 1): z * sigmoid(z) = z / (1 + exp(-z))."""
+    z = np.asarray(z, dtype=np.float64)
+    return z * _expit(z)
+
+
+def relu(z: np.ndarray) -> np.ndarray:
+    """ReLU: max(z, 0); NaN stays NaN."""
+    z = np.asarray(z, dtype=np.float64)
+    return np.where(z < 0.0, 0.0, z)
+
+
+def _max_slope(f, lo: float, hi: float) -> float:
+    """max |f'| on [lo, hi] by central differences on a fine grid, refined
+    around the best point (the activations here are smooth with one maximum)."""
+    z = np.linspace(lo, hi, 200001)
+    h = 1e-6
+    d = np.abs((f(z + h) - f(z - h)) / (2 * h))
+    k = int(np.argmax(d))
+    zz = np.linspace(z[max(k - 1, 0)], z[min(k + 1, z.size - 1)], 20001)
+    return float(np.max(np.abs((f(zz + h) - f(zz - h)) / (2 * h))))
+
+
+# max_z |act'(z)| for the activations without a closed form (computed once at
+# import; pinned against an independent numerical maximisation in the tests).
+GELU_TANH_LIPSCHITZ = _max_slope(gelu_tanh, 0.0, 4.0)
+SILU_LIPSCHITZ = _max_slope(silu, 0.0, 6.0)
+
+ACTIVATIONS = {EPI_BIAS_GELU: gelu, EPI_BIAS_GELU_TANH: gelu_tanh, EPI_BIAS_SILU: silu, EPI_BIAS_RELU: relu}
+
+
 # ---------------------------------------------------------------------------
 # The reference result and its per-element error scale.
 # ---------------------------------------------------------------------------
@@ -177,7 +225,7 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
     """
     if min(M, N, K) < 0:
         raise ValueError("negative size")
-    if epilogue not in (EPI_NONE, EPI_BIAS, EPI_BIAS_GELU):
+    if epilogue not in EPILOGUES:
         raise ValueError("unknown epilogue")
     al, be = fp32_value(alpha), fp32_value(beta)
     row_sel = np.arange(M, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
@@ -193,23 +241,31 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
         c = decode(strided_codes(C, M, N, ldc, 1, row_sel), c_dtype)
         z += be * c
         D += abs(be) * np.abs(c)
-    if epilogue in (EPI_BIAS, EPI_BIAS_GELU):
+    if epilogue != EPI_NONE:
         bvals = np.asarray(bias, dtype=np.float32).astype(np.float64).reshape(-1)
         if bvals.size != N:
             raise ValueError("bias must hold N values")
         z += bvals[None, :]
         D += np.abs(bvals)[None, :]
-    y = gelu(z) if epilogue == EPI_BIAS_GELU else z
+    act = ACTIVATIONS.get(epilogue)
+    y = act(z) if act is not None else z
     return y, D
 
 
+def lipschitz(epilogue: int) -> float:
+    """max |act'| of the epilogue's activation (1 without one): how far an
+    error in z can move the output."""
+    return {EPI_BIAS_GELU: GELU_LIPSCHITZ, EPI_BIAS_GELU_TANH: GELU_TANH_LIPSCHITZ,
+            EPI_BIAS_SILU: SILU_LIPSCHITZ}.get(epilogue, 1.0)
+
+
 def normalized_error(out: np.ndarray, ref: np.ndarray, D: np.ndarray, epilogue: int) -> np.ndarray:
-    """Per-element |out - ref| / scale, scale = D (times max|GELU'| after GELU).
+    """Per-element |out - ref| / scale, scale = D times max|act'| (1 without an activation).
 
     Where the scale is 0 the reference is exact and any difference is
     infinite error; NaN anywhere in ``out`` counts as infinite error.
     """
-    scale = D * GELU_LIPSCHITZ if epilogue == EPI_BIAS_GELU else D
+    scale = D * lipschitz(epilogue)
     diff = np.abs(np.asarray(out, dtype=np.float64) - ref)
     with np.errstate(divide="ignore", invalid="ignore"):
         r = np.where(scale > 0, diff / np.where(scale > 0, scale, 1.0), np.where(diff == 0, 0.0, np.inf))

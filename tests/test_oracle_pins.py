@@ -4,7 +4,9 @@
   over every layout -- catches transposed operands, wrong strides, dropped or
   mis-signed alpha/beta/bias terms;
 * closed forms: identity, all-ones, rank-1, alpha = 0, beta-only, K = 0;
-* GELU against the normal-CDF table and its symmetry identity;
+* GELU against the normal-CDF table and its symmetry identity; the tanh form
+  of GELU, SiLU and ReLU against PyTorch's float64 CPU routines, closed forms
+  and their own identities; ReLU exact through the rational brute force;
 * the BLAS conventions (operands that must not be read are never read);
 * the error metric's behaviour, and that it flags planted mistakes.
 """
@@ -277,3 +279,79 @@ def test_metric_flags_planted_mistakes(mistake):
     # while the correct value rounded to fp16 passes
     assert oracle.max_normalized_error(_fp16_rounded(oracle.gelu(acc + 0.5 * c + bias)), y, D,
                                        wl.EPI_BIAS_GELU) <= 2e-3
+
+
+# ------------------------------------------------------------- activations --
+
+ACTS = {"gelu_tanh": (wl.EPI_BIAS_GELU_TANH, oracle.gelu_tanh), "silu": (wl.EPI_BIAS_SILU, oracle.silu),
+        "relu": (wl.EPI_BIAS_RELU, oracle.relu)}
+
+
+def test_activations_match_library_routines():
+    """PyTorch's CPU routines in float64 (a library primitive, independent code)."""
+    import torch
+    import torch.nn.functional as F
+    z = np.concatenate([np.linspace(-12, 12, 4801), [-1e4, -50.0, -1e-12, 0.0, 1e-12, 50.0, 1e4]])
+    t = torch.from_numpy(z)
+    assert np.max(np.abs(oracle.gelu_tanh(z) - F.gelu(t, approximate="tanh").numpy())) <= 1e-14 * 1e4
+    assert np.max(np.abs(oracle.silu(z) - F.silu(t).numpy()) / np.maximum(1.0, np.abs(z))) <= 1e-15
+    assert np.array_equal(oracle.relu(z), F.relu(t).numpy())
+
+
+def test_activation_closed_forms_and_identities():
+    z = np.linspace(-30, 30, 6001)
+    # sigmoid(z) + sigmoid(-z) = 1 and tanh odd  =>  f(z) - f(-z) = z for both
+    for f in (oracle.gelu_tanh, oracle.silu):
+        assert np.allclose(f(z) - f(-z), z, rtol=0, atol=1e-13)
+        assert f(np.array([0.0]))[0] == 0.0
+    # sigmoid(ln 3) = 3/4
+    assert oracle.silu(np.array([math.log(3.0)]))[0] == pytest.approx(0.75 * math.log(3.0), rel=1e-15)
+    # tanh(u) = 1/2 at u = atanh(1/2) = ln(3)/2: solve sqrt(2/pi)*(z + 0.044715 z^3) = ln(3)/2
+    from scipy.optimize import brentq
+    z0 = brentq(lambda x: math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3) - math.log(3.0) / 2, 0.0, 2.0,
+                xtol=1e-15)
+    assert oracle.gelu_tanh(np.array([z0]))[0] == pytest.approx(0.75 * z0, rel=1e-14)
+    assert oracle.relu(np.array([-2.5, -0.0, 0.0, 3.25]))[[0, 3]].tolist() == [0.0, 3.25]
+    assert np.isnan(oracle.relu(np.array([np.nan])))[0]
+
+
+@pytest.mark.parametrize("name", ["gelu_tanh", "silu"])
+def test_activation_lipschitz_constants_are_max_slopes(name):
+    """Against a plain forward-difference scan of the whole range (a different method)."""
+    epi, f = ACTS[name]
+    z = np.arange(-20.0, 20.0, 1e-5)
+    slope = np.abs(np.diff(f(z))) / 1e-5
+    assert abs(slope.max() - oracle.lipschitz(epi)) < 1e-5
+    assert oracle.lipschitz(wl.EPI_BIAS_RELU) == 1.0 and oracle.lipschitz(wl.EPI_BIAS) == 1.0
+
+
+@pytest.mark.parametrize("layout", ["NN", "TT"])
+def test_brute_force_relu_exact(layout):
+    """ReLU of an exact rational is exact: the float64 result must equal it."""
+    seed = 900
+    for M, N, K in itertools.product(range(1, 4), repeat=3):
+        seed += 3
+        p = wl.random_problem(seed, M, N, K, wl.BF16, wl.F32, layout=layout, alpha=-1.5, beta=0.5,
+                              epilogue=wl.EPI_BIAS_RELU, integer=True, ldc_pad=1)
+        y, _ = oracle.gemm_reference(**p.oracle_args())
+        exact = _frac_ref(p)
+        for i in range(M):
+            for j in range(N):
+                assert Fraction(float(y[i, j])) == max(exact[i][j], Fraction(0)), (M, N, K, i, j)
+
+
+@pytest.mark.parametrize("name", list(ACTS))
+def test_reference_applies_the_named_activation(name):
+    """gemm_reference = activation(bias epilogue's z), and a different activation is flagged."""
+    epi, f = ACTS[name]
+    p = wl.random_problem(33, 40, 48, 56, wl.F16, wl.F32, alpha=1.25, beta=0.0, epilogue=epi)
+    args = p.oracle_args()
+    y, D = oracle.gemm_reference(**args)
+    z, _ = oracle.gemm_reference(**dict(args, epilogue=wl.EPI_BIAS))
+    assert np.array_equal(y, f(z))
+    for other_name, (other_epi, g) in ACTS.items():
+        if other_name != name:
+            assert oracle.max_normalized_error(g(z), y, D, epi) > 1e-5
+    assert oracle.max_normalized_error(oracle.gelu(z), y, D, epi) > 1e-5
+    with pytest.raises(ValueError):
+        oracle.gemm_reference(**dict(args, epilogue=6))

@@ -34,6 +34,7 @@ import torch
 F32, F16, BF16, E4M3 = 0, 1, 2, 3
 # Epilogue codes, numbered like the C ABI's gemm_epilogue_t.
 EPI_NONE, EPI_BIAS, EPI_BIAS_GELU = 0, 1, 2
+EPI_BIAS_GELU_TANH, EPI_BIAS_SILU, EPI_BIAS_RELU = 3, 4, 5
 
 TORCH_DTYPE = {
     F32: torch.float32,
