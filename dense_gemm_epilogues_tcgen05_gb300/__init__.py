@@ -18,7 +18,7 @@ import torch  # noqa: F401  (loads the CUDA runtime the library links against)
 
 __all__ = [
     "F32", "F16", "BF16", "E4M3",
-    "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU",
+    "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_GELU_TANH", "EPI_BIAS_SILU", "EPI_BIAS_RELU",
     "PATH_NOOP", "PATH_EPILOGUE_ONLY", "PATH_TCGEN05", "PATH_SIMT",
     "TILE_AUTO", "TILE_1SM_256", "TILE_1SM_128", "TILE_PAIR",
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
@@ -31,7 +31,7 @@ __all__ = [
 # gemm_dtype_t
 F32, F16, BF16, E4M3 = 0, 1, 2, 3
 # gemm_epilogue_t
-EPI_NONE, EPI_BIAS, EPI_BIAS_GELU = 0, 1, 2
+EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_GELU_TANH, EPI_BIAS_SILU, EPI_BIAS_RELU = 0, 1, 2, 3, 4, 5
 # gemm_path_t
 PATH_NOOP, PATH_EPILOGUE_ONLY, PATH_TCGEN05, PATH_SIMT = 0, 1, 2, 3
 # gemm_tile_policy_t

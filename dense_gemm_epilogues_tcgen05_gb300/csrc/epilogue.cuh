@@ -141,6 +141,54 @@ __device__ __forceinline__ void gelu_erf2(float &z0, float &z1) {
     f2_unpack(y, z0, z1);
 }
 
+// --- the other activations -------------------------------------------------
+// tanh(u) = sign(u) * (1 - 2 / (1 + e^(2|u|))): the hardware 2^x and
+// reciprocal keep the absolute error near 1e-7 (no cancellation for large
+// |u|; for small |u| the absolute error is what matters, since the result is
+// multiplied by z/2).  e^(2|u|) overflows to +inf for large |u|, giving 1.
+__device__ __forceinline__ float tanh_approx_abs(float u) {
+    constexpr float kTwoLog2e = 2.88539008177792681472f;  // 2 / ln 2
+    const float t = fmaf(-2.0f, rcp_approx(ex2_approx(fabsf(u) * kTwoLog2e) + 1.0f), 1.0f);
+    return copysignf(t, u);
+}
+
+// GELU, tanh form: 0.5*z*(1 + tanh(sqrt(2/pi)*(z + 0.044715*z^3))).
+__device__ __forceinline__ float gelu_tanh(float z) {
+    constexpr float kSqrt2OverPi = 0.79788456080286535588f;
+    const float u = kSqrt2OverPi * fmaf(0.044715f * z, z * z, z);
+    return (0.5f * z) * (1.0f + tanh_approx_abs(u));
+}
+
+// SiLU: z * sigmoid(z) = z / (1 + e^-z); e^-z overflows to +inf for very
+// negative z, and z * rcp(inf) = -0.
+__device__ __forceinline__ float silu(float z) {
+    return z * rcp_approx(1.0f + ex2_approx(z * gelu_c::kNegLog2e));
+}
+
+// ReLU: max(z, 0), NaN kept.
+__device__ __forceinline__ float relu(float z) { return z < 0.0f ? 0.0f : z; }
+
+// The epilogue's activation of z (identity for kEpiNone / kEpiBias).
+__device__ __forceinline__ float activate(float z, int epi) {
+    switch (epi) {
+    case kEpiBiasGelu: return gelu_erf(z);
+    case kEpiBiasGeluTanh: return gelu_tanh(z);
+    case kEpiBiasSilu: return silu(z);
+    case kEpiBiasRelu: return relu(z);
+    default: return z;
+    }
+}
+
+// Activation of two values (erf GELU two lanes per instruction).
+__device__ __forceinline__ void activate2(float &z0, float &z1, int epi) {
+    if (epi == kEpiBiasGelu) {
+        gelu_erf2(z0, z1);
+    } else if (epi > kEpiBiasGelu) {
+        z0 = activate(z0, epi);
+        z1 = activate(z1, epi);
+    }
+}
+
 // Scalar epilogue of one element (used by the safe path and the SIMT kernel).
 template <int OUT>
 __device__ __forceinline__ void epilogue_store_one(float acc, typename Elem<OUT>::T *c, float bias_j,
@@ -148,7 +196,7 @@ __device__ __forceinline__ void epilogue_store_one(float acc, typename Elem<OUT>
     float z = e.alpha * acc;
     if (e.beta != 0.0f) z = fmaf(e.beta, Elem<OUT>::load(c), z);
     if (e.epilogue != kEpiNone) z += bias_j;
-    if (e.epilogue == kEpiBiasGelu) z = gelu_erf(z);
+    z = activate(z, e.epilogue);
     *c = Elem<OUT>::cvt(z);
 }
 
@@ -239,9 +287,9 @@ __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename E
             const float4 b = b4[q];
             v[4 * q] += b.x; v[4 * q + 1] += b.y; v[4 * q + 2] += b.z; v[4 * q + 3] += b.w;
         }
-        if (e.epilogue == kEpiBiasGelu) {
+        if (e.epilogue >= kEpiBiasGelu) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) gelu_erf2(v[j], v[j + 1]);
+            for (int j = 0; j < 32; j += 2) activate2(v[j], v[j + 1], e.epilogue);
         }
     }
     uint4 *dst = reinterpret_cast<uint4 *>(crow);
@@ -343,9 +391,9 @@ __device__ __forceinline__ void box_math(float (&v)[32], int h, unsigned char *b
             v[h * PER + 4 * q] += b.x; v[h * PER + 4 * q + 1] += b.y;
             v[h * PER + 4 * q + 2] += b.z; v[h * PER + 4 * q + 3] += b.w;
         }
-        if (e.epilogue == kEpiBiasGelu) {
+        if (e.epilogue >= kEpiBiasGelu) {
 #pragma unroll
-            for (int j = 0; j < PER; j += 2) gelu_erf2(v[h * PER + j], v[h * PER + j + 1]);
+            for (int j = 0; j < PER; j += 2) activate2(v[h * PER + j], v[h * PER + j + 1], e.epilogue);
         }
     }
 #pragma unroll
@@ -421,9 +469,9 @@ __device__ __forceinline__ void box_math_t(float (&v)[32], unsigned char *box, f
     if (e.epilogue != kEpiNone) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] += bias_lane;
-        if (e.epilogue == kEpiBiasGelu) {
+        if (e.epilogue >= kEpiBiasGelu) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) gelu_erf2(v[j], v[j + 1]);
+            for (int j = 0; j < 32; j += 2) activate2(v[j], v[j + 1], e.epilogue);
         }
     }
 #pragma unroll

@@ -141,7 +141,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int ab, const void *A, 
                         const float *bias, int epi, Plan *plan) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (!valid_dtype(ab) || !valid_dtype(cd)) return GEMM_ERR_INVALID_ARG;
-    if (epi < GEMM_EPI_NONE || epi > GEMM_EPI_BIAS_GELU) return GEMM_ERR_INVALID_ARG;
+    if (epi < GEMM_EPI_NONE || epi > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
     if (cd == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
     if (ab == GEMM_F32 && cd != GEMM_F32) return GEMM_ERR_UNSUPPORTED;
     if (ab == GEMM_E4M3 && cd == GEMM_F16) return GEMM_ERR_UNSUPPORTED;

@@ -14,7 +14,8 @@ enum : int { kDtF32 = 0, kDtF16 = 1, kDtBF16 = 2, kDtE4M3 = 3 };
 // Internal operand format of the tensor-core fp32 path: each operand split into
 // a tf32 "hi" and an fp32 "lo" part, stacked in one K-major array (3xTF32).
 enum : int { kDtTF32x3 = 4 };
-enum : int { kEpiNone = 0, kEpiBias = 1, kEpiBiasGelu = 2 };
+enum : int { kEpiNone = 0, kEpiBias = 1, kEpiBiasGelu = 2, kEpiBiasGeluTanh = 3, kEpiBiasSilu = 4,
+             kEpiBiasRelu = 5 };
 
 // Everything the epilogue needs: output geometry and the scalars.
 struct EpiParams {

@@ -50,12 +50,19 @@ typedef enum {
     GEMM_E4M3 = 3
 } gemm_dtype_t;
 
-/* Epilogues, applied to z before the cast.  GELU is the exact erf form
- * 0.5*z*(1 + erf(z/sqrt(2))). */
+/* Epilogues, applied to z before the cast: none, or bias[j] added and then
+ * an activation.  GELU is the exact erf form 0.5*z*(1 + erf(z/sqrt(2))) (the
+ * pages' bias+GELU fusion, Rigel section 1); the others use the same
+ * pluggable place ("Case Study: Steel's BlockMMA", the Epilogue functor):
+ * GELU's tanh form 0.5*z*(1 + tanh(sqrt(2/pi)*(z + 0.044715*z^3))), SiLU
+ * z/(1 + exp(-z)) and ReLU max(z, 0).  Every one needs a bias. */
 typedef enum {
     GEMM_EPI_NONE = 0,
     GEMM_EPI_BIAS = 1,
-    GEMM_EPI_BIAS_GELU = 2
+    GEMM_EPI_BIAS_GELU = 2,
+    GEMM_EPI_BIAS_GELU_TANH = 3,
+    GEMM_EPI_BIAS_SILU = 4,
+    GEMM_EPI_BIAS_RELU = 5
 } gemm_epilogue_t;
 
 typedef enum {

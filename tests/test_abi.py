@@ -120,7 +120,7 @@ def test_degenerate_paths(g):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(M=-1), 1), (dict(K=-5), 1), (dict(ldc=255), 1), (dict(C=None), 1), (dict(A=None), 1),
-    (dict(epi=1), 1), (dict(epi=3, bias=PBIAS), 1), (dict(ab=7), 1), (dict(sam=-256), 1),
+    (dict(epi=1), 1), (dict(epi=6, bias=PBIAS), 1), (dict(epi=-1, bias=PBIAS), 1), (dict(ab=7), 1), (dict(sam=-256), 1),
     (dict(ab=0, cd=2), 2), (dict(ab=3, cd=1), 2), (dict(cd=3), 2), (dict(M=1 << 31), 2),
 ])
 def test_argument_errors(g, kw, status):

@@ -1,0 +1,91 @@
+"""GPU parity of the bias + activation epilogues (tanh-form GELU, SiLU, ReLU).
+
+Every kernel family applies the activation: the pair kernel in both operand
+orders, the one-SM kernel, the CUDA-core kernel (fp32 inputs, or pitches TMA
+cannot take) and the epilogue-only kernel (K = 0).  Random workloads must
+meet the normalised tolerance (error scale times max|act'|); the device
+activations themselves are checked elementwise over a wide range of z.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import run_gemm
+
+pytestmark = pytest.mark.gpu
+
+NEW_ACTS = [wl.EPI_BIAS_GELU_TANH, wl.EPI_BIAS_SILU, wl.EPI_BIAS_RELU]
+ACT_IDS = ["gelu_tanh", "silu", "relu"]
+REF = {wl.EPI_BIAS_GELU_TANH: oracle.gelu_tanh, wl.EPI_BIAS_SILU: oracle.silu, wl.EPI_BIAS_RELU: oracle.relu}
+
+
+@pytest.fixture
+def knobs(cuda_lib, request):
+    policy, order = request.param
+    cuda_lib.gemm_set_tile_policy(policy, 0)
+    cuda_lib.gemm_set_operand_order(order)
+    yield request.param
+    cuda_lib.gemm_set_tile_policy(cuda_lib.TILE_AUTO, 0)
+    cuda_lib.gemm_set_operand_order(cuda_lib.ORDER_AUTO)
+
+
+# (tile policy, operand order): one-SM kernel; pair kernel as given; pair kernel transposed
+KNOBS = [(1, 1), (3, 1), (3, 2)]
+
+
+@pytest.mark.parametrize("knobs", KNOBS, indirect=True, ids=["1sm", "pair", "pair-transposed"])
+@pytest.mark.parametrize("out", [wl.F16, wl.BF16, wl.F32], ids=["f16", "bf16", "f32"])
+@pytest.mark.parametrize("epi", NEW_ACTS, ids=ACT_IDS)
+def test_activation_epilogues_ragged(cuda_lib, epi, out, knobs):
+    for ab, layout in ((wl.F16, "NN"), (wl.BF16, "TT"), (wl.E4M3, "NT")):
+        if ab == wl.E4M3 and out == wl.F16:
+            continue
+        p = wl.random_problem(61 + epi, 336, 528, 272, ab, out, layout=layout, alpha=0.8, beta=0.0, epilogue=epi)
+        r = run_gemm(cuda_lib, p)
+        assert r.status == 0 and r.path == cuda_lib.PATH_TCGEN05
+        res = r.check()
+        assert res["pass"], (ab, layout, res)
+
+
+@pytest.mark.parametrize("epi", NEW_ACTS, ids=ACT_IDS)
+def test_activation_on_other_kernels(cuda_lib, epi):
+    g = cuda_lib
+    # fp32 inputs without a workspace: CUDA-core kernel; with one: 3xTF32 pair kernel
+    p = wl.random_problem(71, 200, 136, 96, wl.F32, wl.F32, alpha=1.0, beta=0.5, epilogue=epi)
+    for use_ws in (False, True):
+        r = run_gemm(g, p, use_workspace=use_ws)
+        assert r.status == 0
+        res = r.check()
+        assert res["pass"], (use_ws, res)
+    # K = 0: epilogue-only kernel on beta*C + bias
+    p0 = wl.random_problem(72, 96, 80, 0, wl.BF16, wl.F32, beta=1.5, epilogue=epi)
+    r0 = run_gemm(g, p0)
+    assert r0.path == g.PATH_EPILOGUE_ONLY
+    assert r0.check()["pass"]
+    # misaligned A base: CUDA-core kernel with 16-bit inputs
+    p1 = wl.random_problem(73, 144, 160, 64, wl.BF16, wl.BF16, epilogue=epi)
+    r1 = run_gemm(g, p1, a_elem_offset=1)
+    assert r1.path == g.PATH_SIMT and r1.check()["pass"]
+
+
+@pytest.mark.parametrize("epi", NEW_ACTS, ids=ACT_IDS)
+@pytest.mark.parametrize("ab", [wl.BF16, wl.F32], ids=["tcgen05", "simt"])
+def test_activation_accuracy_over_range(cuda_lib, epi, ab):
+    """z = bias exactly (the product is zero): fp32 output against the float64 activation."""
+    g = cuda_lib
+    M, N, K = 128, 4096, 64
+    a = torch.zeros(M, K)
+    b = torch.zeros(K, N)
+    bias = torch.linspace(-30.0, 30.0, N, dtype=torch.float32)
+    p = wl.make_problem("act_range", M, N, K, ab, wl.F32, a, b, alpha=1.0, beta=0.0, bias=bias, epilogue=epi)
+    r = run_gemm(g, p, use_workspace=False)
+    assert r.status == 0
+    got = r.values()
+    z = bias.double().numpy()
+    want = REF[epi](z)[None, :]
+    err = np.abs(got - want)
+    # the hardware 2^x / reciprocal approximations: ~1e-7 absolute plus ~3e-7 relative
+    assert np.all(err <= 2e-7 + 6e-7 * np.abs(z)[None, :]), float((err / (2e-7 + 6e-7 * np.abs(z))).max())
+    assert bool(np.all(got[:, z < 0] <= 0.0)) or epi != wl.EPI_BIAS_RELU
