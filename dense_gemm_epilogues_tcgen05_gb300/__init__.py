@@ -23,7 +23,7 @@ __all__ = [
     "TILE_AUTO", "TILE_1SM_256", "TILE_1SM_128", "TILE_PAIR",
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K", "ORDER_AUTO", "ORDER_AS_GIVEN", "ORDER_TRANSPOSED",
-    "gemm_set_operand_order",
+    "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
@@ -40,6 +40,8 @@ TILE_AUTO, TILE_1SM_256, TILE_1SM_128, TILE_PAIR = 0, 1, 2, 3
 SCHED_AUTO, SCHED_TILES, SCHED_STREAM_K = 0, 1, 2
 # gemm_operand_order_t
 ORDER_AUTO, ORDER_AS_GIVEN, ORDER_TRANSPOSED = 0, 1, 2
+# gemm_multicast_t
+MCAST_AUTO, MCAST_OFF, MCAST_ON = 0, 1, 2
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -77,6 +79,8 @@ lib.gemm_set_schedule.restype = _int
 lib.gemm_set_schedule.argtypes = [_int]
 lib.gemm_set_operand_order.restype = _int
 lib.gemm_set_operand_order.argtypes = [_int]
+lib.gemm_set_multicast.restype = _int
+lib.gemm_set_multicast.argtypes = [_int]
 lib.gemm_device_status.restype = _int
 lib.gemm_device_status.argtypes = [_vp]
 lib.gemm_status_string.restype = ctypes.c_char_p
@@ -175,6 +179,11 @@ def gemm_set_schedule(schedule) -> int:
 def gemm_set_operand_order(order) -> int:
     """Process-wide operand order of the pair kernel (ORDER_*): whether it may compute C^T = B^T A^T."""
     return _check(lib.gemm_set_operand_order(order), "gemm_set_operand_order")
+
+
+def gemm_set_multicast(mode) -> int:
+    """Process-wide cluster shape of the pair kernel (MCAST_*): two SM pairs sharing A by TMA multicast, or one."""
+    return _check(lib.gemm_set_multicast(mode), "gemm_set_multicast")
 
 
 def gemm_query_tile(M, N, K, ab_dtype, c_dtype):

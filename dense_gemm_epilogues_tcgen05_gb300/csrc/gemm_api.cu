@@ -10,9 +10,11 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <iterator>
 #include <mutex>
 
 #include "../../include/gemm_gb300.h"
@@ -71,7 +73,9 @@ struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     unsigned int *status = nullptr;
-    int max_clusters[5][4];  // pair kernel, by (ab incl. 3xTF32, out); -1 = not queried yet
+    // Resident clusters of the pair kernel by (cluster of 2 or 4 CTAs, ab incl.
+    // 3xTF32, out); -1 = not queried yet.
+    int max_clusters[2][5][4];
 };
 
 std::mutex g_dev_mu;
@@ -91,8 +95,9 @@ gemm_status_t device_state(DeviceState **out) {
         if (cudaGetSymbolAddress(&p, g_gemm_status_word) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
         d.num_sms = sms;
         d.status = static_cast<unsigned int *>(p);
-        for (auto &row : d.max_clusters)
-            for (int &v : row) v = -1;
+        for (auto &plane : d.max_clusters)
+            for (auto &row : plane)
+                for (int &v : row) v = -1;
         d.ready = true;
     }
     *out = &d;
@@ -289,6 +294,7 @@ std::atomic<int> g_tile_policy{GEMM_TILE_AUTO};
 std::atomic<int> g_tile_policy_bn{0};
 std::atomic<int> g_schedule{GEMM_SCHED_AUTO};
 std::atomic<int> g_operand_order{GEMM_ORDER_AUTO};
+std::atomic<int> g_multicast{GEMM_MCAST_AUTO};
 std::atomic<unsigned int> g_epoch{0};
 
 // Stream-K workspace layout for `clusters` pairs: partial sums, then flags.
@@ -315,12 +321,51 @@ unsigned int next_epoch() {
 // bf16 / fp16 4096^3 +2%; fp8 4096^3 (32 k-blocks) and M=8192 bias+GELU
 // (3.8% idle) would lose 2-4% and keep whole tiles.  Stream-K always needs at
 // least 8 k-blocks per cluster.
-void choose_schedule(int64_t tiles, int num_kb, int max_clusters, bool have_ws, int mode, int *dp_tiles,
-                     long long *sk_units, int *clusters) {
+//
+// Cut points of the stream-K range.  A cluster's piece ends with the first
+// k-blocks of a tile (its OWNER segment) unless it ends on a tile boundary.
+// When that segment is short and something precedes it in the piece, its MMAs
+// finish before the epilogue of the segment before it has freed the other
+// accumulator, and the next segment waits: measured on GB300 (fp16 4096^3) a
+// 7-k-block OWNER after a whole tile cost 4 us, a tenth of the cluster's
+// run.  So each piece is charged max(0, E - b) extra k-blocks for such an
+// ending of b k-blocks (E: an epilogue's length in k-blocks), and the cuts
+// are the greedy ones under the smallest per-cluster charge that covers the
+// range: every piece takes as many units as the charge allows, ending at
+// the tile boundary instead when the short ending would cost more.
+bool stream_k_feasible(long long units, int num_kb, int clusters, int dp_tiles, long long e_kb, long long limit,
+                       unsigned int *cuts) {
+    long long x = 0;
+    cuts[0] = 0;
+    for (int c = 0; c < clusters; ++c) {
+        long long y = x + limit < units ? x + limit : units;
+        const long long b = y % num_kb, ts = y - b;
+        const bool dp_follows = c < dp_tiles;
+        if (b > 0 && b < e_kb && ts > x && dp_follows && (ts - x) + e_kb > limit) y = ts;
+        cuts[c + 1] = static_cast<unsigned int>(y);
+        x = y;
+    }
+    return x == units;
+}
+
+void stream_k_cuts(long long units, int num_kb, int clusters, int dp_tiles, long long e_kb, unsigned int *cuts) {
+    long long lo = (units + clusters - 1) / clusters, hi = lo + e_kb;  // hi always covers the range
+    while (lo < hi) {
+        const long long mid = (lo + hi) / 2;
+        if (stream_k_feasible(units, num_kb, clusters, dp_tiles, e_kb, mid, cuts))
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    stream_k_feasible(units, num_kb, clusters, dp_tiles, e_kb, lo, cuts);
+}
+
+void choose_schedule(int64_t tiles, int num_kb, int max_clusters, bool have_ws, int mode, int bn, int *dp_tiles,
+                     long long *sk_units, unsigned int *cuts, int *clusters) {
     *dp_tiles = static_cast<int>(tiles);
     *sk_units = 0;
     *clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
-    if (!have_ws || mode == GEMM_SCHED_TILES || max_clusters <= 0) return;
+    if (!have_ws || mode == GEMM_SCHED_TILES || max_clusters <= 0 || max_clusters > kMaxSkClusters) return;
     int64_t dp = 0;
     if (mode != GEMM_SCHED_STREAM_K) {
         if (tiles % max_clusters == 0) return;
@@ -330,28 +375,51 @@ void choose_schedule(int64_t tiles, int num_kb, int max_clusters, bool have_ws, 
         dp = (waves - 1) * max_clusters;
     }
     const long long units = static_cast<long long>(tiles - dp) * num_kb;
-    if (units < 8LL * max_clusters) return;
+    if (units < 8LL * max_clusters || units > 0xFFFFFFFFLL) return;
     *dp_tiles = static_cast<int>(dp);
     *sk_units = units;
     *clusters = max_clusters;
+    // An epilogue lasts about as long as 16 k-blocks of a 256-wide tile's MMAs
+    // (fewer columns per k-block make each k-block proportionally shorter).
+    const long long e_kb = 16LL * 256 / (bn > 0 ? bn : 256);
+    stream_k_cuts(units, num_kb, max_clusters, static_cast<int>(dp), e_kb, cuts);
 }
 
-int pair_max_clusters_for(int ab, int cd) {
+int pair_max_clusters_for(int ab, int cd, int cl) {
     switch (ab) {
-    case GEMM_F16: return pair_max_clusters_f16(cd);
-    case GEMM_BF16: return pair_max_clusters_bf16(cd);
-    case GEMM_E4M3: return pair_max_clusters_e4m3(cd);
-    case kDtTF32x3: return pair_max_clusters_tf32x3(cd);
+    case GEMM_F16: return pair_max_clusters_f16(cd, cl);
+    case GEMM_BF16: return pair_max_clusters_bf16(cd, cl);
+    case GEMM_E4M3: return pair_max_clusters_e4m3(cd, cl);
+    case kDtTF32x3: return cl == 2 ? pair_max_clusters_tf32x3(cd) : 0;
     default: return 0;
     }
 }
 
-// Resident two-CTA clusters of the pair kernel on this device (cached).
-int device_max_clusters(DeviceState *d, int ab, int cd) {
+// Resident clusters of `cl` (2 or 4) CTAs of the pair kernel on this device (cached).
+int device_max_clusters(DeviceState *d, int ab, int cd, int cl = 2) {
     std::lock_guard<std::mutex> lock(g_dev_mu);
-    int &v = d->max_clusters[ab][cd];
-    if (v < 0) v = pair_max_clusters_for(ab, cd);
+    int &v = d->max_clusters[cl == 4 ? 1 : 0][ab][cd];
+    if (v < 0) v = pair_max_clusters_for(ab, cd, cl);
     return v;
+}
+
+// Clusters of two pairs (A shared by multicast) or of one pair.  Two pairs
+// need the A tile to split into whole TMA boxes between them (always for a
+// K-contiguous A; for an M-contiguous A only with 16-bit elements, two
+// 128-byte boxes per 128 rows), and AUTO wants the tile columns to pair up
+// evenly, so no pair computes a tile outside the matrix.  Four-CTA clusters
+// may fit on fewer SMs than pairs do (GB300: 36 clusters = 144 SMs against
+// 76 pairs = 152).  Measured there, multicast lowers a launch's fixed cost
+// (about 24 -> 20 us at 4096^3) and raises the per-SM rate by about 3%, so it
+// wins while the fixed cost weighs (fp16 4096^3 +2.7%, bf16 M=2048 N=K=4096
+// +1%: up to about 4 waves of pair tiles) and loses once the lost SMs do
+// (bf16 8192^3 -1.4%, M=8192 N=K=4096 -4%).  AUTO follows that: two-pair
+// clusters when they lose no SM, or when there are at most 4 waves of tiles.
+int choose_cluster(int64_t tiles, int64_t tiles_n, int max_pairs, int max_quads, bool a_splits, int mode) {
+    if (mode == GEMM_MCAST_OFF || !a_splits || max_quads <= 0) return 2;
+    if (mode == GEMM_MCAST_ON) return 4;
+    if (tiles_n % 2 != 0) return 2;
+    return (2 * max_quads >= max_pairs || tiles <= 4LL * max_pairs) ? 4 : 2;
 }
 
 struct TileChoice {
@@ -409,12 +477,12 @@ TileChoice choose_tile(int64_t M, int64_t N, int num_sms, int max_clusters, int 
     return best;
 }
 
-cudaError_t launch_pair(int ab, int cd, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+cudaError_t launch_pair(int ab, int cd, int cl, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                         const TcArgs &args, int clusters, cudaStream_t s) {
     switch (ab) {
-    case GEMM_F16: return launch_pair_f16(cd, ta, tb, tc, args, clusters, s);
-    case GEMM_BF16: return launch_pair_bf16(cd, ta, tb, tc, args, clusters, s);
-    case GEMM_E4M3: return launch_pair_e4m3(cd, ta, tb, tc, args, clusters, s);
+    case GEMM_F16: return launch_pair_f16(cd, cl, ta, tb, tc, args, clusters, s);
+    case GEMM_BF16: return launch_pair_bf16(cd, cl, ta, tb, tc, args, clusters, s);
+    case GEMM_E4M3: return launch_pair_e4m3(cd, cl, ta, tb, tc, args, clusters, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -483,6 +551,7 @@ gemm_status_t gemm_tf32x3(int64_t M, int64_t N, int64_t K, const void *A, int64_
     t.stage_tx = 2u * (128u * 128u + static_cast<uint32_t>(bn / 2) * 128u);
     t.dp_tiles = t.num_tiles;
     t.sk_units = 0;
+    std::fill(std::begin(t.sk_cut), std::end(t.sk_cut), 0u);
     t.partial = nullptr;
     t.flags = nullptr;
     t.epoch = 0;
@@ -600,13 +669,25 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     const int64_t tiles_n = (Nk + tc.bn - 1) / tc.bn;
     // The second operand's box covers this SM's columns: the whole tile (one SM) or half of it (pair).
     const uint32_t b_box = static_cast<uint32_t>(tc.kind == 2 ? tc.bn / 2 : tc.bn);
+    // Pair kernel: clusters of one pair, or of two pairs that each fetch half
+    // of a CTA's A rows (a 64-row box when A is K-contiguous).
+    int cl = 2, max_quads = 0;
+    if (tc.kind == 2) {
+        const int mode = g_multicast.load();
+        const bool a_splits = !op1.mn_major || es == 2;
+        if (mode != GEMM_MCAST_OFF && a_splits) max_quads = device_max_clusters(dev, ab_dtype, c_dtype, 4);
+        cl = choose_cluster(tiles_m * tiles_n, tiles_n, max_clusters, max_quads, a_splits, mode);
+    }
+    const uint32_t a_box = cl == 4 ? 64u : 128u;
     CUtensorMap ta, tb;
     if (swap) {
-        if ((st = encode_operand(&ta, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, 128)) != GEMM_OK) return st;
+        if ((st = encode_operand(&ta, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, a_box)) != GEMM_OK)
+            return st;
         if ((st = encode_operand(&tb, ab_dtype, A, plan.a, M, K, a_stride_m, a_stride_k, b_box)) != GEMM_OK)
             return st;
     } else {
-        if ((st = encode_operand(&ta, ab_dtype, A, plan.a, M, K, a_stride_m, a_stride_k, 128)) != GEMM_OK) return st;
+        if ((st = encode_operand(&ta, ab_dtype, A, plan.a, M, K, a_stride_m, a_stride_k, a_box)) != GEMM_OK)
+            return st;
         if ((st = encode_operand(&tb, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, b_box)) != GEMM_OK)
             return st;
     }
@@ -627,25 +708,36 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     t.stage_tx = 128u * 128u + b_bytes;
     t.dp_tiles = t.num_tiles;
     t.sk_units = 0;
+    std::fill(std::begin(t.sk_cut), std::end(t.sk_cut), 0u);
     t.partial = nullptr;
     t.flags = nullptr;
     t.epoch = 0;
     cudaError_t err;
     if (tc.kind == 2) {
+        // With two pairs per cluster the schedule's unit is a pair of tiles side
+        // by side along N (the second one may lie outside the matrix when
+        // forced with an odd number of tile columns).
+        const int max_units = cl == 4 ? max_quads : max_clusters;
+        const int slot_pairs = cl == 4 ? 2 * max_quads : max_clusters;  // partial-sum slots (per SM pair)
+        if (cl == 4) {
+            t.tiles_n = static_cast<int>((tiles_n + 1) / 2);
+            t.num_tiles = t.tiles_m * t.tiles_n;
+            t.dp_tiles = t.num_tiles;
+        }
         const bool have_ws = workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 &&
-                             workspace_bytes >= workspace_bytes_for(max_clusters);
+                             workspace_bytes >= workspace_bytes_for(slot_pairs);
         int clusters = 0;
-        choose_schedule(t.num_tiles, t.num_kb, max_clusters, have_ws, g_schedule.load(), &t.dp_tiles,
-                        &t.sk_units, &clusters);
+        choose_schedule(t.num_tiles, t.num_kb, max_units, have_ws, g_schedule.load(), t.bn, &t.dp_tiles,
+                        &t.sk_units, t.sk_cut, &clusters);
         if (t.sk_units > 0) {
-            if ((st = check_range(workspace, workspace_bytes_for(max_clusters))) != GEMM_OK) return st;
+            if ((st = check_range(workspace, workspace_bytes_for(slot_pairs))) != GEMM_OK) return st;
             t.partial = static_cast<float *>(workspace);
-            t.flags = reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + partial_bytes(max_clusters));
+            t.flags = reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + partial_bytes(slot_pairs));
             t.epoch = next_epoch();
         }
         t.e.c_tma = c_tma ? 1 : 0;
         t.e.swap = swap ? 1 : 0;
-        err = launch_pair(ab_dtype, c_dtype, ta, tb, tcm, t, clusters, s);
+        err = launch_pair(ab_dtype, c_dtype, cl, ta, tb, tcm, t, clusters, s);
     } else {
         const int grid = static_cast<int>(t.num_tiles < dev->num_sms ? t.num_tiles : dev->num_sms);
         err = launch_tc(ab_dtype, c_dtype, tc.bn, ta, tb, t, grid, s);
@@ -656,6 +748,12 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
 gemm_status_t gemm_set_operand_order(gemm_operand_order_t order) {
     if (order < GEMM_ORDER_AUTO || order > GEMM_ORDER_TRANSPOSED) return GEMM_ERR_INVALID_ARG;
     g_operand_order.store(order);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_set_multicast(gemm_multicast_t mode) {
+    if (mode < GEMM_MCAST_AUTO || mode > GEMM_MCAST_ON) return GEMM_ERR_INVALID_ARG;
+    g_multicast.store(mode);
     return GEMM_OK;
 }
 

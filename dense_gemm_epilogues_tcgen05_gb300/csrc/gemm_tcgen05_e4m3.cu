@@ -1,6 +1,7 @@
 // gemm_tcgen05_e4m3.cu -- tcgen05 GEMM instantiations for e4m3 A/B operands.
 // One-SM kernel: tile widths 256 (4-stage ring) and 128 (6-stage ring).
-// Pair kernel: 256 x BN tiles on two SMs, 6-stage ring of 32 KB per CTA.
+// Pair kernel: 256 x BN tiles on two SMs, 6-stage ring of 32 KB per CTA; clusters
+// of one pair or of two pairs sharing A by multicast (cl = 2 or 4 CTAs).
 #include "gemm_tcgen05.cuh"
 #include "gemm_tcgen05_pair.cuh"
 
@@ -15,14 +16,24 @@ cudaError_t launch_tcgen05_e4m3(int out, int bn, const CUtensorMap &ta, const CU
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_pair_e4m3(int out, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const TcArgs &args,
+cudaError_t launch_pair_e4m3(int out, int cl, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const TcArgs &args,
                               int clusters, cudaStream_t stream) {
+    if (cl == 4) {
+        if (out == kDtBF16) return launch_pair_cfg<kDtE4M3, kDtBF16, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
+        if (out == kDtF32) return launch_pair_cfg<kDtE4M3, kDtF32, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
+        return cudaErrorInvalidValue;
+    }
     if (out == kDtBF16) return launch_pair_cfg<kDtE4M3, kDtBF16, 6>(ta, tb, tc, args, clusters, stream);
     if (out == kDtF32) return launch_pair_cfg<kDtE4M3, kDtF32, 6>(ta, tb, tc, args, clusters, stream);
     return cudaErrorInvalidValue;
 }
 
-int pair_max_clusters_e4m3(int out) {
+int pair_max_clusters_e4m3(int out, int cl) {
+    if (cl == 4) {
+        if (out == kDtBF16) return pair_max_clusters<kDtE4M3, kDtBF16, 6, 128, 4>();
+        if (out == kDtF32) return pair_max_clusters<kDtE4M3, kDtF32, 6, 128, 4>();
+        return 0;
+    }
     if (out == kDtBF16) return pair_max_clusters<kDtE4M3, kDtBF16, 6>();
     if (out == kDtF32) return pair_max_clusters<kDtE4M3, kDtF32, 6>();
     return 0;

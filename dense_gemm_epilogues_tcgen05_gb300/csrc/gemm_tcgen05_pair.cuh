@@ -21,6 +21,14 @@
 // fits the shared-memory bandwidth, where the one-SM 128 x 256 tile needs
 // 192 B/clk.  BN is a runtime multiple of 32 up to 256, chosen by the host to
 // balance waves of tiles over the clusters.
+//
+// With CL = 4 a cluster holds two such pairs that compute two tiles side by
+// side along N (the same 256 rows of A).  Each CTA then fetches only half of
+// its 128 rows of A and TMA multicasts them to the CTA in the same position of
+// the other pair, so the two pairs read each A panel from L2 once: a quarter
+// fewer operand bytes per SM (24 KB instead of 32 KB per stage).  A stage is
+// free again only when both pairs' MMAs have read it, so every CTA's empty[s]
+// takes one commit from each pair's leader and the two pairs run in lockstep.
 #pragma once
 
 #include "epilogue.cuh"
@@ -79,11 +87,21 @@ struct PairConfig {
     static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the pair allocates all 512 TMEM columns");
 };
 
-// A bounded wait that, when it gives up, also raises the peer CTA's abort flag.
+// Raise the abort flag (at shared address `abort_local`) of every other CTA
+// of the cluster.
+template <int CL>
+__device__ __forceinline__ void raise_abort_others(uint32_t abort_local, uint32_t rank) {
+#pragma unroll
+    for (uint32_t r = 0; r < static_cast<uint32_t>(CL); ++r)
+        if (r != rank) st_shared_cluster_u32(mapa_shared(abort_local, r), 1u);
+}
+
+// A bounded wait that, when it gives up, also raises the other CTAs' abort flags.
+template <int CL>
 __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int *status, uint32_t peer_abort_addr) {
+                                          unsigned int *status, uint32_t abort_local, uint32_t rank) {
     if (mbar_wait_bounded(bar, parity, abort_flag, status)) return true;
-    st_shared_cluster_u32(peer_abort_addr, 1u);
+    raise_abort_others<CL>(abort_local, rank);
     return false;
 }
 
@@ -112,7 +130,7 @@ struct SegmentIter {
     long long u, u_end;
     __device__ __forceinline__ SegmentIter(const TcArgs &a, int cluster, int nclusters_)
         : next_dp(cluster), nclusters(nclusters_), dp_tiles(a.dp_tiles), num_kb(a.num_kb),
-          u(a.sk_units * cluster / nclusters_), u_end(a.sk_units * (cluster + 1) / nclusters_) {}
+          u(a.sk_units > 0 ? a.sk_cut[cluster] : 0), u_end(a.sk_units > 0 ? a.sk_cut[cluster + 1] : 0) {}
     __device__ __forceinline__ bool next(Segment &s) {
         if (u >= u_end) {
             if (next_dp >= dp_tiles) return false;
@@ -136,10 +154,13 @@ struct SegmentIter {
     }
 };
 
-// Last cluster whose piece overlaps stream-K tile t: the one holding unit
-// (t + 1) * num_kb - 1, i.e. floor(((t+1)*num_kb*C - 1) / units).
-__device__ __forceinline__ int last_contributor(long long t, int num_kb, int nclusters, long long units) {
-    return static_cast<int>(((t + 1) * num_kb * nclusters - 1) / units);
+// Last cluster whose piece overlaps stream-K tile t, whose first k-block is
+// in `owner`'s piece: the last cluster whose piece starts before the tile's end.
+__device__ __forceinline__ int last_contributor(const TcArgs &a, long long t, int owner, int nclusters) {
+    const long long end = (t + 1) * a.num_kb;
+    int c = owner;
+    while (c + 1 < nclusters && static_cast<long long>(a.sk_cut[c + 1]) < end) ++c;
+    return c;
 }
 
 // Index (in floats) of column group q (4 columns) of chunk ci, row r, inside
@@ -223,12 +244,15 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
     return ok;
 }
 
-template <int AB, int OUT, int STAGES, int BNH>
+// CL: CTAs per cluster, 2 (one pair) or 4 (two pairs sharing A by multicast).
+template <int AB, int OUT, int STAGES, int BNH, int CL>
 __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
+                             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcArgs args) {
     using Cfg = PairConfig<AB, STAGES, BNH>;
     constexpr int BM = Cfg::BM, BK = Cfg::BK, SWZ = Cfg::SWZ;
+    static_assert(CL == 2 || (CL == 4 && !Cfg::X3), "two pairs per cluster only for single-copy operands");
+    constexpr int PAIRS = CL / 2;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
@@ -245,16 +269,19 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();  // 0: leader, 1: peer
-    const int cluster = blockIdx.x >> 1;
-    const int nclusters = gridDim.x >> 1;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t prank = rank & 1u;   // position in the pair: 0 leader, 1 peer
+    const uint32_t pidx = rank >> 1;    // which pair of the cluster
+    const uint32_t lead = rank & ~1u;   // cluster rank of this pair's leader
+    const int cluster = blockIdx.x / CL;
+    const int nclusters = gridDim.x / CL;
     const int bn = args.bn;
     const int bnh = bn >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);   // the leader's expect_tx arrive covers both CTAs' bytes
-            mbar_init(&empty[s], 1);  // one multicast commit
+            mbar_init(&empty[s], PAIRS);  // one multicast commit per pair reading the stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -281,9 +308,9 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
     grid_dep_wait();
     grid_dep_launch();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
-    const uint32_t tempty0_leader = mapa_shared(smem_u32(&tempty[0]), 0);
-    const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u);
+    const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), lead);
+    const uint32_t tempty0_leader = mapa_shared(smem_u32(&tempty[0]), lead);
+    const uint32_t abort_local = smem_u32(const_cast<int *>(abort_flag));
 
     const int M = args.e.M, N = args.e.N;
     const int num_kb = args.num_kb;
@@ -298,10 +325,11 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             while (ok && it.next(seg)) {
                 int tm, tn;
                 tile_coords(seg.tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
-                const int m0 = tm * 2 * BM + static_cast<int>(rank) * BM;
-                const int n0 = tn * bn + static_cast<int>(rank) * bnh;
+                tn = tn * PAIRS + static_cast<int>(pidx);
+                const int m0 = tm * 2 * BM + static_cast<int>(prank) * BM;
+                const int n0 = tn * bn + static_cast<int>(prank) * bnh;
                 for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
-                    if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, args.status, peer_abort)) {
+                    if (!pair_wait<CL>(&empty[stage], phase ^ 1u, abort_flag, args.status, abort_local, rank)) {
                         ok = false;
                         break;
                     }
@@ -311,7 +339,7 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                     // phase cannot end before the leader's arrive).  This keeps
                     // cluster-scope fences off the per-k-block path.
                     const uint32_t fbar = full0_leader + 8u * stage;
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2u * args.stage_tx);
+                    if (prank == 0) mbar_arrive_expect_tx(&full[stage], 2u * args.stage_tx);
                     issued = true;
                     unsigned char *sA = smem + stage * Cfg::STAGE_BYTES;
                     unsigned char *sB = sA + Cfg::B_OFF;
@@ -322,6 +350,17 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                         tma_load_2d_pair(sA + Cfg::A_LO, &tmA, fbar, k0, m0 + args.lo_row_a);
                         tma_load_2d_pair(sB, &tmB, fbar, k0, n0);
                         tma_load_2d_pair(sA + Cfg::B_LO, &tmB, fbar, k0, n0 + args.lo_row_b);
+                    } else if constexpr (CL == 4) {
+                        // This CTA's share of the A rows, delivered to both pairs.
+                        const uint16_t amask = static_cast<uint16_t>((1u << prank) | (4u << prank));
+                        if (!args.a_mn_major) {
+                            tma_load_2d_pair_mc(sA + pidx * (BM / 2) * 128, &tmA, fbar, k0,
+                                                m0 + static_cast<int>(pidx) * (BM / 2), amask);
+                        } else {
+                            // BM / SWZ boxes of SWZ rows; the host runs this only when that is even.
+                            for (int j = static_cast<int>(pidx); j < BM / SWZ; j += PAIRS)
+                                tma_load_2d_pair_mc(sA + j * 128 * BK, &tmA, fbar, m0 + j * SWZ, k0, amask);
+                        }
                     } else if (!args.a_mn_major) {
                         tma_load_2d_pair(sA, &tmA, fbar, k0, m0);
                     } else {
@@ -351,8 +390,12 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
+        if (lane == 0 && prank == 0) {
             // --------------------------------------------- MMA issuer (leader) --
+            // Stages are released in every CTA that multicast into this pair's;
+            // the accumulator is published to this pair only.
+            constexpr uint16_t kEmptyMask = CL == 4 ? 0xF : 0x3;
+            const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
             const uint32_t idesc = mma_idesc(TcTraits<AB>::kFmt, TcTraits<AB>::kFmt, 2 * BM, bn) |
                                    (args.a_mn_major << 15) | (args.b_mn_major << 16);
             const uint32_t a_lbo = args.a_mn_major ? 128u * BK : 16u;
@@ -366,11 +409,11 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             Segment seg;
             for (; ok && it.next(seg); ++local) {
                 const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
-                if (!pair_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, args.status, peer_abort)) break;
+                if (!pair_wait<CL>(&tempty[acc], acc_phase ^ 1u, abort_flag, args.status, abort_local, rank)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * Cfg::ACC_STRIDE;
                 for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
-                    if (!pair_wait(&full[stage], phase, abort_flag, args.status, peer_abort)) {
+                    if (!pair_wait<CL>(&full[stage], phase, abort_flag, args.status, abort_local, rank)) {
                         ok = false;
                         break;
                     }
@@ -394,16 +437,16 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                         }
                     }
                     issued = true;
-                    tc_commit_pair(&empty[stage], 0x3);
+                    tc_commit_pair(&empty[stage], kEmptyMask);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok) tc_commit_pair(&tfull[acc], 0x3);
+                if (ok) tc_commit_pair(&tfull[acc], pair_mask);
             }
             if (*abort_flag && issued) {
-                tc_commit_pair(mma_done, 0x1);
+                tc_commit_pair(mma_done, static_cast<uint16_t>(1u << rank));
                 mbar_drain_wait(mma_done, 0, 100000000ull);
             }
         }
@@ -431,9 +474,10 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             const bool last = !peek.next(after);
             int tm, tn;
             tile_coords(seg.tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
+            tn = tn * PAIRS + static_cast<int>(pidx);
             // Accumulator rows (TMEM lanes) and columns: output rows and columns,
             // or output columns and rows when the kernel computes C^T (e.swap).
-            const int row0 = tm * 2 * BM + static_cast<int>(rank) * BM + quad * 32;  // the warp's first lane row
+            const int row0 = tm * 2 * BM + static_cast<int>(prank) * BM + quad * 32;  // the warp's first lane row
             const int row = row0 + lane;
             const int n_tile = tn * bn;
             float *bias_s = bias_stage + (acc * Cfg::EPI_WARPS + ew) * 128;
@@ -444,7 +488,7 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                 else
                     epilogue_prefetch<OUT>(bias_s, n_tile + c_begin * 32, c_end - c_begin, row, row < M, e);
             }
-            const bool got = pair_wait(&tfull[acc], acc_phase, abort_flag, args.status, peer_abort);
+            const bool got = pair_wait<CL>(&tfull[acc], acc_phase, abort_flag, args.status, abort_local, rank);
             if (__any_sync(0xffffffffu, !got)) break;
             tc_fence_after();
             const int lane_extent = e.swap ? N : M, col_extent = e.swap ? M : N;
@@ -467,36 +511,36 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                     fail = !epilogue_rows_tma<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, bias_lane, e,
                                                    &tmC, cbuf, &cbar[ew], cphase, abort_flag, args.status);
             } else if (seg.kind == kSegPart) {
-                float *slot = args.partial + (static_cast<long long>(cluster) * 2 + rank) * kPartialFloatsPerCta;
+                float *slot = args.partial + (static_cast<long long>(cluster) * CL + rank) * kPartialFloatsPerCta;
                 store_partial_chunks(t_row + c_begin * 32, c_begin, nvalid, r, slot);
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_gpu(&args.flags[(cluster * 2 + rank) * 8 + ew], args.epoch);
+                if (lane == 0) st_release_gpu(&args.flags[(cluster * CL + rank) * 8 + ew], args.epoch);
             } else {
-                const int c_last = last_contributor(seg.sk_tile, num_kb, nclusters, args.sk_units);
+                const int c_last = last_contributor(args, seg.sk_tile, cluster, nclusters);
                 const int ncontrib = c_last - cluster;
                 for (int k = 1; k <= ncontrib && !fail; ++k) {
-                    const unsigned int *f = &args.flags[((cluster + k) * 2 + rank) * 8 + ew];
+                    const unsigned int *f = &args.flags[((cluster + k) * CL + rank) * 8 + ew];
                     fail = !flag_wait_bounded(f, args.epoch, abort_flag, args.status);
                 }
                 if (__any_sync(0xffffffffu, fail)) {
-                    st_shared_cluster_u32(peer_abort, 1u);
+                    raise_abort_others<CL>(abort_local, rank);
                     break;
                 }
                 const float *slot0 =
-                    args.partial + (static_cast<long long>(cluster + 1) * 2 + rank) * kPartialFloatsPerCta;
+                    args.partial + (static_cast<long long>(cluster + 1) * CL + rank) * kPartialFloatsPerCta;
                 fail = !owner_row_chunks<OUT>(t_row + c_begin * 32, col_base, c_begin, nvalid, row, row_ok, r, slot0,
-                                              2 * kPartialFloatsPerCta, ncontrib, bias_s, e, row0, &tmC, cbuf,
+                                              CL * kPartialFloatsPerCta, ncontrib, bias_s, e, row0, &tmC, cbuf,
                                               &cbar[ew], cphase, abort_flag, args.status, bias_lane);
                 __syncwarp();
                 if (lane == 0)
-                    for (int k = 1; k <= ncontrib; ++k) args.flags[((cluster + k) * 2 + rank) * 8 + ew] = 0u;
+                    for (int k = 1; k <= ncontrib; ++k) args.flags[((cluster + k) * CL + rank) * 8 + ew] = 0u;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tempty0_leader + 8u * acc);
             if (__any_sync(0xffffffffu, fail)) {
-                st_shared_cluster_u32(peer_abort, 1u);
+                raise_abort_others<CL>(abort_local, rank);
                 break;
             }
         }
@@ -514,7 +558,11 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
     }
 }
 
-template <int AB, int OUT, int STAGES, int BNH = 128>
+// `clusters` clusters of CL CTAs.  With CL = 4, args.tiles_n / num_tiles /
+// dp_tiles / sk_units count pairs of side-by-side tiles, and the A map's box
+// is half a pair tile's rows (K-major A) or one swizzle row (MN-major A, an
+// even number of them per 128 rows).
+template <int AB, int OUT, int STAGES, int BNH = 128, int CL = 2>
 cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const TcArgs &args,
                             int clusters,
                             cudaStream_t stream) {
@@ -522,17 +570,19 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     // What one CTA's loads of a stage occupy must fit its slots.
     if (args.bn > 2 * BNH) return cudaErrorInvalidValue;
     if (args.stage_tx > static_cast<uint32_t>(Cfg::STAGE_BYTES)) return cudaErrorInvalidValue;
-    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH>;
+    // Two pairs split each CTA's A rows between them: whole boxes only.
+    if (CL == 4 && args.a_mn_major && (Cfg::BM / Cfg::SWZ) % 2 != 0) return cudaErrorInvalidValue;
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.gridDim = dim3(CL * clusters, 1, 1);
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     // The prologue may start while the previous grid drains (the kernel waits
@@ -544,20 +594,20 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, args);
 }
 
-// Largest number of two-CTA clusters of this kernel that can be resident at once.
-template <int AB, int OUT, int STAGES, int BNH = 128>
+// Largest number of CL-CTA clusters of this kernel that can be resident at once.
+template <int AB, int OUT, int STAGES, int BNH = 128, int CL = 2>
 int pair_max_clusters() {
     using Cfg = PairConfig<AB, STAGES, BNH>;
-    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH>;
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(CL, 1, 1);
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

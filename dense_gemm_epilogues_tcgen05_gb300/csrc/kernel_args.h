@@ -30,6 +30,9 @@ struct EpiParams {
     int swap;         // pair kernel: the MMA computes C^T = B^T A^T (TMEM lanes are output columns)
 };
 
+// Most clusters a stream-K schedule spreads over (the cut table's size).
+constexpr int kMaxSkClusters = 128;
+
 // tcgen05 path: operands come through the two tensor maps.
 struct TcArgs {
     EpiParams e;
@@ -42,11 +45,14 @@ struct TcArgs {
     // Pair kernel schedule.  Tiles [0, dp_tiles) are computed whole, cluster c
     // taking c, c + clusters, ...; the k-blocks of tiles [dp_tiles, num_tiles)
     // form one range of sk_units = (num_tiles - dp_tiles) * num_kb units that
-    // is cut into `clusters` contiguous pieces (stream-K).
+    // is cut into `clusters` contiguous pieces (stream-K): cluster c's piece is
+    // units [sk_cut[c], sk_cut[c + 1]).  The cuts start at 0, end at sk_units
+    // and never decrease; only trailing pieces may be empty.
     int dp_tiles;
     long long sk_units;
-    float *partial;                   // stream-K: per cluster, 2 CTAs x 128 x 256 fp32 partial sums
-    unsigned int *flags;              // stream-K: per cluster, 2 CTAs x 8 epilogue warps
+    unsigned int sk_cut[kMaxSkClusters + 1];
+    float *partial;                   // stream-K: per CTA, 128 x 256 fp32 partial sums
+    unsigned int *flags;              // stream-K: per CTA, 8 epilogue warps
     unsigned int epoch;               // stream-K: value a flag takes when its partial is ready (never 0)
     int lo_row_a, lo_row_b;           // 3xTF32: first row of the "lo" half in the stacked A / B arrays
 };
@@ -73,17 +79,18 @@ cudaError_t launch_tcgen05_bf16(int out, int bn, const CUtensorMap &, const CUte
                                 cudaStream_t);
 cudaError_t launch_tcgen05_e4m3(int out, int bn, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int grid,
                                 cudaStream_t);
-//   pair kernel (tile width in args.bn), `clusters` two-CTA clusters; the third map
-//   describes C (read only when args.e.c_tma != 0):
-cudaError_t launch_pair_f16(int out, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
-                            cudaStream_t);
-cudaError_t launch_pair_bf16(int out, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
-                             cudaStream_t);
-cudaError_t launch_pair_e4m3(int out, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
-                             cudaStream_t);
-int pair_max_clusters_f16(int out);
-int pair_max_clusters_bf16(int out);
-int pair_max_clusters_e4m3(int out);
+//   pair kernel (tile width in args.bn), `clusters` clusters of `cl` CTAs (2: one
+//   pair; 4: two pairs sharing A by multicast, the schedule counting pairs of
+//   side-by-side tiles); the third map describes C (read only when args.e.c_tma != 0):
+cudaError_t launch_pair_f16(int out, int cl, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                            const TcArgs &, int clusters, cudaStream_t);
+cudaError_t launch_pair_bf16(int out, int cl, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                             const TcArgs &, int clusters, cudaStream_t);
+cudaError_t launch_pair_e4m3(int out, int cl, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                             const TcArgs &, int clusters, cudaStream_t);
+int pair_max_clusters_f16(int out, int cl);
+int pair_max_clusters_bf16(int out, int cl);
+int pair_max_clusters_e4m3(int out, int cl);
 //   3xTF32 pair kernel (fp32 output) and the hi/lo split pre-pass:
 cudaError_t launch_pair_tf32x3(int out, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int clusters,
                                cudaStream_t);

@@ -319,6 +319,21 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// The same load delivered to every CTA of `cta_mask` (same shared-memory
+// offset in each).  Each destination's bytes are counted on the barrier at
+// `bar_cluster_addr`'s offset in the CTA of the destination's pair that has
+// the same pair position as the CTA holding `bar_cluster_addr` (the pair
+// leader's barrier when that address is a leader's).
+__device__ __forceinline__ void tma_load_2d_pair_mc(void *smem_dst, const CUtensorMap *map,
+                                                    uint32_t bar_cluster_addr, int32_t x, int32_t y,
+                                                    uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
 // Collective over one warp in EACH CTA of the pair.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),

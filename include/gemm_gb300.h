@@ -107,11 +107,11 @@ typedef enum {
  *   alpha, beta    fp32 scalars.  beta == 0: C is not read (NaNs in C do not
  *                  propagate).  For fp8 with per-tensor dequantisation scales
  *                  s_a, s_b, pass alpha * s_a * s_b.
- *   bias           fp32[N] device array, required (non-NULL) when epilogue is
- *                  BIAS or BIAS_GELU, ignored otherwise.
- *   epilogue       GEMM_EPI_NONE, GEMM_EPI_BIAS or GEMM_EPI_BIAS_GELU; the
- *                  order is z = alpha*AB + beta*C + bias, then GELU, then cast
- *                  (round to nearest even).
+ *   bias           fp32[N] device array, required (non-NULL) for every
+ *                  epilogue other than GEMM_EPI_NONE, ignored for NONE.
+ *   epilogue       a gemm_epilogue_t; the order is z = alpha*AB + beta*C +
+ *                  bias, then the activation, then the cast (round to nearest
+ *                  even).
  *   workspace      optional device scratch, 256-byte aligned, owned by the
  *   workspace_bytes  caller: with at least gemm_workspace_size(...) bytes the
  *                  last waves of output tiles are split along K over all SM
@@ -184,6 +184,35 @@ typedef enum {
  * GEMM_ERR_INVALID_ARG for an unknown value; never touches the device.
  */
 gemm_status_t gemm_set_operand_order(gemm_operand_order_t order);
+
+/*
+ * Cluster shape of the pair kernel.  A cluster can hold two SM pairs that
+ * compute two output tiles side by side along N, over the same rows of A:
+ * each CTA then fetches half of its A rows and the TMA multicasts them to the
+ * CTA in the same place of the other pair, so every A panel crosses from L2
+ * to shared memory once per two tiles (a quarter fewer operand bytes per SM).
+ * Tiles, results and the summation order are the same either way.  Four-CTA
+ * clusters may fit on fewer SMs (GB300: 144 of 152), so AUTO uses them where
+ * that costs less than the traffic saves: when the tile columns pair up
+ * evenly and either no SM is lost or the problem has at most four waves of
+ * tiles.  Both shapes need A's tile rows to split into whole TMA boxes (any
+ * K-contiguous A; an M-contiguous A with 16-bit elements).  ON forces
+ * two-pair clusters wherever A splits, even with an odd number of tile
+ * columns (the last pair then computes a tile outside the matrix and stores
+ * nothing).
+ */
+typedef enum {
+    GEMM_MCAST_AUTO = 0,   /* two-pair clusters where they measured faster (above) */
+    GEMM_MCAST_OFF = 1,    /* one pair per cluster */
+    GEMM_MCAST_ON = 2      /* two pairs per cluster wherever A's rows split between them */
+} gemm_multicast_t;
+
+/*
+ * gemm_set_multicast -- cluster shape of later gemm() calls on the pair
+ * kernel, for every thread of the process.  Meant for tuning and tests.
+ * GEMM_ERR_INVALID_ARG for an unknown value; never touches the device.
+ */
+gemm_status_t gemm_set_multicast(gemm_multicast_t mode);
 
 /*
  * gemm_query_path -- validate the same arguments gemm() takes and report, in

@@ -80,6 +80,15 @@ def test_operand_order_validation(g):
     g.gemm_set_operand_order(g.ORDER_AUTO)
 
 
+def test_multicast_validation(g):
+    for v in (g.MCAST_AUTO, g.MCAST_OFF, g.MCAST_ON):
+        assert g.gemm_set_multicast(v) == 0
+    for v in (-1, 3):
+        with pytest.raises(g.GemmError):
+            g.gemm_set_multicast(v)
+    g.gemm_set_multicast(g.MCAST_AUTO)
+
+
 # Fake, aligned device addresses: query_path never dereferences them.
 PA, PB, PC, PBIAS = 0x7F0000000000, 0x7F1000000000, 0x7F2000000000, 0x7F3000000000
 
