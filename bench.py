@@ -245,6 +245,20 @@ def cell(g, p, steps, warmup, stream, n_sets=3):
             "mean_ms": round(total / steps, 5), "reps": steps}
 
 
+def describe_launch(info):
+    """One line for the roofline's kernel field, from gemm_last_launch()."""
+    if info.get("kind") == 2:
+        shape = {4: "two-pair clusters (A shared by TMA multicast)", 2: "one-pair clusters"}.get(
+            info["cluster_ctas"], f"{info['cluster_ctas']}-CTA clusters")
+        order = ", C^T = B^T A^T" if info.get("transposed") else ""
+        sk = f", stream-K over {info['stream_k_tiles']} of {info['tiles']} units" if info.get("stream_k_tiles") else ""
+        return (f"gemm_tcgen05_pair_kernel 256x{info['bn']} tiles, {shape}, {info['grid_ctas']} CTAs"
+                f"{order}{sk}")
+    if info.get("kind") == 1:
+        return f"gemm_tcgen05_kernel 128x{info['bn']} tiles, {info['grid_ctas']} CTAs"
+    return f"path {info.get('path')}"
+
+
 def e2e_measure(g, p, steps, stream):
     """Same metric through the public call with host buffers: H2D of A, B, C
     from pinned memory, the GEMM, and D2H of C inside each timed step."""
@@ -337,9 +351,8 @@ def run_ours(a):
     peaks = measured_peaks()
     avg_ms = sum(per) / len(per)
     achieved = p.flops / (avg_ms * 1e-3) / 1e12
-    kind, bn, units = g.gemm_query_tile(p.M, p.N, p.K, p.ab_dtype, p.c_dtype)
-    kernel = (f"gemm_tcgen05_pair_kernel<f16,f16> 256x{bn} tiles on {units} SM pairs" if kind == 2 else
-              f"gemm_tcgen05_kernel<f16,f16,{bn}> 128x{bn} tiles on {units} SMs")
+    launch = g.gemm_last_launch()  # what the timed calls enqueued (the same call every step)
+    kernel = describe_launch(launch)
     traffic = recorded_traffic("tcgen05_f16_4096")
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
@@ -356,6 +369,7 @@ def run_ours(a):
                      "kernel": kernel},
         "clocks": sampler.summary(),
         "gpu_launches": a.steps,
+        "launch": launch,
     }
     if rank == 0:
         out["e2e"] = e2e_measure(g, p, 10, stream)

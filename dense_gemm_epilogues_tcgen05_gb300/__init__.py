@@ -23,7 +23,7 @@ __all__ = [
     "TILE_AUTO", "TILE_1SM_256", "TILE_1SM_128", "TILE_PAIR",
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K", "ORDER_AUTO", "ORDER_AS_GIVEN", "ORDER_TRANSPOSED",
-    "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast",
+    "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast", "gemm_last_launch",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
@@ -81,6 +81,16 @@ lib.gemm_set_operand_order.restype = _int
 lib.gemm_set_operand_order.argtypes = [_int]
 lib.gemm_set_multicast.restype = _int
 lib.gemm_set_multicast.argtypes = [_int]
+
+
+class _LaunchInfo(ctypes.Structure):
+    """gemm_launch_info_t"""
+    _fields_ = [(n, _int) for n in ("path", "kind", "bn", "transposed", "cluster_ctas", "grid_ctas", "tiles",
+                                    "stream_k_tiles", "tf32x3")]
+
+
+lib.gemm_last_launch.restype = _int
+lib.gemm_last_launch.argtypes = [ctypes.POINTER(_LaunchInfo)]
 lib.gemm_device_status.restype = _int
 lib.gemm_device_status.argtypes = [_vp]
 lib.gemm_status_string.restype = ctypes.c_char_p
@@ -184,6 +194,13 @@ def gemm_set_operand_order(order) -> int:
 def gemm_set_multicast(mode) -> int:
     """Process-wide cluster shape of the pair kernel (MCAST_*): two SM pairs sharing A by TMA multicast, or one."""
     return _check(lib.gemm_set_multicast(mode), "gemm_set_multicast")
+
+
+def gemm_last_launch() -> dict:
+    """What this thread's last successful gemm() enqueued (gemm_launch_info_t as a dict)."""
+    info = _LaunchInfo()
+    _check(lib.gemm_last_launch(ctypes.byref(info)), "gemm_last_launch")
+    return {n: getattr(info, n) for n, _ in _LaunchInfo._fields_}
 
 
 def gemm_query_tile(M, N, K, ab_dtype, c_dtype):

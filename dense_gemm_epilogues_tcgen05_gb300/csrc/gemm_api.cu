@@ -297,6 +297,14 @@ std::atomic<int> g_operand_order{GEMM_ORDER_AUTO};
 std::atomic<int> g_multicast{GEMM_MCAST_AUTO};
 std::atomic<unsigned int> g_epoch{0};
 
+// The calling thread's last successful gemm() launch (gemm_last_launch).
+thread_local gemm_launch_info_t t_last_launch = {};
+
+gemm_status_t record(gemm_status_t st, const gemm_launch_info_t &info) {
+    if (st == GEMM_OK) t_last_launch = info;
+    return st;
+}
+
 // Stream-K workspace layout for `clusters` pairs: partial sums, then flags.
 size_t partial_bytes(int clusters) { return static_cast<size_t>(clusters) * 2 * kPartialFloatsPerCta * 4; }
 size_t workspace_bytes_for(int clusters) {
@@ -520,7 +528,7 @@ EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alp
 // on the stacked hi/lo arrays (whole tiles, 256 x 256).
 gemm_status_t gemm_tf32x3(int64_t M, int64_t N, int64_t K, const void *A, int64_t sam, int64_t sak, const void *B,
                           int64_t sbk, int64_t sbn, const EpiParams &e, void *workspace, int max_clusters,
-                          DeviceState *dev, cudaStream_t s) {
+                          DeviceState *dev, cudaStream_t s, gemm_launch_info_t *info) {
     const int64_t pitch = tf32x3_pitch(K);
     float *a2 = static_cast<float *>(workspace);
     float *b2 = reinterpret_cast<float *>(static_cast<char *>(workspace) +
@@ -561,6 +569,13 @@ gemm_status_t gemm_tf32x3(int64_t M, int64_t N, int64_t K, const void *A, int64_
     std::memset(&tc, 0, sizeof(tc));
     t.e.c_tma = encode_c(&tc, GEMM_F32, e.C, M, N, e.ldc) ? 1 : 0;
     const int clusters = t.num_tiles < max_clusters ? t.num_tiles : max_clusters;
+    info->path = GEMM_PATH_TCGEN05;
+    info->kind = 2;
+    info->bn = bn;
+    info->cluster_ctas = 2;
+    info->grid_ctas = 2 * clusters;
+    info->tiles = t.num_tiles;
+    info->tf32x3 = 1;
     return launch_pair_tf32x3(GEMM_F32, ta, tb, tc, t, clusters, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -605,7 +620,9 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     Plan plan;
     gemm_status_t st = make_plan(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc,
                                  c_dtype, alpha, bias, epilogue, &plan);
-    if (st != GEMM_OK || plan.path == GEMM_PATH_NOOP) return st;
+    gemm_launch_info_t info = {};
+    info.path = plan.path;
+    if (st != GEMM_OK || plan.path == GEMM_PATH_NOOP) return record(st, info);
     if (!driver_fns().ok) return GEMM_ERR_CUDA;
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != GEMM_OK) return st;
@@ -617,7 +634,7 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     EpiParams e = make_epi(M, N, C, ldc, c_dtype, alpha, beta, bias, epilogue);
 
     if (plan.path == GEMM_PATH_EPILOGUE_ONLY)
-        return launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+        return record(launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA, info);
 
     if ((st = check_range(A, span_bytes(M, K, a_stride_m, a_stride_k, es))) != GEMM_OK) return st;
     if ((st = check_range(B, span_bytes(K, N, b_stride_k, b_stride_n, es))) != GEMM_OK) return st;
@@ -630,8 +647,9 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
         if (need > 0 && workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 &&
             workspace_bytes >= need && max_clusters > 0) {
             if ((st = check_range(workspace, need)) != GEMM_OK) return st;
-            return gemm_tf32x3(M, N, K, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, e, workspace,
-                               max_clusters, dev, s);
+            return record(gemm_tf32x3(M, N, K, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, e, workspace,
+                                      max_clusters, dev, s, &info),
+                          info);
         }
     }
     if (plan.path == GEMM_PATH_SIMT) {
@@ -640,7 +658,7 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
         a.K = static_cast<int>(K);
         a.A = A; a.sam = a_stride_m; a.sak = a_stride_k;
         a.B = B; a.sbk = b_stride_k; a.sbn = b_stride_n;
-        return launch_simt(ab_dtype, c_dtype, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+        return record(launch_simt(ab_dtype, c_dtype, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA, info);
     }
 
     // tcgen05 path: one SM or a pair of SMs per tile, by the cost model.  The
@@ -737,12 +755,28 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
         }
         t.e.c_tma = c_tma ? 1 : 0;
         t.e.swap = swap ? 1 : 0;
+        info.kind = 2;
+        info.transposed = swap ? 1 : 0;
+        info.cluster_ctas = cl;
+        info.grid_ctas = cl * clusters;
+        info.stream_k_tiles = t.num_tiles - t.dp_tiles;
         err = launch_pair(ab_dtype, c_dtype, cl, ta, tb, tcm, t, clusters, s);
     } else {
         const int grid = static_cast<int>(t.num_tiles < dev->num_sms ? t.num_tiles : dev->num_sms);
+        info.kind = 1;
+        info.cluster_ctas = 1;
+        info.grid_ctas = grid;
         err = launch_tc(ab_dtype, c_dtype, tc.bn, ta, tb, t, grid, s);
     }
-    return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    info.bn = tc.bn;
+    info.tiles = t.num_tiles;
+    return record(err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA, info);
+}
+
+gemm_status_t gemm_last_launch(gemm_launch_info_t *info) {
+    if (info == nullptr) return GEMM_ERR_INVALID_ARG;
+    *info = t_last_launch;
+    return GEMM_OK;
 }
 
 gemm_status_t gemm_set_operand_order(gemm_operand_order_t order) {

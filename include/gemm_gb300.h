@@ -258,6 +258,31 @@ gemm_status_t gemm_query_tile(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_d
                               int *kind, int *bn, int *units);
 
 /*
+ * What the calling thread's last gemm() (or gemm_builtin_scratch()) call
+ * enqueued, for tuning, tests and reports.  No counterpart on the pages.
+ */
+typedef struct {
+    int path;          /* gemm_path_t of the kernel family launched (NOOP when nothing was) */
+    int kind;          /* tcgen05 path: 1 one SM per tile, 2 a pair of SMs per tile; else 0 */
+    int bn;            /* tcgen05 path: tile width in columns of the MMA's output */
+    int transposed;    /* 1 when the pair kernel ran C^T = B^T A^T */
+    int cluster_ctas;  /* CTAs per cluster: 1 (one-SM kernel), 2 (one pair) or 4 (two pairs sharing A) */
+    int grid_ctas;     /* CTAs of the tcgen05 GEMM kernel (0 on the other paths) */
+    int tiles;         /* its scheduling units: output tiles, or pairs of tiles side by side for
+                          4-CTA clusters (0 on the other paths) */
+    int stream_k_tiles;/* of those, units whose k-blocks are split over all clusters */
+    int tf32x3;        /* 1 when fp32 inputs ran as 3xTF32 (split pre-pass + tensor cores) */
+} gemm_launch_info_t;
+
+/*
+ * gemm_last_launch -- copy the calling thread's record of its last gemm()
+ * call that returned GEMM_OK into *info (host pointer).  A call that failed
+ * leaves the record as it was.  GEMM_ERR_INVALID_ARG for info == NULL.
+ * Touches no device.
+ */
+gemm_status_t gemm_last_launch(gemm_launch_info_t *info);
+
+/*
  * gemm_builtin_scratch -- gemm() for callers that cannot allocate device
  * memory.  (The pages have no counterpart: this is a deployment convenience
  * of this library, not part of the method.)

@@ -38,7 +38,8 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     assert {"gemm", "gemm_workspace_size", "gemm_query_path", "gemm_bias_gelu", "gemm_device_status",
             "gemm_status_string", "gemm_version", "gemm_set_tile_policy", "gemm_query_tile",
-            "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest"} <= names
+            "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest", "gemm_set_multicast",
+            "gemm_last_launch"} <= names
 
 
 def test_library_exports_every_declared_symbol(g):
@@ -78,6 +79,18 @@ def test_operand_order_validation(g):
         with pytest.raises(g.GemmError):
             g.gemm_set_operand_order(v)
     g.gemm_set_operand_order(g.ORDER_AUTO)
+
+
+def test_last_launch_records_only_successful_calls(g):
+    """A no-op call (M = 0) is recorded without touching a device; a rejected call is not."""
+    assert g.gemm(0, 16, 16, g.F16, 0, 16, 1, 0, 16, 1, 0, 16, g.F16, 1.0, 0.0, None, g.EPI_NONE, stream=0) == 0
+    info = g.gemm_last_launch()
+    assert info["path"] == g.PATH_NOOP and info["grid_ctas"] == 0 and info["kind"] == 0
+    with pytest.raises(g.GemmError):
+        g.gemm(-1, 16, 16, g.F16, 0, 16, 1, 0, 16, 1, 0, 16, g.F16, 1.0, 0.0, None, g.EPI_NONE, stream=0)
+    assert g.gemm_last_launch() == info
+    assert set(info) == {"path", "kind", "bn", "transposed", "cluster_ctas", "grid_ctas", "tiles",
+                         "stream_k_tiles", "tf32x3"}
 
 
 def test_multicast_validation(g):

@@ -106,3 +106,14 @@ def test_reference_arm_json_line():
         assert key in line, key
     assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_describe_launch():
+    import bench
+    pair = {"path": 2, "kind": 2, "bn": 256, "transposed": 1, "cluster_ctas": 4, "grid_ctas": 144, "tiles": 128,
+            "stream_k_tiles": 56, "tf32x3": 0}
+    d = bench.describe_launch(pair)
+    assert "256x256" in d and "two-pair clusters" in d and "144 CTAs" in d and "C^T" in d and "56 of 128" in d
+    one = dict(pair, kind=1, bn=128, cluster_ctas=1, grid_ctas=152, transposed=0, stream_k_tiles=0)
+    assert bench.describe_launch(one) == "gemm_tcgen05_kernel 128x128 tiles, 152 CTAs"
+    assert bench.describe_launch({"path": 3, "kind": 0}) == "path 3"

@@ -126,3 +126,43 @@ def test_fp16_headline_shape_stream_k_tolerance(cuda_lib, mcast_on):
     assert r.status == 0
     res = r.check(rows=sample_rows(4096))
     assert res["pass"], res
+
+
+def test_launch_record_matches_the_chosen_shape(cuda_lib):
+    """gemm_last_launch reports what ran: the transposed pair kernel at fp16 4096^3, with two-pair
+    clusters under AUTO (4 waves of tiles or fewer, even tile columns), and the shape the knob forces."""
+    g = cuda_lib
+    p = wl.fp16_alpha_beta(4096)
+    r = run_gemm(g, p)
+    assert r.status == 0
+    info = g.gemm_last_launch()
+    assert info["path"] == g.PATH_TCGEN05 and info["kind"] == 2 and info["bn"] == 256
+    # A row-major, B row-major fp16 with 16-bit output: the pair kernel runs C^T = B^T A^T
+    assert info["transposed"] == 1
+    assert info["cluster_ctas"] in (2, 4) and info["grid_ctas"] % info["cluster_ctas"] == 0
+    assert info["tiles"] == (256 if info["cluster_ctas"] == 2 else 128)
+    try:
+        g.gemm_set_multicast(g.MCAST_OFF)
+        run_gemm(g, p)
+        off = g.gemm_last_launch()
+        assert off["cluster_ctas"] == 2 and off["tiles"] == 256
+        g.gemm_set_multicast(g.MCAST_ON)
+        run_gemm(g, p)
+        on = g.gemm_last_launch()
+        assert on["cluster_ctas"] == 4 and on["tiles"] == 128
+        # AUTO: two-pair clusters if they lose no SM pair or the problem has at most 4 waves of tiles
+        if 2 * (on["grid_ctas"] // 4) >= off["grid_ctas"] // 2 or 256 <= 4 * (off["grid_ctas"] // 2):
+            assert info["cluster_ctas"] == 4
+    finally:
+        g.gemm_set_multicast(g.MCAST_AUTO)
+
+
+def test_launch_record_fp32_paths(cuda_lib):
+    g = cuda_lib
+    p = wl.fp32_square(256)
+    run_gemm(g, p)
+    info = g.gemm_last_launch()
+    assert info["path"] == g.PATH_TCGEN05 and info["tf32x3"] == 1 and info["cluster_ctas"] == 2
+    run_gemm(g, p, use_workspace=False)
+    info = g.gemm_last_launch()
+    assert info["path"] == g.PATH_SIMT and info["tf32x3"] == 0 and info["grid_ctas"] == 0
