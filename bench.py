@@ -70,10 +70,11 @@ def measured_peaks():
         with open(path) as f:
             d = json.load(f)
         return {"bf16_tflops": float(d["bf16_tflops"]), "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]),
-                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+                "hbm_gbs": float(d["hbm_gbs"]), "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)),
+                "source": "measured"}
     except Exception:
         return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
-                "source": "fallback"}
+                "sm_max_mhz": 2070.0, "source": "fallback"}
 
 
 def recorded_traffic(kernel_tag):
@@ -195,18 +196,22 @@ def _make_sets(problem, n_sets, device):
     return sets
 
 
-def _call(g, p, s, stream):
+def _call(g, p, s, stream, baseline=None):
     A, B, C, bias = s
+    if baseline is not None:
+        g.gemm_baseline(baseline, p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k,
+                        p.b_stride_n, C, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue, stream=stream)
+        return
     ws = _workspace(g, C.device, g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype))
     g.gemm(p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k, p.b_stride_n, C, p.ldc,
            p.c_dtype, p.alpha, p.beta, bias, p.epilogue, workspace=ws, workspace_bytes=ws.numel(), stream=stream)
 
 
-def time_steps(g, p, sets, steps, warmup, stream, sampler=None, dist=None):
+def time_steps(g, p, sets, steps, warmup, stream, sampler=None, dist=None, baseline=None):
     """Warm up, then time `steps` calls; returns (per-step ms list, total ms)."""
     import torch
     for i in range(warmup):
-        _call(g, p, sets[i % len(sets)], stream)
+        _call(g, p, sets[i % len(sets)], stream, baseline)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -216,7 +221,7 @@ def time_steps(g, p, sets, steps, warmup, stream, sampler=None, dist=None):
         torch.cuda.synchronize()
         ev[0].record(stream)
         for i in range(steps):
-            _call(g, p, sets[i % len(sets)], stream)
+            _call(g, p, sets[i % len(sets)], stream, baseline)
             ev[i + 1].record(stream)
         torch.cuda.synchronize()
     if dist is not None:
@@ -233,10 +238,10 @@ class _Null:
         return False
 
 
-def cell(g, p, steps, warmup, stream, n_sets=3):
+def cell(g, p, steps, warmup, stream, n_sets=3, baseline=None):
     import torch
     sets = _make_sets(p, n_sets, torch.device("cuda", torch.cuda.current_device()))
-    per, total = time_steps(g, p, sets, steps, warmup, stream)
+    per, total = time_steps(g, p, sets, steps, warmup, stream, baseline=baseline)
     tf = [p.flops / (t * 1e-3) / 1e12 for t in per]
     med, ci = bootstrap_ci(tf)
     del sets
@@ -403,7 +408,42 @@ def extra_cells(g, stream):
         cells[f"gelu_M{M}"] = {"fused": fused, "none": plain,
                                "fused_cost_pct": round(100 * (plain["median_tflops"] / fused["median_tflops"] - 1),
                                                        2)}
+    cells["baseline_gate_fp16_4096"] = baseline_gate(g, stream)
     return cells
+
+
+def alu_fp16_roofline_tflops(num_sms, sm_mhz):
+    """Baseline (A) of the cheap-baseline gate: fp16 FMA on the CUDA cores, taken as
+    2 x the FP32 FMA rate (128 lanes x 2 halves x 2 flops per SM per clock, HFMA2)."""
+    return num_sms * 128 * 2 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def gate_verdict(tcgen05, alu, simt, mma_sync, win=1.10):
+    """Rigel section 3: a kernel wins only if it beats the strongest trivial explanation by >= 1.10x."""
+    strongest = max(alu, simt, mma_sync)
+    ratio = tcgen05 / strongest
+    return {"over_strongest": round(ratio, 3), "over_simt": round(tcgen05 / simt, 2),
+            "over_mma_sync": round(tcgen05 / mma_sync, 3), "over_alu_roofline": round(tcgen05 / alu, 2),
+            "threshold": win, "win": bool(ratio >= win)}
+
+
+def baseline_gate(g, stream):
+    """The cheap-baseline gate (Rigel section 3; section 4, signal 2) on the headline
+    workload: the tcgen05 kernel against (A) the CUDA-core fp16 roofline, (B) the
+    SIMT kernel and (C) the warp-level mma.sync kernel, all through the C ABI."""
+    import torch
+    import workloads as wl
+    p = wl.fp16_alpha_beta(4096)
+    tc = cell(g, p, 30, 5, stream)
+    simt = cell(g, p, 5, 1, stream, n_sets=2, baseline=g.BASELINE_SIMT)
+    ms = cell(g, p, 30, 5, stream, baseline=g.BASELINE_MMA_SYNC)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = measured_peaks()["sm_max_mhz"]
+    alu = alu_fp16_roofline_tflops(sms, mhz)
+    out = {"workload": "fp16 4096^3, C = 1.5*A*B + 0.5*C", "tcgen05": tc, "simt": simt, "mma_sync": ms,
+           "alu_fp16_roofline_tflops": round(alu, 1)}
+    out.update(gate_verdict(tc["median_tflops"], alu, simt["median_tflops"], ms["median_tflops"]))
+    return out
 
 
 # ------------------------------------------------------------ reference arm --

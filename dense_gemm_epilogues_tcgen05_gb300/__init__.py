@@ -24,6 +24,7 @@ __all__ = [
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K", "ORDER_AUTO", "ORDER_AS_GIVEN", "ORDER_TRANSPOSED",
     "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast", "gemm_last_launch",
+    "BASELINE_SIMT", "BASELINE_MMA_SYNC", "gemm_baseline",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
@@ -42,6 +43,8 @@ SCHED_AUTO, SCHED_TILES, SCHED_STREAM_K = 0, 1, 2
 ORDER_AUTO, ORDER_AS_GIVEN, ORDER_TRANSPOSED = 0, 1, 2
 # gemm_multicast_t
 MCAST_AUTO, MCAST_OFF, MCAST_ON = 0, 1, 2
+# gemm_baseline_t
+BASELINE_SIMT, BASELINE_MMA_SYNC = 0, 1
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -91,6 +94,10 @@ class _LaunchInfo(ctypes.Structure):
 
 lib.gemm_last_launch.restype = _int
 lib.gemm_last_launch.argtypes = [ctypes.POINTER(_LaunchInfo)]
+lib.gemm_baseline.restype = _int
+lib.gemm_baseline.argtypes = [_int, _i64, _i64, _i64, _int, ctypes.c_void_p, _i64, _i64, ctypes.c_void_p, _i64, _i64,
+                              ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
+                              ctypes.c_void_p]
 lib.gemm_device_status.restype = _int
 lib.gemm_device_status.argtypes = [_vp]
 lib.gemm_status_string.restype = ctypes.c_char_p
@@ -194,6 +201,14 @@ def gemm_set_operand_order(order) -> int:
 def gemm_set_multicast(mode) -> int:
     """Process-wide cluster shape of the pair kernel (MCAST_*): two SM pairs sharing A by TMA multicast, or one."""
     return _check(lib.gemm_set_multicast(mode), "gemm_set_multicast")
+
+
+def gemm_baseline(kind, M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc, c_dtype,
+                  alpha, beta, bias, epilogue, stream=None) -> int:
+    """The same operation as gemm() on a baseline kernel of the cheap-baseline gate (BASELINE_*)."""
+    st = lib.gemm_baseline(kind, M, N, K, ab_dtype, _ptr(A), a_stride_m, a_stride_k, _ptr(B), b_stride_k, b_stride_n,
+                           _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue, _stream(stream))
+    return _check(st, "gemm_baseline")
 
 
 def gemm_last_launch() -> dict:

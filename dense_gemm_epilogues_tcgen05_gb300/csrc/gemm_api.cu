@@ -832,6 +832,44 @@ gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dt
                                                                                                 : GEMM_ERR_CUDA;
 }
 
+gemm_status_t gemm_baseline(gemm_baseline_t kind, int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype,
+                            const void *A, int64_t a_stride_m, int64_t a_stride_k, const void *B, int64_t b_stride_k,
+                            int64_t b_stride_n, void *C, int64_t ldc, gemm_dtype_t c_dtype, float alpha, float beta,
+                            const float *bias, gemm_epilogue_t epilogue, gemm_stream_t stream) {
+    if (kind != GEMM_BASELINE_SIMT && kind != GEMM_BASELINE_MMA_SYNC) return GEMM_ERR_INVALID_ARG;
+    Plan plan;
+    gemm_status_t st = make_plan(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc,
+                                 c_dtype, alpha, bias, epilogue, &plan);
+    if (st != GEMM_OK || plan.path == GEMM_PATH_NOOP) return st;
+    const bool mma = kind == GEMM_BASELINE_MMA_SYNC;
+    if (mma && plan.path != GEMM_PATH_EPILOGUE_ONLY) {
+        if (ab_dtype != GEMM_F16 && ab_dtype != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
+        if (!plan.a.tma || !plan.b.tma) return GEMM_ERR_UNSUPPORTED;
+        const int64_t a_extent = plan.a.mn_major ? M : K, b_extent = plan.b.mn_major ? N : K;
+        if (a_extent % 8 != 0 || b_extent % 8 != 0) return GEMM_ERR_UNSUPPORTED;
+    }
+    if (!driver_fns().ok) return GEMM_ERR_CUDA;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != GEMM_OK) return st;
+    const int es = elem_bytes(ab_dtype), ces = elem_bytes(c_dtype);
+    if ((st = check_range(C, span_bytes(M, N, ldc, 1, ces))) != GEMM_OK) return st;
+    if (epilogue != GEMM_EPI_NONE && (st = check_range(bias, static_cast<size_t>(N) * 4)) != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const EpiParams e = make_epi(M, N, C, ldc, c_dtype, alpha, beta, bias, epilogue);
+    if (plan.path == GEMM_PATH_EPILOGUE_ONLY)
+        return launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    if ((st = check_range(A, span_bytes(M, K, a_stride_m, a_stride_k, es))) != GEMM_OK) return st;
+    if ((st = check_range(B, span_bytes(K, N, b_stride_k, b_stride_n, es))) != GEMM_OK) return st;
+    SimtArgs a;
+    a.e = e;
+    a.K = static_cast<int>(K);
+    a.A = A; a.sam = a_stride_m; a.sak = a_stride_k;
+    a.B = B; a.sbk = b_stride_k; a.sbn = b_stride_n;
+    const cudaError_t err = mma ? launch_mma_sync(ab_dtype, c_dtype, a, !plan.a.mn_major, !plan.b.mn_major, s)
+                                : launch_simt(ab_dtype, c_dtype, a, s);
+    return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 gemm_status_t gemm_wait_selftest(const unsigned int *never_set, uint64_t limit_ns, gemm_stream_t stream) {
     if (never_set == nullptr || limit_ns == 0 || limit_ns > 1000000000ull) return GEMM_ERR_INVALID_ARG;
     if (!driver_fns().ok) return GEMM_ERR_CUDA;

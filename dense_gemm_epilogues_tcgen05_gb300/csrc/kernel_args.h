@@ -99,6 +99,9 @@ cudaError_t launch_tf32_split(const float *src, long long rows, long long cols, 
                               float *dst, long long pitch, cudaStream_t stream);
 //   CUDA-core kernels:
 cudaError_t launch_simt(int ab, int out, const SimtArgs &args, cudaStream_t stream);
+//   warp-level mma.sync baseline (fp16 / bf16; operand layouts by contiguity):
+cudaError_t launch_mma_sync(int ab, int out, const SimtArgs &args, bool a_k_contig, bool b_k_contig,
+                            cudaStream_t stream);
 cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t stream);
 cudaError_t launch_bias_gelu(int out, const EpiParams &e, cudaStream_t stream);
 cudaError_t launch_wait_selftest(const unsigned int *never_set, unsigned long long limit_ns, unsigned int *status,

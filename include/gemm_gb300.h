@@ -329,6 +329,37 @@ gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dt
                              const float *bias, gemm_stream_t stream);
 
 /*
+ * Baselines of the cheap-baseline gate (Rigel section 3; section 4, signal
+ * 2): a claim that the tensor path is fast stands only once the trivial
+ * explanations have run and lost -- a GEMM on the ordinary ALUs, and the
+ * legacy warp-matrix instruction (simdgroup_matrix on the pages).  For
+ * measurement and tests only; gemm() never runs them.
+ */
+typedef enum {
+    GEMM_BASELINE_SIMT = 0,     /* threadgroup-tiled CUDA-core FFMA kernel (no matrix instructions) */
+    GEMM_BASELINE_MMA_SYNC = 1  /* warp-level mma.sync.m16n8k16 kernel, fp16 / bf16 inputs */
+} gemm_baseline_t;
+
+/*
+ * gemm_baseline -- the same operation and arguments as gemm() (no workspace),
+ * computed by the baseline kernel `kind`.  GEMM_BASELINE_SIMT takes every
+ * combination gemm() takes.  GEMM_BASELINE_MMA_SYNC takes F16 or BF16 inputs
+ * whose operands are TMA-streamable in gemm()'s sense (one unit stride,
+ * 16-byte aligned base and other stride) and whose contiguous extents (K for
+ * a K-contiguous operand, M or N otherwise) are multiples of 8; anything else
+ * returns GEMM_ERR_UNSUPPORTED.  K == 0, alpha == 0, M == 0 and N == 0
+ * behave as in gemm().  Asynchronous on `stream`; errors as gemm().
+ */
+gemm_status_t gemm_baseline(gemm_baseline_t kind, int64_t M, int64_t N, int64_t K,
+                            gemm_dtype_t ab_dtype,
+                            const void *A, int64_t a_stride_m, int64_t a_stride_k,
+                            const void *B, int64_t b_stride_k, int64_t b_stride_n,
+                            void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                            float alpha, float beta,
+                            const float *bias, gemm_epilogue_t epilogue,
+                            gemm_stream_t stream);
+
+/*
  * gemm_device_status -- synchronise `stream`, then return and clear the
  * device-side status word of the current device: GEMM_ERR_TIMEOUT if any
  * kernel gave up on a bounded wait since the last call, GEMM_ERR_CUDA if the

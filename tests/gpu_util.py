@@ -44,8 +44,9 @@ def workspace(g, device="cuda", nbytes=0):
 
 
 def run_gemm(g, p, *, nan_c=False, stream=None, a_elem_offset=0, b_elem_offset=0, device="cuda",
-             use_workspace=True):
-    """Run problem ``p`` on the GPU; guards and padding columns must stay intact."""
+             use_workspace=True, baseline=None):
+    """Run problem ``p`` on the GPU; guards and padding columns must stay intact.  With ``baseline``
+    (a BASELINE_* kind) the call goes to gemm_baseline instead of gemm."""
     view = wl.CODE_VIEW[p.c_dtype]
     n = p.C.numel()
     host = torch.full((2 * GUARD + n,), CANARY[p.c_dtype], dtype=view)
@@ -72,10 +73,15 @@ def run_gemm(g, p, *, nan_c=False, stream=None, a_elem_offset=0, b_elem_offset=0
     path = g.gemm_query_path(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr,
                              p.b_stride_k, p.b_stride_n, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta,
                              bias, p.epilogue)
-    ws = workspace(g, device, g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype)) if use_workspace else None
-    g.gemm(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr, p.b_stride_k, p.b_stride_n,
-           c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue,
-           workspace=ws, workspace_bytes=0 if ws is None else ws.numel(), stream=stream)
+    if baseline is not None:
+        g.gemm_baseline(baseline, p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr,
+                        p.b_stride_k, p.b_stride_n, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue,
+                        stream=stream)
+    else:
+        ws = workspace(g, device, g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype)) if use_workspace else None
+        g.gemm(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr, p.b_stride_k, p.b_stride_n,
+               c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue,
+               workspace=ws, workspace_bytes=0 if ws is None else ws.numel(), stream=stream)
     status = g.gemm_device_status(stream)
     torch.cuda.synchronize()
     back = cbuf.cpu()

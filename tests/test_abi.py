@@ -170,3 +170,30 @@ def test_tile_policy_validation(g):
             g.gemm_set_tile_policy(policy, bn)
         assert ei.value.status == g.ERR_INVALID_ARG
     g.gemm_set_tile_policy(g.TILE_AUTO, 0)
+
+
+def test_baseline_validation_without_gpu(g):
+    """Argument and support checks of gemm_baseline happen on the host, before any CUDA call."""
+    A, B, C = 0x100000, 0x200000, 0x300000  # 16-byte aligned stand-ins, never dereferenced
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_baseline(7, 64, 64, 64, g.F16, A, 64, 1, B, 64, 1, C, 64, g.F16, 1.0, 0.0, None, g.EPI_NONE,
+                        stream=0)
+    assert e.value.status == g.ERR_INVALID_ARG
+    # mma.sync: fp16 / bf16 only
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_baseline(g.BASELINE_MMA_SYNC, 64, 64, 64, g.F32, A, 64, 1, B, 64, 1, C, 64, g.F32, 1.0, 0.0, None,
+                        g.EPI_NONE, stream=0)
+    assert e.value.status == g.ERR_UNSUPPORTED
+    # mma.sync: K-contiguous A needs K % 8 == 0
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_baseline(g.BASELINE_MMA_SYNC, 64, 64, 60, g.F16, A, 64, 1, B, 64, 1, C, 64, g.F16, 1.0, 0.0, None,
+                        g.EPI_NONE, stream=0)
+    assert e.value.status == g.ERR_UNSUPPORTED
+    # mma.sync: strides the TMA could not take (odd row pitch)
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_baseline(g.BASELINE_MMA_SYNC, 64, 64, 64, g.F16, A, 65, 1, B, 64, 1, C, 64, g.F16, 1.0, 0.0, None,
+                        g.EPI_NONE, stream=0)
+    assert e.value.status == g.ERR_UNSUPPORTED
+    # no-op sizes succeed without a device
+    assert g.gemm_baseline(g.BASELINE_MMA_SYNC, 0, 64, 64, g.F16, A, 64, 1, B, 64, 1, C, 64, g.F16, 1.0, 0.0,
+                           None, g.EPI_NONE, stream=0) == 0

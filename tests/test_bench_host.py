@@ -117,3 +117,15 @@ def test_describe_launch():
     one = dict(pair, kind=1, bn=128, cluster_ctas=1, grid_ctas=152, transposed=0, stream_k_tiles=0)
     assert bench.describe_launch(one) == "gemm_tcgen05_kernel 128x128 tiles, 152 CTAs"
     assert bench.describe_launch({"path": 3, "kind": 0}) == "path 3"
+
+
+def test_baseline_gate_arithmetic():
+    import bench
+    # 152 SMs at 2070 MHz: 152 * 512 flop/clk * 2.07e9 = 161.1 TFLOP/s
+    assert abs(bench.alu_fp16_roofline_tflops(152, 2070.0) - 161.1) < 0.1
+    v = bench.gate_verdict(1400.0, 161.1, 30.0, 1000.0)
+    assert v["over_strongest"] == 1.4 and v["win"] is True and v["over_mma_sync"] == 1.4
+    v = bench.gate_verdict(1050.0, 161.1, 30.0, 1000.0)
+    assert v["win"] is False and v["over_strongest"] == 1.05
+    # the strongest explanation may be the roofline itself
+    assert bench.gate_verdict(170.0, 161.1, 30.0, 100.0)["over_strongest"] == round(170.0 / 161.1, 3)
