@@ -298,3 +298,109 @@ def random_problem(seed: int, M: int, N: int, K: int, ab_dtype: int, c_dtype: in
                         ldb_pad=ldb_pad, ldc=N + ldc_pad, alpha=alpha, beta=beta, bias=bias,
                         epilogue=epilogue,
                         recipe=f"random seed={seed} {M}x{N}x{K} ab={ab_dtype} c={c_dtype} {layout} int={integer}")
+
+
+# ---------------------------------------------------------------------------
+# 4-bit group-quantized weights (affine, 64 values per group along K).
+# ---------------------------------------------------------------------------
+Q4_GROUP = 64
+
+
+@dataclasses.dataclass
+class Q4Problem:
+    """One quantized-matmul call: y = cast(act(alpha * x @ W^T + beta*C + bias)).
+
+    ``X`` is M x ldx row-major storage of x (x_dtype); ``Wq`` holds N*K/8
+    little-endian 32-bit words, code q[n][k] in bits 4*(k%8).. of word
+    n*K/8 + k//8; ``SB`` holds N*K/64 pairs of binary16 codes (scale, bias)
+    of the groups of 64 consecutive k of one row n: W = scale*q + bias.
+    """
+
+    name: str
+    M: int
+    N: int
+    K: int
+    x_dtype: int
+    c_dtype: int
+    X: torch.Tensor
+    ldx: int
+    Wq: torch.Tensor
+    SB: torch.Tensor
+    C: torch.Tensor
+    ldc: int
+    alpha: float
+    beta: float
+    bias: Optional[torch.Tensor]
+    epilogue: int
+    recipe: str
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def weight_bytes(self) -> int:
+        return self.Wq.numel() * 4 + self.SB.numel() * 2
+
+    def oracle_args(self) -> dict:
+        return dict(M=self.M, N=self.N, K=self.K, x_dtype=self.x_dtype,
+                    X=self.X.view(CODE_VIEW[self.x_dtype]).numpy(), ldx=self.ldx,
+                    Wq=self.Wq.numpy(), scale_bias=self.SB.numpy(),
+                    C=self.C.view(CODE_VIEW[self.c_dtype]).numpy(), ldc=self.ldc, c_dtype=self.c_dtype,
+                    alpha=self.alpha, beta=self.beta,
+                    bias=None if self.bias is None else self.bias.numpy(), epilogue=self.epilogue)
+
+
+def pack_q4(q: torch.Tensor) -> torch.Tensor:
+    """Pack N x K codes 0..15 into N*K/8 int32 words, code k%8 at bits 4*(k%8)."""
+    N, K = q.shape
+    q = q.to(torch.int64).reshape(N, K // 8, 8)
+    words = torch.zeros((N, K // 8), dtype=torch.int64)
+    for j in range(8):
+        words |= q[:, :, j] << (4 * j)
+    words = torch.where(words >= 2 ** 31, words - 2 ** 32, words)  # the same 32 bits as a signed int
+    return words.to(torch.int32).reshape(-1)
+
+
+def quantize_q4(w: torch.Tensor):
+    """Affine 4-bit group quantization of an N x K float32 matrix: per group of 64
+    along K, bias = fp16(min), scale = fp16((max - min) / 15), q = clamp(round((w -
+    bias) / scale), 0, 15) with the rounded scale and bias.  Returns (q, scale, bias)
+    as N x K int64 and N x K/64 float16 tensors."""
+    N, K = w.shape
+    g = w.reshape(N, K // Q4_GROUP, Q4_GROUP)
+    lo, hi = g.min(dim=2).values, g.max(dim=2).values
+    bias = lo.to(torch.float16)
+    scale = ((hi - lo) / 15.0).to(torch.float16)
+    s = scale.to(torch.float32)[:, :, None]
+    b = bias.to(torch.float32)[:, :, None]
+    q = torch.where(s > 0, torch.round((g - b) / torch.where(s > 0, s, torch.ones_like(s))), torch.zeros_like(g))
+    q = q.clamp(0, 15).to(torch.int64).reshape(N, K)
+    return q, scale, bias
+
+
+def q4_problem(seed: int, M: int, N: int, K: int, x_dtype: int = F16, c_dtype: int = F16, *,
+               alpha: float = 1.0, beta: float = 0.0, epilogue: int = EPI_NONE, integer: bool = False,
+               ldc_pad: int = 0, w_std: float = 0.02) -> Q4Problem:
+    """Seeded quantized-matmul problem.  Weights: W ~ N(0, w_std^2) quantized by
+    quantize_q4 (the usual 4-bit recipe for an LLM layer); x ~ N(0, 1) in x_dtype.
+    With ``integer``: codes uniform in 0..15, scale in {1, 2}, bias in -8..0 and x
+    small integers, so every product and sum is exact in fp32 accumulation."""
+    if integer:
+        q = torch.randint(0, 16, (N, K), generator=_gen(seed))
+        scale = torch.randint(1, 3, (N, K // Q4_GROUP), generator=_gen(seed + 1)).to(torch.float16)
+        bias = torch.randint(-8, 1, (N, K // Q4_GROUP), generator=_gen(seed + 2)).to(torch.float16)
+        x = small_integers(seed + 3, M, K, bound=2)
+    else:
+        q, scale, bias = quantize_q4(normal(seed, N, K, std=w_std))
+        x = normal(seed + 3, M, K)
+    sb = torch.stack([scale, bias], dim=2).reshape(-1).contiguous()
+    X = x.to(TORCH_DTYPE[x_dtype]).reshape(-1).contiguous()
+    c = normal(seed + 4, M, N) if beta != 0 else None
+    ldc = N + ldc_pad
+    C = lay_out_c(None if c is None else c.to(TORCH_DTYPE[c_dtype]), M, N, ldc, c_dtype)
+    bvec = normal(seed + 5, 1, N, std=0.1).reshape(N) if epilogue != EPI_NONE else None
+    return Q4Problem(name=f"q4_s{seed}_{M}x{N}x{K}_{DTYPE_NAME[x_dtype]}_{DTYPE_NAME[c_dtype]}", M=M, N=N, K=K,
+                     x_dtype=x_dtype, c_dtype=c_dtype, X=X, ldx=K, Wq=pack_q4(q), SB=sb.view(torch.int16),
+                     C=C, ldc=ldc, alpha=alpha, beta=beta, bias=bvec, epilogue=epilogue,
+                     recipe=f"q4 seed={seed} {M}x{N}x{K} x={x_dtype} c={c_dtype} int={integer} w_std={w_std}")
