@@ -47,6 +47,9 @@ def _args(argv=None):
     ap.add_argument("--size", type=int, default=4096)
     ap.add_argument("--no-cells", action="store_true", help="skip the extra per-dtype cells")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    ap.add_argument("--q4-decode", type=int, default=0, metavar="M",
+                    help="only the quantized decode cell with M rows of x (for profiling); prints its JSON")
+    ap.add_argument("--q4-reps", type=int, default=50, help="timed calls of the --q4-decode cell")
     return ap.parse_args(argv)
 
 
@@ -265,40 +268,63 @@ def describe_launch(info):
 
 
 def e2e_measure(g, p, steps, stream):
-    """Same metric through the public call with host buffers: H2D of A, B, C
-    from pinned memory, the GEMM, and D2H of C inside each timed step."""
+    """Same metric through the public call with host buffers: every step copies
+    its inputs A, B, C from pinned host memory, runs the GEMM and copies C back,
+    all inside the timed region.  Steps are pipelined the way a serving loop
+    would run them: copy-in, GEMM and copy-out each have a stream, device
+    buffers alternate between two sets, and events order each step's three
+    parts, so step i+1's copy-in overlaps step i's GEMM and step i-1's
+    copy-out (the host-device link is the bound either way)."""
     import torch
     dev = torch.device("cuda", torch.cuda.current_device())
     hA, hB, hC = p.A.pin_memory(), p.B.pin_memory(), p.C.clone().pin_memory()
-    dA, dB, dC = torch.empty_like(hA, device=dev), torch.empty_like(hB, device=dev), torch.empty_like(hC, device=dev)
-    hOut = torch.empty_like(hC).pin_memory()
+    d_sets = [(torch.empty_like(hA, device=dev), torch.empty_like(hB, device=dev), torch.empty_like(hC, device=dev))
+              for _ in range(2)]
+    h_out = [torch.empty_like(hC).pin_memory() for _ in range(2)]
     bias = None
     ws = _workspace(g, dev)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_free:
+        e.record(s_out)
 
-    def step():
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        dC.copy_(hC, non_blocking=True)
+    def step(i):
+        b = i & 1
+        dA, dB, dC = d_sets[b]
+        s_in.wait_event(ev_free[b])  # the set's previous GEMM and copy-out are done
+        with torch.cuda.stream(s_in):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            dC.copy_(hC, non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
         g.gemm(p.M, p.N, p.K, p.ab_dtype, dA, p.a_stride_m, p.a_stride_k, dB, p.b_stride_k, p.b_stride_n, dC,
                p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue, workspace=ws, workspace_bytes=ws.numel(),
                stream=stream)
-        hOut.copy_(dC, non_blocking=True)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            h_out[b].copy_(dC, non_blocking=True)
+        ev_free[b].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(steps):
+        step(i)
+    s_in.wait_stream(s_out)  # e1 after every step's copy-out
+    e1.record(s_in)
+    torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + hC.numel() * hC.element_size()
-    d2h = hOut.numel() * hOut.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
     return {"value": round(p.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "pipelined": "copy-in / GEMM / copy-out streams, two device buffer sets"}
 
 
 def cpu_baseline(p, seconds, single_sample=False):
@@ -377,7 +403,7 @@ def run_ours(a):
         "launch": launch,
     }
     if rank == 0:
-        out["e2e"] = e2e_measure(g, p, 10, stream)
+        out["e2e"] = e2e_measure(g, p, 30, stream)
         del sets
         torch.cuda.empty_cache()
         if not a.no_cells and world == 1:
@@ -409,7 +435,58 @@ def extra_cells(g, stream):
                                "fused_cost_pct": round(100 * (plain["median_tflops"] / fused["median_tflops"] - 1),
                                                        2)}
     cells["baseline_gate_fp16_4096"] = baseline_gate(g, stream)
+    for M in (1, 8):
+        cells[f"q4_decode_M{M}_16384"] = q4_decode_cell(g, stream, M)
     return cells
+
+
+def q4_decode_cell(g, stream, M, N=16384, K=16384, reps=50):
+    """Decode with 4-bit group-quantized weights (gemm_q4): M rows of x against an
+    N x K weight matrix, HBM-bound.  Two weight sets (2 x 151 MB > L2) alternate;
+    codes and scale/bias are seeded random (uniform codes 0..15, scales in
+    [2^-10, 2^-8), biases -8 x scale), x ~ N(0,1) fp16, fp16 output.  Roofline:
+    algorithmic bytes (weights + scales + x + y) per call / mean call time,
+    against the measured HBM copy bandwidth."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    sets = []
+    for _ in range(2):
+        wq = torch.randint(-2 ** 31, 2 ** 31 - 1, (N * K // 8,), dtype=torch.int32, device=dev, generator=gen)
+        s = (torch.rand(N * K // 64, device=dev, generator=gen) * 3 + 1) * 2.0 ** -10
+        sb = torch.stack([s, -8 * s], dim=1).to(torch.float16).reshape(-1)
+        x = torch.randn(M * K, device=dev, generator=gen).to(torch.float16)
+        sets.append((x, wq, sb, torch.empty(M * N, dtype=torch.float16, device=dev)))
+
+    def call(i):
+        x, wq, sb, y = sets[i % 2]
+        g.gemm_q4(M, N, K, g.F16, x, K, wq, sb, y, N, g.F16, 1.0, 0.0, None, g.EPI_NONE, stream=stream)
+
+    for i in range(5):
+        call(i)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record(stream)
+    for i in range(reps):
+        call(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    st = g.gemm_device_status()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+    nbytes = N * K // 2 + (N * K // 64) * 4 + M * K * 2 + M * N * 2
+    gbs = [nbytes / (t * 1e-3) / 1e9 for t in per]
+    med, ci = bootstrap_ci(gbs)
+    mean_ms = ev[0].elapsed_time(ev[reps]) / reps
+    achieved = nbytes / (mean_ms * 1e-3) / 1e9
+    peak = measured_peaks()["hbm_gbs"]
+    del sets
+    torch.cuda.empty_cache()
+    return {"M": M, "N": N, "K": K, "bytes_per_call": nbytes, "median_gbs": round(med, 1),
+            "ci95": [round(ci[0], 1), round(ci[1], 1)], "mean_us": round(mean_ms * 1e3, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4)},
+            "tflops": round(2.0 * M * N * K / (mean_ms * 1e-3) / 1e12, 2), "reps": reps, "status": st}
 
 
 def alu_fp16_roofline_tflops(num_sms, sm_mhz):
@@ -484,7 +561,11 @@ def main(argv=None):
     a = _args(argv)
     if a.warmup < 3 and a.impl == "ours":
         raise SystemExit("--warmup must be >= 3")
-    if a.impl == "reference":
+    if a.q4_decode:
+        import torch
+        import dense_gemm_epilogues_tcgen05_gb300 as g
+        print(json.dumps(q4_decode_cell(g, torch.cuda.current_stream(), a.q4_decode, reps=a.q4_reps)), flush=True)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)

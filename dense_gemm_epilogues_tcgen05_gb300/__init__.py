@@ -24,7 +24,7 @@ __all__ = [
     "GemmError", "gemm", "gemm_query_path", "gemm_workspace_size", "gemm_bias_gelu",
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K", "ORDER_AUTO", "ORDER_AS_GIVEN", "ORDER_TRANSPOSED",
     "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast", "gemm_last_launch",
-    "BASELINE_SIMT", "BASELINE_MMA_SYNC", "gemm_baseline",
+    "BASELINE_SIMT", "BASELINE_MMA_SYNC", "gemm_baseline", "gemm_q4", "gemm_q4_dequantize", "Q4_MAX_ROWS",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
@@ -45,6 +45,8 @@ ORDER_AUTO, ORDER_AS_GIVEN, ORDER_TRANSPOSED = 0, 1, 2
 MCAST_AUTO, MCAST_OFF, MCAST_ON = 0, 1, 2
 # gemm_baseline_t
 BASELINE_SIMT, BASELINE_MMA_SYNC = 0, 1
+# gemm_q4 takes at most this many rows of x (decode)
+Q4_MAX_ROWS = 8
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -94,6 +96,13 @@ class _LaunchInfo(ctypes.Structure):
 
 lib.gemm_last_launch.restype = _int
 lib.gemm_last_launch.argtypes = [ctypes.POINTER(_LaunchInfo)]
+lib.gemm_q4.restype = _int
+lib.gemm_q4.argtypes = [_i64, _i64, _i64, _int, ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p,
+                        ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
+                        ctypes.c_void_p]
+lib.gemm_q4_dequantize.restype = _int
+lib.gemm_q4_dequantize.argtypes = [_i64, _i64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, _int,
+                                   ctypes.c_void_p]
 lib.gemm_baseline.restype = _int
 lib.gemm_baseline.argtypes = [_int, _i64, _i64, _i64, _int, ctypes.c_void_p, _i64, _i64, ctypes.c_void_p, _i64, _i64,
                               ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
@@ -209,6 +218,20 @@ def gemm_baseline(kind, M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_strid
     st = lib.gemm_baseline(kind, M, N, K, ab_dtype, _ptr(A), a_stride_m, a_stride_k, _ptr(B), b_stride_k, b_stride_n,
                            _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue, _stream(stream))
     return _check(st, "gemm_baseline")
+
+
+def gemm_q4(M, N, K, x_dtype, X, ldx, Wq, scale_bias, C, ldc, c_dtype, alpha, beta, bias, epilogue,
+            stream=None) -> int:
+    """C = cast(epilogue(alpha * x W^T + beta*C + bias)) with 4-bit group-quantized W (decode, M <= 8)."""
+    st = lib.gemm_q4(M, N, K, x_dtype, _ptr(X), ldx, _ptr(Wq), _ptr(scale_bias), _ptr(C), ldc, c_dtype, alpha,
+                     beta, _ptr(bias), epilogue, _stream(stream))
+    return _check(st, "gemm_q4")
+
+
+def gemm_q4_dequantize(N, K, Wq, scale_bias, W, w_dtype, stream=None) -> int:
+    """W = round(s*q + b) as an N x K row-major fp16 / bf16 array (prefill: then gemm())."""
+    st = lib.gemm_q4_dequantize(N, K, _ptr(Wq), _ptr(scale_bias), _ptr(W), w_dtype, _stream(stream))
+    return _check(st, "gemm_q4_dequantize")
 
 
 def gemm_last_launch() -> dict:

@@ -870,6 +870,73 @@ gemm_status_t gemm_baseline(gemm_baseline_t kind, int64_t M, int64_t N, int64_t 
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, const void *X, int64_t ldx,
+                      const uint32_t *Wq, const void *scale_bias, void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                      float alpha, float beta, const float *bias, gemm_epilogue_t epilogue, gemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    if (!valid_dtype(x_dtype) || !valid_dtype(c_dtype)) return GEMM_ERR_INVALID_ARG;
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
+    if (x_dtype != GEMM_F16 && x_dtype != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
+    if (c_dtype == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+    if (K % 64 != 0) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (M > kQ4MaxRows) return GEMM_ERR_UNSUPPORTED;
+    if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (epilogue != GEMM_EPI_NONE && bias == nullptr) return GEMM_ERR_INVALID_ARG;
+    const bool reads_x = K > 0 && alpha != 0.0f;
+    if (reads_x) {
+        if (X == nullptr || Wq == nullptr || scale_bias == nullptr || ldx < K) return GEMM_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(X) & 15u) != 0 || (ldx * 2) % 16 != 0 ||
+            (reinterpret_cast<uintptr_t>(Wq) & 15u) != 0 || (reinterpret_cast<uintptr_t>(scale_bias) & 3u) != 0)
+            return GEMM_ERR_MISALIGNED;
+    }
+    if (!driver_fns().ok) return GEMM_ERR_CUDA;
+    DeviceState *dev = nullptr;
+    gemm_status_t st;
+    if ((st = device_state(&dev)) != GEMM_OK) return st;
+    if ((st = check_range(C, span_bytes(M, N, ldc, 1, elem_bytes(c_dtype)))) != GEMM_OK) return st;
+    if (epilogue != GEMM_EPI_NONE && (st = check_range(bias, static_cast<size_t>(N) * 4)) != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const EpiParams e = make_epi(M, N, C, ldc, c_dtype, alpha, beta, bias, epilogue);
+    if (!reads_x) return launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    if ((st = check_range(X, span_bytes(M, K, ldx, 1, 2))) != GEMM_OK) return st;
+    if ((st = check_range(Wq, static_cast<size_t>(N) * static_cast<size_t>(K / 8) * 4)) != GEMM_OK) return st;
+    if ((st = check_range(scale_bias, static_cast<size_t>(N) * static_cast<size_t>(K / 64) * 4)) != GEMM_OK)
+        return st;
+    Q4Args a;
+    a.e = e;
+    a.K = static_cast<int>(K);
+    a.X = X;
+    a.ldx = ldx;
+    a.Wq = Wq;
+    a.SB = static_cast<const uint32_t *>(scale_bias);
+    return launch_q4_gemv(x_dtype, c_dtype, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_q4_dequantize(int64_t N, int64_t K, const uint32_t *Wq, const void *scale_bias, void *W,
+                                 gemm_dtype_t w_dtype, gemm_stream_t stream) {
+    if (N < 0 || K < 0 || K % 64 != 0) return GEMM_ERR_INVALID_ARG;
+    if (w_dtype != GEMM_F16 && w_dtype != GEMM_BF16) return valid_dtype(w_dtype) ? GEMM_ERR_UNSUPPORTED
+                                                                                 : GEMM_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return GEMM_OK;
+    if (Wq == nullptr || scale_bias == nullptr || W == nullptr) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(Wq) & 3u) != 0 || (reinterpret_cast<uintptr_t>(scale_bias) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(W) & 15u) != 0)
+        return GEMM_ERR_MISALIGNED;
+    if (!driver_fns().ok) return GEMM_ERR_CUDA;
+    DeviceState *dev = nullptr;
+    gemm_status_t st;
+    if ((st = device_state(&dev)) != GEMM_OK) return st;
+    if ((st = check_range(Wq, static_cast<size_t>(N) * static_cast<size_t>(K / 8) * 4)) != GEMM_OK) return st;
+    if ((st = check_range(scale_bias, static_cast<size_t>(N) * static_cast<size_t>(K / 64) * 4)) != GEMM_OK)
+        return st;
+    if ((st = check_range(W, static_cast<size_t>(N) * static_cast<size_t>(K) * 2)) != GEMM_OK) return st;
+    return launch_q4_dequantize(w_dtype, N, K, Wq, static_cast<const uint32_t *>(scale_bias), W,
+                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_CUDA;
+}
+
 gemm_status_t gemm_wait_selftest(const unsigned int *never_set, uint64_t limit_ns, gemm_stream_t stream) {
     if (never_set == nullptr || limit_ns == 0 || limit_ns > 1000000000ull) return GEMM_ERR_INVALID_ARG;
     if (!driver_fns().ok) return GEMM_ERR_CUDA;

@@ -71,6 +71,16 @@ struct SimtArgs {
     long long sbk, sbn;
 };
 
+// Quantized matrix product (4-bit codes, 64 per group along K; see gemm_q4.cu).
+struct Q4Args {
+    EpiParams e;              // M rows of x / C, N outputs per row, C, ldc, alpha, beta, bias, epilogue
+    int K;
+    const void *X;            // M x ldx row-major, fp16 or bf16
+    long long ldx;
+    const uint32_t *Wq;       // N * K/8 words: code of (n, k) in bits 4*(k%8) of word n*K/8 + k/8
+    const uint32_t *SB;       // N * K/64 words: binary16 scale (low half) and bias (high half) of group (n, g)
+};
+
 // Launchers (each returns the launch's cudaError_t), defined by the kernel files.
 //   one-SM tcgen05 kernel, `bn` = 256 or 128, `grid` CTAs:
 cudaError_t launch_tcgen05_f16(int out, int bn, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int grid,
@@ -104,6 +114,11 @@ cudaError_t launch_mma_sync(int ab, int out, const SimtArgs &args, bool a_k_cont
                             cudaStream_t stream);
 cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t stream);
 cudaError_t launch_bias_gelu(int out, const EpiParams &e, cudaStream_t stream);
+//   4-bit quantized product for up to kQ4MaxRows rows of x, and the dequantisation pass:
+constexpr int kQ4MaxRows = 8;
+cudaError_t launch_q4_gemv(int x_dtype, int out, const Q4Args &args, cudaStream_t stream);
+cudaError_t launch_q4_dequantize(int out, long long N, long long K, const uint32_t *Wq, const uint32_t *SB, void *W,
+                                 cudaStream_t stream);
 cudaError_t launch_wait_selftest(const unsigned int *never_set, unsigned long long limit_ns, unsigned int *status,
                                  cudaStream_t stream);
 

@@ -329,6 +329,52 @@ gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dt
                              const float *bias, gemm_stream_t stream);
 
 /*
+ * Products with 4-bit group-quantized weights.  "X3: Metal GEMM" section 7
+ * names quantized matmul -- a memory-bound GEMV when decoding, a GEMM when
+ * filling the prompt -- as the main LLM workload; the pages give no storage
+ * format, so this library takes the affine one with groups of 64 along K:
+ *
+ *     W[n][k] = s[n][k/64] * q[n][k] + b[n][k/64],   q[n][k] in 0..15,
+ *
+ * W being N x K (output features x input features).
+ *   Wq          N*K/8 32-bit words, 16-byte aligned: q[n][k] is bits
+ *               4*(k%8) .. 4*(k%8)+3 of word n*K/8 + k/8.
+ *   scale_bias  N*K/64 pairs of binary16 values (s, b), in that order, one
+ *               pair per group (n, g) at pair index n*K/64 + g; 4-byte aligned.
+ */
+
+/*
+ * gemm_q4 -- C = cast(epilogue(alpha * x W^T + beta*C + bias)) for M rows of
+ * x (decode: 1 <= M <= 8; M == 0 or N == 0 is a no-op).
+ *   x_dtype     F16 or BF16.  X is M x ldx row-major, 16-byte aligned base,
+ *               ldx >= K with ldx*2 a multiple of 16.
+ *   K           a multiple of 64.
+ *   C, c_dtype, ldc, alpha, beta, bias, epilogue: as in gemm(), with the
+ *               output M x N and bias fp32[N]; the same fused epilogues.
+ * Larger M: GEMM_ERR_UNSUPPORTED -- dequantise once with gemm_q4_dequantize
+ * and call gemm() (the dense tensor-core path), which is how this library
+ * does prefill.  Asynchronous on `stream`; errors as gemm().
+ */
+gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype,
+                      const void *X, int64_t ldx,
+                      const uint32_t *Wq, const void *scale_bias,
+                      void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                      float alpha, float beta,
+                      const float *bias, gemm_epilogue_t epilogue,
+                      gemm_stream_t stream);
+
+/*
+ * gemm_q4_dequantize -- W[n][k] = round(s*q + b) into the N x K row-major
+ * device array W of type w_dtype (F16 or BF16; 16-byte aligned), for
+ * gemm(M, N, K, w_dtype, X, ldx, 1, W, 1, K, ...) to multiply (W^T as B,
+ * K-contiguous).  The rounding to 16 bits is the only difference from the
+ * exact product: at most 2^-11 (F16) or 2^-8 (BF16) of each |W| value.
+ * K a multiple of 64.  Asynchronous on `stream`; errors as gemm().
+ */
+gemm_status_t gemm_q4_dequantize(int64_t N, int64_t K, const uint32_t *Wq, const void *scale_bias,
+                                 void *W, gemm_dtype_t w_dtype, gemm_stream_t stream);
+
+/*
  * Baselines of the cheap-baseline gate (Rigel section 3; section 4, signal
  * 2): a claim that the tensor path is fast stands only once the trivial
  * explanations have run and lost -- a GEMM on the ordinary ALUs, and the

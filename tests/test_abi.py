@@ -197,3 +197,31 @@ def test_baseline_validation_without_gpu(g):
     # no-op sizes succeed without a device
     assert g.gemm_baseline(g.BASELINE_MMA_SYNC, 0, 64, 64, g.F16, A, 64, 1, B, 64, 1, C, 64, g.F16, 1.0, 0.0,
                            None, g.EPI_NONE, stream=0) == 0
+
+
+def test_q4_validation_without_gpu(g):
+    X, W, SB, C = 0x100000, 0x200000, 0x300000, 0x400000
+    def call(M=1, N=64, K=128, xd=None, ldx=128, X=X, W=W, SB=SB, cd=None, epi=None, bias=None):
+        return g.gemm_q4(M, N, K, g.F16 if xd is None else xd, X, ldx, W, SB, C, N, g.F16 if cd is None else cd,
+                         1.0, 0.0, bias, g.EPI_NONE if epi is None else epi, stream=0)
+    for kwargs, status in [(dict(K=100), g.ERR_INVALID_ARG),             # K not a multiple of 64
+                           (dict(M=9), g.ERR_UNSUPPORTED),               # decode only
+                           (dict(xd=g.F32), g.ERR_UNSUPPORTED),
+                           (dict(xd=g.E4M3), g.ERR_UNSUPPORTED),
+                           (dict(cd=g.E4M3), g.ERR_UNSUPPORTED),
+                           (dict(ldx=100), g.ERR_INVALID_ARG),           # ldx < K
+                           (dict(ldx=132), g.ERR_MISALIGNED),            # row pitch not a multiple of 16 bytes
+                           (dict(X=X + 2), g.ERR_MISALIGNED),
+                           (dict(W=W + 4), g.ERR_MISALIGNED),
+                           (dict(epi=g.EPI_BIAS), g.ERR_INVALID_ARG)]:   # bias missing
+        with pytest.raises(g.GemmError) as e:
+            call(**kwargs)
+        assert e.value.status == status, kwargs
+    assert call(M=0) == 0 and call(N=0) == 0
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_q4_dequantize(64, 100, W, SB, C, g.F16, stream=0)
+    assert e.value.status == g.ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_q4_dequantize(64, 128, W, SB, C, g.F32, stream=0)
+    assert e.value.status == g.ERR_UNSUPPORTED
+    assert g.gemm_q4_dequantize(0, 128, W, SB, C, g.F16, stream=0) == 0

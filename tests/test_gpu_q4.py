@@ -1,0 +1,131 @@
+"""GPU parity of the 4-bit quantized products (gemm_q4, gemm_q4_dequantize)
+against the float64 oracle (oracle.q4), through the C ABI.
+
+* Integer-valued problems (codes 0..15, scale 1 or 2, bias -8..0, x in -2..2:
+  every product and partial sum exact in fp32) come back bit-exact with fp32
+  output, for every row count 1..8, ragged N and K not a multiple of a warp's
+  1024-deep step.
+* Realistic problems (N(0, 0.02^2) weights quantized per group, x ~ N(0,1))
+  meet the normalised tolerance for every output type and epilogue.
+* The full-size decode workload (1 x 16384 x 16384) is checked on sampled
+  output columns, from the oracle on those weight rows alone.
+* The dequantisation pass is exact (rounding of s*q + b, which fp32 holds
+  exactly for these inputs), and dequantise-then-gemm() meets the tolerance.
+Every call also checks that nothing outside the M x N block of C was written.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import CANARY, GUARD
+from oracle import q4
+
+pytestmark = pytest.mark.gpu
+
+
+def run_q4(g, p):
+    """Run a Q4Problem on the GPU with guarded C; returns the output codes (M x ldc flat)."""
+    view = wl.CODE_VIEW[p.c_dtype]
+    n = p.C.numel()
+    host = torch.full((2 * GUARD + n,), CANARY[p.c_dtype], dtype=view)
+    mid = host[GUARD:GUARD + n]
+    mid.copy_(p.C.view(view))
+    mid.view(p.M, p.ldc)[:, p.N:] = CANARY[p.c_dtype]
+    cbuf = host.cuda()
+    c_ptr = cbuf.data_ptr() + GUARD * cbuf.element_size()
+    X, Wq, SB = p.X.cuda(), p.Wq.cuda(), p.SB.cuda()
+    bias = None if p.bias is None else p.bias.cuda()
+    g.gemm_q4(p.M, p.N, p.K, p.x_dtype, X, p.ldx, Wq, SB, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias,
+              p.epilogue)
+    assert g.gemm_device_status() == 0
+    back = cbuf.cpu()
+    assert bool((back[:GUARD] == CANARY[p.c_dtype]).all()) and bool((back[GUARD + n:] == CANARY[p.c_dtype]).all())
+    out = back[GUARD:GUARD + n]
+    assert bool((out.view(p.M, p.ldc)[:, p.N:] == CANARY[p.c_dtype]).all()), "ldc padding overwritten"
+    return out.numpy()
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("N,K", [(1, 64), (7, 1088), (64, 1024), (129, 4096)], ids=lambda v: str(v))
+@pytest.mark.parametrize("xd", [wl.F16, wl.BF16], ids=["f16", "bf16"])
+def test_integer_exact(cuda_lib, M, N, K, xd):
+    p = wl.q4_problem(100 + M + N + K, M, N, K, xd, wl.F32, integer=True, ldc_pad=3)
+    out = run_q4(cuda_lib, p)
+    y, _ = q4.q4_reference(**p.oracle_args())
+    got = oracle.output_values(out, p.M, p.N, p.ldc, p.c_dtype)
+    assert np.array_equal(got, y)
+
+
+@pytest.mark.parametrize("cd", [wl.F16, wl.BF16, wl.F32], ids=["f16", "bf16", "f32"])
+@pytest.mark.parametrize("epi", [wl.EPI_NONE, wl.EPI_BIAS, wl.EPI_BIAS_GELU, wl.EPI_BIAS_SILU],
+                         ids=["none", "bias", "gelu", "silu"])
+def test_realistic_tolerance(cuda_lib, cd, epi):
+    for M, xd in ((1, wl.F16), (4, wl.BF16), (8, wl.F16)):
+        p = wl.q4_problem(7 + M, M, 320, 2048, xd, cd, alpha=1.25, beta=0.5 if epi == wl.EPI_NONE else 0.0,
+                          epilogue=epi)
+        res = q4.check(p.oracle_args(), run_q4(cuda_lib, p))
+        assert res["pass"], (M, res)
+
+
+def test_degenerate(cuda_lib):
+    g = cuda_lib
+    # alpha == 0: C = beta*C, weights unread (NULL pointers accepted)
+    p = wl.q4_problem(3, 2, 40, 128, wl.F16, wl.F32, alpha=0.0, beta=0.5)
+    C = p.C.cuda()
+    g.gemm_q4(2, 40, 128, wl.F16, None, 128, None, None, C, p.ldc, wl.F32, 0.0, 0.5, None, wl.EPI_NONE)
+    assert g.gemm_device_status() == 0
+    y, _ = q4.q4_reference(**p.oracle_args())
+    assert np.array_equal(C.cpu().numpy().reshape(2, -1)[:, :40], y.astype(np.float32))
+    # more than 8 rows is the dense path's job
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_q4(9, 40, 128, wl.F16, p.X.cuda(), 128, p.Wq.cuda(), p.SB.cuda(), C, p.ldc, wl.F32, 1.0, 0.0, None,
+                  wl.EPI_NONE)
+    assert e.value.status == g.ERR_UNSUPPORTED
+
+
+def test_decode_workload_sampled_columns(cuda_lib):
+    """1 x 16384 x 16384 (the bench's decode cell) on 96 sampled outputs, against the
+    oracle run on just those weight rows (an output column needs only its row of W)."""
+    N = K = 16384
+    p = wl.q4_problem(41, 1, N, K, wl.F16, wl.F16)
+    out = run_q4(cuda_lib, p)
+    rng = np.random.default_rng(7)
+    cols = np.unique(np.concatenate([[0, 1, N - 1], rng.integers(0, N, 93)]))
+    a = p.oracle_args()
+    wq = a["Wq"].reshape(N, K // 8)[cols].reshape(-1)
+    sb = a["scale_bias"].reshape(N, K // 64 * 2)[cols].reshape(-1)
+    sub = dict(a, N=len(cols), Wq=wq, scale_bias=sb, ldc=len(cols), C=np.zeros(len(cols), np.int16))
+    y, D = q4.q4_reference(**sub)
+    got = oracle.output_values(out, 1, N, p.ldc, p.c_dtype)[:, cols]
+    err = oracle.max_normalized_error(got, y, D, wl.EPI_NONE)
+    assert err <= oracle.tolerance(wl.F16, wl.F16), err
+
+
+@pytest.mark.parametrize("wd", [wl.F16, wl.BF16], ids=["f16", "bf16"])
+def test_dequantize_exact(cuda_lib, wd):
+    g = cuda_lib
+    p = wl.q4_problem(55, 1, 96, 1024, wd, wd)
+    W = torch.empty(96 * 1024, dtype=wl.TORCH_DTYPE[wd], device="cuda")
+    g.gemm_q4_dequantize(96, 1024, p.Wq.cuda(), p.SB.cuda(), W, wd)
+    assert g.gemm_device_status() == 0
+    exact = q4.dequantize(p.Wq.numpy(), p.SB.numpy(), 96, 1024)
+    assert np.array_equal(exact.astype(np.float32).astype(np.float64), exact)  # fp32 holds s*q + b exactly
+    want = torch.from_numpy(exact).to(torch.float32).to(wl.TORCH_DTYPE[wd]).reshape(-1)
+    assert torch.equal(W.cpu().view(torch.int16), want.view(torch.int16))
+
+
+def test_prefill_dequantize_then_gemm(cuda_lib):
+    """Prefill: dequantise to fp16 once, then the dense tensor-core gemm() with W^T as
+    B (K-contiguous).  The fp16 rounding of W adds at most 2^-11 of D."""
+    g = cuda_lib
+    M, N, K = 512, 768, 2048
+    p = wl.q4_problem(61, M, N, K, wl.F16, wl.F16, alpha=1.0)
+    W = torch.empty(N * K, dtype=torch.float16, device="cuda")
+    g.gemm_q4_dequantize(N, K, p.Wq.cuda(), p.SB.cuda(), W, wl.F16)
+    C = p.C.clone().cuda()
+    g.gemm(M, N, K, wl.F16, p.X.cuda(), K, 1, W, 1, K, C, p.ldc, wl.F16, 1.0, 0.0, None, wl.EPI_NONE)
+    assert g.gemm_device_status() == 0
+    res = q4.check(p.oracle_args(), C.cpu().view(torch.int16).numpy())
+    assert res["pass"], res
