@@ -212,7 +212,9 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
                    C: Optional[np.ndarray], ldc: int, c_dtype: int,
                    alpha: float, beta: float,
                    bias: Optional[np.ndarray], epilogue: int,
-                   rows: Optional[Sequence[int]] = None):
+                   rows: Optional[Sequence[int]] = None,
+                   alpha_scale: Optional[np.ndarray] = None, row_scale: Optional[np.ndarray] = None,
+                   col_scale: Optional[np.ndarray] = None):
     """Reference output y (float64, not rounded to the output type) and scale D.
 
     A, B, C are raw code arrays (flat) in the given element types; ``bias`` is
@@ -222,6 +224,11 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
     len(rows) x N (all M rows when ``rows`` is None), with
 
         D_ij = |alpha| * sum_k |a_ik||b_kj| + |beta||c_ij| + |bias_j|.
+
+    Optional product scales (float32 arrays, as the extended call reads them
+    from device memory; each absent one is 1): the product term becomes
+    alpha * alpha_scale[0] * row_scale[i] * col_scale[j] * sum_k a_ik b_kj,
+    and D's first term takes the same factors in absolute value.
     """
     if min(M, N, K) < 0:
         raise ValueError("negative size")
@@ -235,8 +242,14 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
     if al != 0.0 and K > 0 and R > 0 and N > 0:
         a = decode(strided_codes(A, M, K, a_stride_m, a_stride_k, row_sel), ab_dtype)
         b = decode(strided_codes(B, K, N, b_stride_k, b_stride_n), ab_dtype)
-        z += al * (a @ b)
-        D += abs(al) * (np.abs(a) @ np.abs(b))
+        f = al if alpha_scale is None else al * float(np.asarray(alpha_scale, np.float32).reshape(-1)[0])
+        fac = np.full((R, N), f, dtype=np.float64)
+        if row_scale is not None:
+            fac *= np.asarray(row_scale, np.float32).astype(np.float64).reshape(-1)[row_sel][:, None]
+        if col_scale is not None:
+            fac *= np.asarray(col_scale, np.float32).astype(np.float64).reshape(-1)[None, :N]
+        z += fac * (a @ b)
+        D += np.abs(fac) * (np.abs(a) @ np.abs(b))
     if be != 0.0 and R > 0 and N > 0:
         c = decode(strided_codes(C, M, N, ldc, 1, row_sel), c_dtype)
         z += be * c

@@ -355,3 +355,67 @@ def test_reference_applies_the_named_activation(name):
     assert oracle.max_normalized_error(oracle.gelu(z), y, D, epi) > 1e-5
     with pytest.raises(ValueError):
         oracle.gemm_reference(**dict(args, epilogue=6))
+
+
+# ------------------------------------------------------------- product scales --
+
+def test_product_scales_brute_force_exact():
+    """alpha * alpha_scale * row_scale[i] * col_scale[j] * sum_k a b, against exact rationals."""
+    from fractions import Fraction
+    for layout in ("NN", "TT"):
+        p = wl.with_product_scales(wl.random_problem(7, 3, 4, 5, wl.F16, wl.F32, layout=layout, alpha=0.5, beta=0.25,
+                                                     integer=True), 9, dyadic=True)
+        a = p.oracle_args()
+        y, _ = oracle.gemm_reference(**a)
+        A = oracle.decode(a["A"], wl.F16)
+        B = oracle.decode(a["B"], wl.F16)
+        Cv = oracle.decode(a["C"], wl.F32)
+        s0 = Fraction(float(a["alpha_scale"][0]))
+        for i in range(3):
+            for j in range(4):
+                acc = sum(Fraction(float(A[i * a["a_stride_m"] + k * a["a_stride_k"]])) *
+                          Fraction(float(B[k * a["b_stride_k"] + j * a["b_stride_n"]])) for k in range(5))
+                want = (Fraction(0.5) * s0 * Fraction(float(a["row_scale"][i])) * Fraction(float(a["col_scale"][j]))
+                        * acc + Fraction(0.25) * Fraction(float(Cv[i * a["ldc"] + j])))
+                assert Fraction(y[i, j]) == want
+
+
+def test_product_scales_of_one_change_nothing():
+    p = wl.random_problem(8, 6, 5, 9, wl.BF16, wl.F32, alpha=1.5, beta=0.5, epilogue=wl.EPI_BIAS_GELU)
+    a = p.oracle_args()
+    y0, D0 = oracle.gemm_reference(**a)
+    y1, D1 = oracle.gemm_reference(**a, alpha_scale=np.ones(1, np.float32), row_scale=np.ones(6, np.float32),
+                                   col_scale=np.ones(5, np.float32))
+    assert np.array_equal(y0, y1) and np.array_equal(D0, D1)
+
+
+def test_product_scales_factor_out_of_rows_and_columns():
+    """Power-of-two scales commute exactly with the float64 sums: y = rs_i * cs_j * s * y_unscaled."""
+    base = wl.random_problem(10, 7, 6, 33, wl.F16, wl.F32, alpha=1.0, integer=False)
+    p = wl.with_product_scales(base, 11, dyadic=True)
+    a = p.oracle_args()
+    y, D = oracle.gemm_reference(**a)
+    y0, D0 = oracle.gemm_reference(**base.oracle_args())
+    f = a["alpha_scale"][0] * np.outer(a["row_scale"], a["col_scale"]).astype(np.float64)
+    assert np.array_equal(y, f * y0) and np.array_equal(D, f * D0)
+
+
+@pytest.mark.parametrize("mistake", ["scaled_beta", "rows_for_cols", "no_alpha_scale"])
+def test_product_scale_mistakes_are_flagged(mistake):
+    p = wl.with_product_scales(wl.random_problem(12, 16, 16, 64, wl.F16, wl.F32, alpha=1.0, beta=1.0), 13)
+    a = p.oracle_args()
+    y, D = oracle.gemm_reference(**a)
+    A = oracle.decode(oracle.strided_codes(a["A"], 16, 64, a["a_stride_m"], a["a_stride_k"]), wl.F16)
+    B = oracle.decode(oracle.strided_codes(a["B"], 64, 16, a["b_stride_k"], a["b_stride_n"]), wl.F16)
+    Cv = oracle.decode(oracle.strided_codes(a["C"], 16, 16, a["ldc"], 1), wl.F32)
+    s, rs, cs = a["alpha_scale"][0], a["row_scale"].astype(np.float64), a["col_scale"].astype(np.float64)
+    prod = A @ B
+    if mistake == "scaled_beta":
+        out = s * np.outer(rs, cs) * (prod + Cv)
+    elif mistake == "rows_for_cols":
+        out = s * np.outer(cs, rs) * prod + Cv
+    else:
+        out = np.outer(rs, cs) * prod + Cv
+    assert oracle.max_normalized_error(out, y, D, wl.EPI_NONE) > oracle.TOL_F32_OUT
+    good = s * np.outer(rs, cs) * prod + Cv
+    assert oracle.max_normalized_error(good.astype(np.float32), y, D, wl.EPI_NONE) <= oracle.TOL_F32_OUT

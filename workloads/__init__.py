@@ -79,6 +79,9 @@ class Problem:
     epilogue: int
     recipe: str
     scales: dict = dataclasses.field(default_factory=dict)
+    # Product scales of the extended call (gemm_ex): float32 tensors
+    # "alpha_scale" (1 value), "row_scale" (M), "col_scale" (N); absent = 1.
+    product_scales: dict = dataclasses.field(default_factory=dict)
 
     @property
     def flops(self) -> float:
@@ -98,7 +101,8 @@ class Problem:
                     C=self.codes("C"), ldc=self.ldc, c_dtype=self.c_dtype,
                     alpha=self.alpha, beta=self.beta,
                     bias=None if self.bias is None else self.bias.numpy(),
-                    epilogue=self.epilogue)
+                    epilogue=self.epilogue,
+                    **{k: v.numpy() for k, v in self.product_scales.items()})
 
     def recipe_hash(self) -> str:
         return hashlib.sha256(self.recipe.encode()).hexdigest()[:16]
@@ -404,3 +408,26 @@ def q4_problem(seed: int, M: int, N: int, K: int, x_dtype: int = F16, c_dtype: i
                      x_dtype=x_dtype, c_dtype=c_dtype, X=X, ldx=K, Wq=pack_q4(q), SB=sb.view(torch.int16),
                      C=C, ldc=ldc, alpha=alpha, beta=beta, bias=bvec, epilogue=epilogue,
                      recipe=f"q4 seed={seed} {M}x{N}x{K} x={x_dtype} c={c_dtype} int={integer} w_std={w_std}")
+
+
+def with_product_scales(p: Problem, seed: int, *, alpha_scale: bool = True, row: bool = True, col: bool = True,
+                        dyadic: bool = False) -> Problem:
+    """Attach seeded product scales to a problem: per-tensor in [0.5, 2), per-row and
+    per-column in [0.25, 4) (log-uniform); with ``dyadic`` powers of two only (2^-2 ..
+    2^2), so that scaled integer problems stay exact in fp32."""
+    g = _gen(seed)
+
+    def draw(n):
+        if dyadic:
+            return torch.pow(2.0, torch.randint(-2, 3, (n,), generator=g).to(torch.float32))
+        return torch.pow(2.0, torch.rand((n,), generator=g) * 4.0 - 2.0)
+
+    ps = {}
+    if alpha_scale:
+        ps["alpha_scale"] = torch.pow(2.0, torch.randint(-1, 2, (1,), generator=g).to(torch.float32)) if dyadic \
+            else torch.pow(2.0, torch.rand((1,), generator=g) * 2.0 - 1.0)
+    if row:
+        ps["row_scale"] = draw(p.M)
+    if col:
+        ps["col_scale"] = draw(p.N)
+    return dataclasses.replace(p, product_scales=ps, recipe=p.recipe + f" scales(seed={seed}, dyadic={dyadic})")
