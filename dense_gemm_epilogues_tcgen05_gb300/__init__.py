@@ -25,6 +25,7 @@ __all__ = [
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K", "ORDER_AUTO", "ORDER_AS_GIVEN", "ORDER_TRANSPOSED",
     "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast", "gemm_last_launch",
     "BASELINE_SIMT", "BASELINE_MMA_SYNC", "gemm_baseline", "gemm_q4", "gemm_q4_dequantize", "Q4_MAX_ROWS",
+    "gemm_ex",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
@@ -96,6 +97,14 @@ class _LaunchInfo(ctypes.Structure):
 
 lib.gemm_last_launch.restype = _int
 lib.gemm_last_launch.argtypes = [ctypes.POINTER(_LaunchInfo)]
+class _Scales(ctypes.Structure):
+    """gemm_scales_t"""
+    _fields_ = [("alpha_scale", ctypes.c_void_p), ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p)]
+
+
+lib.gemm_ex.restype = _int
+lib.gemm_ex.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _int,
+                        _f32, _f32, _vp, _int, ctypes.POINTER(_Scales), _vp, _sz, _vp]
 lib.gemm_q4.restype = _int
 lib.gemm_q4.argtypes = [_i64, _i64, _i64, _int, ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p,
                         ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
@@ -218,6 +227,17 @@ def gemm_baseline(kind, M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_strid
     st = lib.gemm_baseline(kind, M, N, K, ab_dtype, _ptr(A), a_stride_m, a_stride_k, _ptr(B), b_stride_k, b_stride_n,
                            _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue, _stream(stream))
     return _check(st, "gemm_baseline")
+
+
+def gemm_ex(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc, c_dtype,
+            alpha, beta, bias, epilogue, alpha_scale=None, row_scale=None, col_scale=None, workspace=None,
+            workspace_bytes=0, stream=None) -> int:
+    """gemm() with product scales (device fp32 arrays: alpha_scale[1], row_scale[M], col_scale[N]; None = 1)."""
+    sc = _Scales(_ptr(alpha_scale), _ptr(row_scale), _ptr(col_scale))
+    st = lib.gemm_ex(M, N, K, ab_dtype, _ptr(A), a_stride_m, a_stride_k, _ptr(B), b_stride_k, b_stride_n,
+                     _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue, ctypes.byref(sc), _ptr(workspace),
+                     workspace_bytes, _stream(stream))
+    return _check(st, "gemm_ex")
 
 
 def gemm_q4(M, N, K, x_dtype, X, ldx, Wq, scale_bias, C, ldc, c_dtype, alpha, beta, bias, epilogue,

@@ -189,6 +189,39 @@ __device__ __forceinline__ void activate2(float &z0, float &z1, int epi) {
     }
 }
 
+// Product scale of output (row, col) beyond alpha: alpha_scale[0] * row_scale[row]
+// * col_scale[col], each factor 1 when absent (1 without any: e.scaled == 0).
+__device__ __forceinline__ float product_scale(const EpiParams &e, int row, int col) {
+    if (!e.scaled) return 1.0f;
+    float f = e.alpha_scale ? *e.alpha_scale : 1.0f;
+    if (e.row_scale) f *= e.row_scale[row];
+    if (e.col_scale) f *= e.col_scale[col];
+    return f;
+}
+
+// The same product scale over one chunk of 32 accumulators: the thread's fixed
+// index is `lane_idx`, accumulator j has running index run0 + j.  Untransposed
+// they are the output row and columns; transposed (the kernel computed C^T)
+// the output column and rows.  Running indices at or past the matrix's end
+// (masked outputs) keep factor 1.  SC = false compiles it out: kernels built
+// for calls without scales keep the registers the scaled path needs.
+template <bool SC = true>
+__device__ __forceinline__ void product_scale_chunk(float (&v)[32], const EpiParams &e, int lane_idx, int run0,
+                                                    bool transposed) {
+    if constexpr (!SC) return;
+    if (!e.scaled) return;
+    const float *lane_vec = transposed ? e.col_scale : e.row_scale;
+    const float *run_vec = transposed ? e.row_scale : e.col_scale;
+    const int lane_ext = transposed ? e.N : e.M, run_ext = transposed ? e.M : e.N;
+    float f = e.alpha_scale ? *e.alpha_scale : 1.0f;
+    if (lane_vec && lane_idx < lane_ext) f *= lane_vec[lane_idx];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float r = (run_vec && run0 + j < run_ext) ? run_vec[run0 + j] : 1.0f;
+        v[j] *= f * r;
+    }
+}
+
 // Scalar epilogue of one element (used by the safe path and the SIMT kernel).
 template <int OUT>
 __device__ __forceinline__ void epilogue_store_one(float acc, typename Elem<OUT>::T *c, float bias_j,
@@ -316,7 +349,7 @@ __device__ __forceinline__ void epilogue_chunk32_safe(const float (&v)[32], type
 // global memory, or staged in shared memory).  The TMEM load of chunk i+1 is
 // in flight while chunk i is processed.  Warp-collective (every lane calls it
 // with the same t_base, col_base and nvalid); nvalid <= MAXC.
-template <int OUT, int MAXC>
+template <int OUT, int MAXC, bool SC = true>
 __device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_base, int nvalid, int row, bool row_ok,
                                                     const float *bias_base, const EpiParams &e) {
     using OutT = typename Elem<OUT>::T;
@@ -337,6 +370,7 @@ __device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_bas
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(cur[j]);
         const int col0 = col_base + i * 32;
+        product_scale_chunk<SC>(v, e, row, col0, false);
         if (row_ok) {
             if (e.c_vec && col0 + 32 <= e.N)
                 epilogue_chunk32_fast<OUT>(v, crow + col0, bias_base + i * 32, e);
@@ -494,7 +528,7 @@ __device__ __forceinline__ void box_math_t(float (&v)[32], unsigned char *box, f
 // With e.swap the accumulators are transposed (TMEM lanes are output columns
 // row0 + lane, chunk columns are output rows col0 ..; bias_lane is the
 // lane's column bias); see box_math_t.
-template <int OUT>
+template <int OUT, bool SC = true>
 __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, int row0, const float *bias_chunk,
                                                      float bias_lane, const EpiParams &e, const CUtensorMap *tmC,
                                                      unsigned char *buf, uint64_t *cbar, uint32_t &cphase,
@@ -503,6 +537,7 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
     constexpr int NSUB = 32 / PER;
     const int lane = threadIdx.x & 31;
     scale_alpha(v, e.alpha);
+    product_scale_chunk<SC>(v, e, row0 + lane, col0, e.swap != 0);
     if constexpr (OUT != kDtF32) {
         if (e.swap) {
             if (lane == 0) bulk_wait_read<0>();
@@ -555,7 +590,7 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
 // Staged epilogue of one warp's rows row0 .. row0+31 and chunks 0 .. nvalid-1
 // of 32 columns from TMEM column address t_base / output column col_base,
 // through the warp's one box.  Warp-collective.
-template <int OUT>
+template <int OUT, bool SC = true>
 __device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base, int nvalid, int row0,
                                                   const float *bias_base, float bias_lane, const EpiParams &e,
                                                   const CUtensorMap *tmC, unsigned char *buf, uint64_t *cbar,
@@ -571,7 +606,7 @@ __device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base,
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
         if (ok)
-            ok = epilogue_chunk32_tma<OUT>(v, col_base + i * 32, row0, bias_base + i * 32, bias_lane, e, tmC, buf,
+            ok = epilogue_chunk32_tma<OUT, SC>(v, col_base + i * 32, row0, bias_base + i * 32, bias_lane, e, tmC, buf,
                                            cbar, cphase, abort_flag, status);
     }
     __syncwarp();
@@ -582,7 +617,7 @@ __device__ __forceinline__ bool epilogue_rows_tma(uint32_t t_base, int col_base,
 // the warp gets its own slot in `area` (box b of chunk i, part h at slot
 // i*NSUB + h), all C boxes are requested at once and no store waits for a
 // slot to be read, so the tail of the kernel is not a chain of round trips.
-template <int OUT>
+template <int OUT, bool SC = true>
 __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col_base, int nvalid, int row0,
                                                         const float *bias_base, float bias_lane, const EpiParams &e,
                                                         const CUtensorMap *tmC, unsigned char *area, uint64_t *cbar,
@@ -615,6 +650,7 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
                 scale_alpha(v, e.alpha);
+                product_scale_chunk<SC>(v, e, row0 + lane, col_base + i * 32, true);
                 box_math_t<OUT>(v, area + i * kStageBoxBytes, bias_lane, e);
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -654,6 +690,7 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
         scale_alpha(v, e.alpha);
+        product_scale_chunk<SC>(v, e, row0 + lane, col_base + i * 32, false);
 #pragma unroll
         for (int h = 0; h < NSUB; ++h) {
             const int x = col_base + i * 32 + h * PER;

@@ -521,6 +521,8 @@ EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alp
     e.c_vec = (c_al && b_al) ? 1 : 0;
     e.c_tma = 0;  // set by the pair-kernel launch once C's tensor map is encoded
     e.swap = 0;   // set by the pair-kernel launch when it computes C^T = B^T A^T
+    e.scaled = 0;  // product scales: set by gemm_ex
+    e.alpha_scale = e.row_scale = e.col_scale = nullptr;
     return e;
 }
 
@@ -613,10 +615,10 @@ gemm_status_t gemm_set_schedule(gemm_schedule_t schedule) {
     return GEMM_OK;
 }
 
-gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const void *A, int64_t a_stride_m,
-                   int64_t a_stride_k, const void *B, int64_t b_stride_k, int64_t b_stride_n, void *C, int64_t ldc,
-                   gemm_dtype_t c_dtype, float alpha, float beta, const float *bias, gemm_epilogue_t epilogue,
-                   void *workspace, size_t workspace_bytes, gemm_stream_t stream) {
+gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const void *A, int64_t a_stride_m,
+                      int64_t a_stride_k, const void *B, int64_t b_stride_k, int64_t b_stride_n, void *C, int64_t ldc,
+                      gemm_dtype_t c_dtype, float alpha, float beta, const float *bias, gemm_epilogue_t epilogue,
+                      const gemm_scales_t *scales, void *workspace, size_t workspace_bytes, gemm_stream_t stream) {
     Plan plan;
     gemm_status_t st = make_plan(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc,
                                  c_dtype, alpha, bias, epilogue, &plan);
@@ -632,6 +634,17 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
     if (epilogue != GEMM_EPI_NONE && (st = check_range(bias, static_cast<size_t>(N) * 4)) != GEMM_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EpiParams e = make_epi(M, N, C, ldc, c_dtype, alpha, beta, bias, epilogue);
+    if (scales != nullptr && plan.path != GEMM_PATH_EPILOGUE_ONLY) {
+        if (scales->alpha_scale && (st = check_range(scales->alpha_scale, 4)) != GEMM_OK) return st;
+        if (scales->row_scale && (st = check_range(scales->row_scale, static_cast<size_t>(M) * 4)) != GEMM_OK)
+            return st;
+        if (scales->col_scale && (st = check_range(scales->col_scale, static_cast<size_t>(N) * 4)) != GEMM_OK)
+            return st;
+        e.alpha_scale = scales->alpha_scale;
+        e.row_scale = scales->row_scale;
+        e.col_scale = scales->col_scale;
+        e.scaled = (e.alpha_scale || e.row_scale || e.col_scale) ? 1 : 0;
+    }
 
     if (plan.path == GEMM_PATH_EPILOGUE_ONLY)
         return record(launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA, info);
@@ -777,6 +790,14 @@ gemm_status_t gemm_last_launch(gemm_launch_info_t *info) {
     if (info == nullptr) return GEMM_ERR_INVALID_ARG;
     *info = t_last_launch;
     return GEMM_OK;
+}
+
+gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const void *A, int64_t a_stride_m,
+                   int64_t a_stride_k, const void *B, int64_t b_stride_k, int64_t b_stride_n, void *C, int64_t ldc,
+                   gemm_dtype_t c_dtype, float alpha, float beta, const float *bias, gemm_epilogue_t epilogue,
+                   void *workspace, size_t workspace_bytes, gemm_stream_t stream) {
+    return gemm_ex(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc, c_dtype, alpha,
+                   beta, bias, epilogue, nullptr, workspace, workspace_bytes, stream);
 }
 
 gemm_status_t gemm_set_operand_order(gemm_operand_order_t order) {

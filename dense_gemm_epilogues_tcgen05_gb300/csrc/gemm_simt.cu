@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtArgs 
             const int col = n0 + tx + 16 * j;
             if (col < N) {
                 const float b = (a.e.epilogue != kEpiNone) ? a.e.bias[col] : 0.0f;
-                epilogue_store_one<OUT>(acc[i][j], C + (long long)row * a.e.ldc + col, b, a.e);
+                epilogue_store_one<OUT>(acc[i][j] * product_scale(a.e, row, col), C + (long long)row * a.e.ldc + col,
+                                        b, a.e);
             }
         }
     }

@@ -200,7 +200,7 @@ __device__ __forceinline__ void store_partial_chunks(uint32_t t_base, int c0, in
 // the accumulators before alpha / beta / bias / GELU / cast.
 // With e.c_tma the chunks go through the warp's staged C box (rows row0 ..
 // row0+31, row0 < M) instead.  Returns false if a wait for C gave up.
-template <int OUT>
+template <int OUT, bool SC>
 __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, int c0, int nvalid, int row,
                                                  bool row_ok, int r, const float *slot0, long long slot_stride,
                                                  int ncontrib, const float *bias_base, const EpiParams &e,
@@ -229,9 +229,10 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
             }
         }
         const int col0 = col_base + i * 32;
+        if (!e.c_tma) product_scale_chunk<SC>(v, e, row, col0, false);  // the TMA path scales in epilogue_chunk32_tma
         if (e.c_tma) {
             if (ok && row0 < (e.swap ? e.N : e.M))
-                ok = epilogue_chunk32_tma<OUT>(v, col0, row0, bias_base + i * 32, bias_lane, e, tmC, cbuf, cbar,
+                ok = epilogue_chunk32_tma<OUT, SC>(v, col0, row0, bias_base + i * 32, bias_lane, e, tmC, cbuf, cbar,
                                                cphase, abort_flag, status);
         } else if (row_ok) {
             if (e.c_vec && col0 + 32 <= e.N)
@@ -245,7 +246,8 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
 }
 
 // CL: CTAs per cluster, 2 (one pair) or 4 (two pairs sharing A by multicast).
-template <int AB, int OUT, int STAGES, int BNH, int CL>
+// SC: built for calls with product scales (gemm_ex); without, that code is left out.
+template <int AB, int OUT, int STAGES, int BNH, int CL, bool SC>
 __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcArgs args) {
@@ -502,13 +504,13 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             bool fail = false;
             if (seg.kind == kSegFull) {
                 if (!e.c_tma)
-                    epilogue_row_chunks<OUT, 4>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, bias_s, e);
+                    epilogue_row_chunks<OUT, 4, SC>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, bias_s, e);
                 else if (row0 < lane_extent && last)
-                    fail = !epilogue_rows_tma_burst<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s,
+                    fail = !epilogue_rows_tma_burst<OUT, SC>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s,
                                                          bias_lane, e, &tmC, smem + ew * Cfg::BURST_BYTES_PER_WARP,
                                                          &cbar[ew], cphase, abort_flag, args.status);
                 else if (row0 < lane_extent)
-                    fail = !epilogue_rows_tma<OUT>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, bias_lane, e,
+                    fail = !epilogue_rows_tma<OUT, SC>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, bias_lane, e,
                                                    &tmC, cbuf, &cbar[ew], cphase, abort_flag, args.status);
             } else if (seg.kind == kSegPart) {
                 float *slot = args.partial + (static_cast<long long>(cluster) * CL + rank) * kPartialFloatsPerCta;
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                 }
                 const float *slot0 =
                     args.partial + (static_cast<long long>(cluster + 1) * CL + rank) * kPartialFloatsPerCta;
-                fail = !owner_row_chunks<OUT>(t_row + c_begin * 32, col_base, c_begin, nvalid, row, row_ok, r, slot0,
+                fail = !owner_row_chunks<OUT, SC>(t_row + c_begin * 32, col_base, c_begin, nvalid, row, row_ok, r, slot0,
                                               CL * kPartialFloatsPerCta, ncontrib, bias_s, e, row0, &tmC, cbuf,
                                               &cbar[ew], cphase, abort_flag, args.status, bias_lane);
                 __syncwarp();
@@ -572,7 +574,8 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     if (args.stage_tx > static_cast<uint32_t>(Cfg::STAGE_BYTES)) return cudaErrorInvalidValue;
     // Two pairs split each CTA's A rows between them: whole boxes only.
     if (CL == 4 && args.a_mn_major && (Cfg::BM / Cfg::SWZ) % 2 != 0) return cudaErrorInvalidValue;
-    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL>;
+    auto kern = args.e.scaled ? gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, true>
+                              : gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -598,7 +601,7 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
 template <int AB, int OUT, int STAGES, int BNH = 128, int CL = 2>
 int pair_max_clusters() {
     using Cfg = PairConfig<AB, STAGES, BNH>;
-    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL>;
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, false>;  // the scaled build has the same footprint
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};

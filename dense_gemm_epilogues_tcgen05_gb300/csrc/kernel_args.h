@@ -28,6 +28,10 @@ struct EpiParams {
     int c_vec;        // C base and row pitch allow 16-byte vector access
     int c_tma;        // pair kernel: C moves through shared memory by TMA (the kernel's C map is valid)
     int swap;         // pair kernel: the MMA computes C^T = B^T A^T (TMEM lanes are output columns)
+    // Product scales (gemm_ex), device pointers, each NULL when absent: the product
+    // term is alpha * alpha_scale[0] * row_scale[i] * col_scale[j] * acc.
+    int scaled;       // any of the three is present
+    const float *alpha_scale, *row_scale, *col_scale;
 };
 
 // Most clusters a stream-K schedule spreads over (the cut table's size).

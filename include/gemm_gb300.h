@@ -134,6 +134,41 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K,
                    gemm_stream_t stream);
 
 /*
+ * Product scales of gemm_ex, each a DEVICE pointer read when the kernel runs
+ * (so a scale computed by an earlier kernel needs no host round trip), each
+ * optional (NULL = 1):
+ *   alpha_scale  fp32[1]  per-tensor, e.g. s_a * s_b of fp8 operands;
+ *   row_scale    fp32[M]  per row of A / C (per token);
+ *   col_scale    fp32[N]  per column of B / C (per output channel).
+ * The product term becomes alpha * alpha_scale[0] * row_scale[i] *
+ * col_scale[j] * sum_k A[i][k] B[k][j]; beta*C and the bias are not scaled.
+ * ("Case Study: Steel's BlockMMA": the epilogue is a functor applied to every
+ * accumulator before the store; these are its per-row / per-column forms.)
+ */
+typedef struct {
+    const float *alpha_scale;
+    const float *row_scale;
+    const float *col_scale;
+} gemm_scales_t;
+
+/*
+ * gemm_ex -- gemm() with product scales (scales may be NULL: then exactly
+ * gemm()).  Same arguments, conventions and errors; the scale arrays are
+ * checked against their device allocations like every other buffer.  With
+ * K == 0 or alpha == 0 the scales are not read.
+ */
+gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K,
+                      gemm_dtype_t ab_dtype,
+                      const void *A, int64_t a_stride_m, int64_t a_stride_k,
+                      const void *B, int64_t b_stride_k, int64_t b_stride_n,
+                      void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                      float alpha, float beta,
+                      const float *bias, gemm_epilogue_t epilogue,
+                      const gemm_scales_t *scales,
+                      void *workspace, size_t workspace_bytes,
+                      gemm_stream_t stream);
+
+/*
  * gemm_workspace_size -- bytes of device scratch that let gemm() use its
  * fastest path.  fp16 / bf16 / fp8 inputs: the stream-K schedule on the
  * current device, 256 KB of partial sums and 64 bytes of flags per pair of SMs

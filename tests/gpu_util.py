@@ -73,7 +73,13 @@ def run_gemm(g, p, *, nan_c=False, stream=None, a_elem_offset=0, b_elem_offset=0
     path = g.gemm_query_path(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr,
                              p.b_stride_k, p.b_stride_n, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta,
                              bias, p.epilogue)
-    if baseline is not None:
+    if p.product_scales:
+        sc = {k: v.to(device) for k, v in p.product_scales.items()}
+        ws = workspace(g, device, g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype)) if use_workspace else None
+        g.gemm_ex(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr, p.b_stride_k, p.b_stride_n,
+                  c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue, workspace=ws,
+                  workspace_bytes=0 if ws is None else ws.numel(), stream=stream, **sc)
+    elif baseline is not None:
         g.gemm_baseline(baseline, p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr,
                         p.b_stride_k, p.b_stride_n, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue,
                         stream=stream)
