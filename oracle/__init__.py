@@ -309,3 +309,51 @@ def check(problem_args: dict, C_out: np.ndarray, rows: Optional[Sequence[int]] =
     err = max_normalized_error(out, y, D, p["epilogue"])
     tol = tolerance(p["ab_dtype"], p["c_dtype"])
     return {"err": err, "tol": tol, "pass": bool(err <= tol)}
+
+
+# ---------------------------------------------------------------------------
+# fp8 E4M3 outputs and the amax reduction (gemm_ex).
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+FP8_OUT_REL = 2.0 ** -4   # half a unit in the last place of a 3-bit fraction, relative to |value|
+FP8_OUT_ABS = 2.0 ** -10  # half the subnormal step 2^-9
+
+
+def fp8_output_error(out_values: np.ndarray, ref: np.ndarray, D: np.ndarray, out_scale: float,
+                     epilogue: int) -> np.ndarray:
+    """Per-element error of an E4M3 output that encodes y / out_scale (saturating at 448).
+
+    The output must be y/s rounded to a representable E4M3 value: saturate the
+    reference to +-448 s, allow the rounding of a 3-bit fraction (2^-4 of the
+    value, or 2^-10 s among subnormals), and measure what is left over in units
+    of the accumulation's error scale D (times max|act'|), as for other outputs."""
+    s = fp32_value(out_scale)
+    yc = np.clip(ref, -E4M3_MAX * s, E4M3_MAX * s)
+    got = np.asarray(out_values, dtype=np.float64) * s
+    excess = np.maximum(np.abs(got - yc) - (FP8_OUT_REL * np.abs(yc) + FP8_OUT_ABS * s), 0.0)
+    scale = D * lipschitz(epilogue)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(scale > 0, excess / np.where(scale > 0, scale, 1.0), np.where(excess == 0, 0.0, np.inf))
+    return np.where(np.isnan(got), np.inf, r)
+
+
+def check_fp8_output(problem_args: dict, C_out: np.ndarray, out_scale: float,
+                     rows: Optional[Sequence[int]] = None) -> dict:
+    """An E4M3 output buffer against the reference: the rounding allowance of
+    fp8_output_error, then the 16-bit-output tolerance on what remains."""
+    p = problem_args
+    y, D = gemm_reference(rows=rows, **p)
+    out = output_values(C_out, p["M"], p["N"], p["ldc"], E4M3, rows)
+    r = fp8_output_error(out, y, D, out_scale, p["epilogue"])
+    err = float(r.max()) if r.size else 0.0
+    return {"err": err, "tol": TOL_16BIT_OUT, "pass": bool(err <= TOL_16BIT_OUT)}
+
+
+def amax_reference(problem_args: dict):
+    """max over all outputs of |y| (the activated value before any output scaling
+    or cast) and the error scale D's largest value, which bounds how far an
+    fp32-accumulated maximum may differ (its allowance is TOL_F32_OUT * that)."""
+    y, D = gemm_reference(**problem_args)
+    if y.size == 0:
+        return 0.0, 0.0
+    return float(np.abs(y).max()), float((D * lipschitz(problem_args["epilogue"])).max())

@@ -15,6 +15,7 @@ import math
 from fractions import Fraction
 
 import numpy as np
+import torch
 import pytest
 
 import oracle
@@ -419,3 +420,55 @@ def test_product_scale_mistakes_are_flagged(mistake):
     assert oracle.max_normalized_error(out, y, D, wl.EPI_NONE) > oracle.TOL_F32_OUT
     good = s * np.outer(rs, cs) * prod + Cv
     assert oracle.max_normalized_error(good.astype(np.float32), y, D, wl.EPI_NONE) <= oracle.TOL_F32_OUT
+
+
+# ---------------------------------------------------------- fp8 outputs, amax --
+
+def _e4m3_codes(values):
+    """RNE-saturating E4M3 codes of float values, by torch's CPU cast (a library routine)."""
+    t = torch.tensor(np.asarray(values, dtype=np.float32)).clamp(-448, 448).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def test_fp8_output_check_accepts_correct_rounding_and_saturation():
+    p = wl.random_problem(31, 40, 24, 64, wl.F16, wl.F32, alpha=3.0)
+    a = p.oracle_args()
+    y, D = oracle.gemm_reference(**a)
+    for s in (1.0, 0.05, 2.0 ** -6):                                  # 2^-6: most outputs saturate at 448
+        codes = _e4m3_codes(y / s).reshape(40, 24)
+        C = np.zeros((40, 24), np.uint8); C[:] = codes
+        ax = dict(a, c_dtype=wl.E4M3, C=C.reshape(-1))
+        assert oracle.check_fp8_output(ax, C.reshape(-1), s)["pass"], s
+
+
+@pytest.mark.parametrize("mistake", ["one_ulp_up", "no_scale", "half_scale", "no_saturation_sign"])
+def test_fp8_output_check_flags_mistakes(mistake):
+    p = wl.random_problem(32, 40, 24, 64, wl.F16, wl.F32, alpha=3.0)
+    a = p.oracle_args()
+    y, D = oracle.gemm_reference(**a)
+    s = 0.05
+    q = y / s
+    if mistake == "one_ulp_up":
+        codes = _e4m3_codes(q).astype(np.int64)
+        codes = np.where((codes & 0x7F) < 0x7E, codes + 1, codes).astype(np.uint8)   # next code away from zero
+    elif mistake == "no_scale":
+        codes = _e4m3_codes(y)
+    elif mistake == "half_scale":
+        codes = _e4m3_codes(q / 2)
+    else:
+        codes = _e4m3_codes(np.abs(q))
+    C = codes.reshape(-1)
+    ax = dict(a, c_dtype=wl.E4M3, C=C)
+    assert not oracle.check_fp8_output(ax, C, s)["pass"]
+
+
+def test_amax_reference():
+    p = wl.random_problem(33, 7, 9, 16, wl.BF16, wl.F32, alpha=1.0, integer=True, epilogue=wl.EPI_BIAS_RELU)
+    a = p.oracle_args()
+    y, D = oracle.gemm_reference(**a)
+    amax, dmax = oracle.amax_reference(a)
+    assert amax == float(np.abs(y).max()) and amax >= 0 and dmax == float(D.max())
+    # closed form: all-ones operands, K = 16, alpha = 1: every z = 16 + bias_j
+    ones = wl.make_problem("ones", 3, 4, 16, wl.F16, wl.F32, torch.ones(3, 16), torch.ones(16, 4), alpha=1.0,
+                           bias=torch.tensor([1.0, -40.0, 2.0, 0.0]), epilogue=wl.EPI_BIAS)
+    assert oracle.amax_reference(ones.oracle_args())[0] == 24.0
