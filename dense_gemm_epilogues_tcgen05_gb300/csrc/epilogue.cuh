@@ -43,6 +43,12 @@ template <> struct Elem<kDtBF16> {
 template <> struct Elem<kDtE4M3> {
     using T = __nv_fp8_e4m3;
     static __device__ __forceinline__ float load(const T *p) { return static_cast<float>(*p); }
+    // Round to nearest even, saturating to +-448 (OCP E4M3 "fn" has no infinity).
+    static __device__ __forceinline__ T cvt(float x) {
+        T r;
+        r.__x = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+        return r;
+    }
 };
 
 // GELU, erf form: 0.5*z*(1 + erf(z/sqrt(2))), with erf from the rational
@@ -222,15 +228,31 @@ __device__ __forceinline__ void product_scale_chunk(float (&v)[32], const EpiPar
     }
 }
 
+// Raise *amax to the largest `local` (>= 0) of the calling threads: one atomic
+// per group of converged lanes (non-negative floats order like their bits).
+__device__ __forceinline__ void amax_push(float local, float *amax) {
+    const unsigned mask = __activemask();
+    const unsigned v = __reduce_max_sync(mask, __float_as_uint(local));
+    if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(mask) - 1))
+        atomicMax(reinterpret_cast<unsigned int *>(amax), v);
+}
+
 // Scalar epilogue of one element (used by the safe path and the SIMT kernel).
+// Returns the activated value before any output scaling (for amax).
 template <int OUT>
-__device__ __forceinline__ void epilogue_store_one(float acc, typename Elem<OUT>::T *c, float bias_j,
-                                                   const EpiParams &e) {
+__device__ __forceinline__ float epilogue_store_one(float acc, typename Elem<OUT>::T *c, float bias_j,
+                                                    const EpiParams &e) {
     float z = e.alpha * acc;
-    if (e.beta != 0.0f) z = fmaf(e.beta, Elem<OUT>::load(c), z);
+    if constexpr (OUT != kDtE4M3) {
+        if (e.beta != 0.0f) z = fmaf(e.beta, Elem<OUT>::load(c), z);  // E4M3 outputs are written only
+    }
     if (e.epilogue != kEpiNone) z += bias_j;
     z = activate(z, e.epilogue);
-    *c = Elem<OUT>::cvt(z);
+    if constexpr (OUT == kDtE4M3)
+        *c = Elem<OUT>::cvt(e.out_scale ? z / *e.out_scale : z);
+    else
+        *c = Elem<OUT>::cvt(z);
+    return z;
 }
 
 // --- 16-byte packing helpers for the fast path -----------------------------
@@ -290,9 +312,34 @@ template <> struct Vec16<kDtBF16> {
     }
 };
 
+template <> struct Vec16<kDtE4M3> {
+    static constexpr int kPerVec = 16;
+    static __device__ __forceinline__ void unpack(const uint4 &u, float *f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const __nv_fp8x2_storage_t two = static_cast<__nv_fp8x2_storage_t>(w[i / 2] >> (16 * (i % 2)));
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+            f[2 * i] = t.x; f[2 * i + 1] = t.y;
+        }
+    }
+    static __device__ __forceinline__ uint4 pack(const float *f) {
+        uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t two = __nv_cvt_float2_to_fp8x2(make_float2(f[2 * i], f[2 * i + 1]), __NV_SATFINITE,
+                                                          __NV_E4M3);
+            w[i / 2] |= (two & 0xFFFFu) << (16 * (i % 2));
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
 // Fast path: 32 in-range columns of one row, C and bias 16-byte aligned.
-// `bias_chunk` may point to global or shared memory (generic loads).
-template <int OUT>
+// `bias_chunk` may point to global or shared memory (generic loads).  With SC,
+// also the amax reduction and (E4M3 output) the output scale.
+template <int OUT, bool SC = true>
 __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename Elem<OUT>::T *crow,
                                                       const float *bias_chunk, const EpiParams &e) {
     constexpr int PV = Vec16<OUT>::kPerVec;
@@ -325,21 +372,40 @@ __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename E
             for (int j = 0; j < 32; j += 2) activate2(v[j], v[j + 1], e.epilogue);
         }
     }
+    if constexpr (SC) {
+        if (e.amax) {
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(v[j]));
+            amax_push(m, e.amax);
+        }
+    }
+    if constexpr (OUT == kDtE4M3) {
+        if (e.out_scale) {
+            const float inv = 1.0f / *e.out_scale;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= inv;
+        }
+    }
     uint4 *dst = reinterpret_cast<uint4 *>(crow);
 #pragma unroll
     for (int q = 0; q < NV; ++q) dst[q] = Vec16<OUT>::pack(&v[q * PV]);
 }
 
 // Safe path: columns col0 .. col0+31, of which only those < N are touched.
-template <int OUT>
+template <int OUT, bool SC = true>
 __device__ __forceinline__ void epilogue_chunk32_safe(const float (&v)[32], typename Elem<OUT>::T *crow, int col0,
                                                       const EpiParams &e) {
+    float m = 0.0f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         if (col0 + j < e.N) {
             const float b = (e.epilogue != kEpiNone) ? e.bias[col0 + j] : 0.0f;
-            epilogue_store_one<OUT>(v[j], crow + j, b, e);
+            m = fmaxf(m, fabsf(epilogue_store_one<OUT>(v[j], crow + j, b, e)));
         }
+    }
+    if constexpr (SC) {
+        if (e.amax) amax_push(m, e.amax);
     }
 }
 
@@ -373,9 +439,9 @@ __device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_bas
         product_scale_chunk<SC>(v, e, row, col0, false);
         if (row_ok) {
             if (e.c_vec && col0 + 32 <= e.N)
-                epilogue_chunk32_fast<OUT>(v, crow + col0, bias_base + i * 32, e);
+                epilogue_chunk32_fast<OUT, SC>(v, crow + col0, bias_base + i * 32, e);
             else
-                epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
+                epilogue_chunk32_safe<OUT, SC>(v, crow + col0, col0, e);
         }
         __syncwarp();  // reconverge after the per-row store before the collective wait
         if (more) tmem_ld_wait(nxt);

@@ -143,11 +143,11 @@ struct Plan {
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int ab, const void *A, int64_t sam, int64_t sak,
                         const void *B, int64_t sbk, int64_t sbn, const void *C, int64_t ldc, int cd, float alpha,
-                        const float *bias, int epi, Plan *plan) {
+                        const float *bias, int epi, Plan *plan, bool fp8_out = false) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (!valid_dtype(ab) || !valid_dtype(cd)) return GEMM_ERR_INVALID_ARG;
     if (epi < GEMM_EPI_NONE || epi > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
-    if (cd == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+    if (cd == GEMM_E4M3 && !fp8_out) return GEMM_ERR_UNSUPPORTED;
     if (ab == GEMM_F32 && cd != GEMM_F32) return GEMM_ERR_UNSUPPORTED;
     if (ab == GEMM_E4M3 && cd == GEMM_F16) return GEMM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) {
@@ -507,7 +507,7 @@ cudaError_t launch_tc(int ab, int cd, int bn, const CUtensorMap &ta, const CUten
 
 EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alpha, float beta, const float *bias,
                    int epi) {
-    EpiParams e;
+    EpiParams e = {};  // every field defined, including those later calls fill in
     e.M = static_cast<int>(M);
     e.N = static_cast<int>(N);
     e.C = C;
@@ -521,8 +521,10 @@ EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alp
     e.c_vec = (c_al && b_al) ? 1 : 0;
     e.c_tma = 0;  // set by the pair-kernel launch once C's tensor map is encoded
     e.swap = 0;   // set by the pair-kernel launch when it computes C^T = B^T A^T
-    e.scaled = 0;  // product scales: set by gemm_ex
+    e.scaled = 0;  // scales, fp8 output scale and amax: set by gemm_ex
     e.alpha_scale = e.row_scale = e.col_scale = nullptr;
+    e.out_scale = nullptr;
+    e.amax = nullptr;
     return e;
 }
 
@@ -530,7 +532,7 @@ EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alp
 // on the stacked hi/lo arrays (whole tiles, 256 x 256).
 gemm_status_t gemm_tf32x3(int64_t M, int64_t N, int64_t K, const void *A, int64_t sam, int64_t sak, const void *B,
                           int64_t sbk, int64_t sbn, const EpiParams &e, void *workspace, int max_clusters,
-                          DeviceState *dev, cudaStream_t s, gemm_launch_info_t *info) {
+                          DeviceState *dev, cudaStream_t s, gemm_launch_info_t *info, bool direct_c) {
     const int64_t pitch = tf32x3_pitch(K);
     float *a2 = static_cast<float *>(workspace);
     float *b2 = reinterpret_cast<float *>(static_cast<char *>(workspace) +
@@ -546,7 +548,7 @@ gemm_status_t gemm_tf32x3(int64_t M, int64_t N, int64_t K, const void *A, int64_
         return st;
     if ((st = encode_2d_dt(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, b2, K, 2 * N, pitch, 32, bn / 2)) != GEMM_OK)
         return st;
-    TcArgs t;
+    TcArgs t = {};
     t.e = e;
     t.K = static_cast<int>(K);
     t.tiles_m = static_cast<int>((M + 255) / 256);
@@ -569,7 +571,7 @@ gemm_status_t gemm_tf32x3(int64_t M, int64_t N, int64_t K, const void *A, int64_
     t.lo_row_b = static_cast<int>(N);
     CUtensorMap tc;
     std::memset(&tc, 0, sizeof(tc));
-    t.e.c_tma = encode_c(&tc, GEMM_F32, e.C, M, N, e.ldc) ? 1 : 0;
+    t.e.c_tma = (!direct_c && encode_c(&tc, GEMM_F32, e.C, M, N, e.ldc)) ? 1 : 0;
     const int clusters = t.num_tiles < max_clusters ? t.num_tiles : max_clusters;
     info->path = GEMM_PATH_TCGEN05;
     info->kind = 2;
@@ -619,9 +621,11 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
                       int64_t a_stride_k, const void *B, int64_t b_stride_k, int64_t b_stride_n, void *C, int64_t ldc,
                       gemm_dtype_t c_dtype, float alpha, float beta, const float *bias, gemm_epilogue_t epilogue,
                       const gemm_scales_t *scales, void *workspace, size_t workspace_bytes, gemm_stream_t stream) {
+    // E4M3 outputs: through gemm_ex only, written (beta == 0), from 16-bit or fp8 inputs.
+    if (c_dtype == GEMM_E4M3 && (beta != 0.0f || ab_dtype == GEMM_F32)) return GEMM_ERR_UNSUPPORTED;
     Plan plan;
     gemm_status_t st = make_plan(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc,
-                                 c_dtype, alpha, bias, epilogue, &plan);
+                                 c_dtype, alpha, bias, epilogue, &plan, /*fp8_out=*/true);
     gemm_launch_info_t info = {};
     info.path = plan.path;
     if (st != GEMM_OK || plan.path == GEMM_PATH_NOOP) return record(st, info);
@@ -643,8 +647,16 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
         e.alpha_scale = scales->alpha_scale;
         e.row_scale = scales->row_scale;
         e.col_scale = scales->col_scale;
-        e.scaled = (e.alpha_scale || e.row_scale || e.col_scale) ? 1 : 0;
     }
+    if (scales != nullptr) {
+        if (scales->out_scale && (st = check_range(scales->out_scale, 4)) != GEMM_OK) return st;
+        if (scales->amax && (st = check_range(scales->amax, 4)) != GEMM_OK) return st;
+        e.out_scale = c_dtype == GEMM_E4M3 ? scales->out_scale : nullptr;
+        e.amax = scales->amax;
+    }
+    e.scaled = (e.alpha_scale || e.row_scale || e.col_scale || e.out_scale || e.amax || c_dtype == GEMM_E4M3) ? 1 : 0;
+    // E4M3 outputs and the amax reduction use the direct stores (no staged C).
+    const bool direct_c = c_dtype == GEMM_E4M3 || e.amax != nullptr;
 
     if (plan.path == GEMM_PATH_EPILOGUE_ONLY)
         return record(launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA, info);
@@ -661,12 +673,12 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
             workspace_bytes >= need && max_clusters > 0) {
             if ((st = check_range(workspace, need)) != GEMM_OK) return st;
             return record(gemm_tf32x3(M, N, K, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, e, workspace,
-                                      max_clusters, dev, s, &info),
+                                      max_clusters, dev, s, &info, direct_c),
                           info);
         }
     }
     if (plan.path == GEMM_PATH_SIMT) {
-        SimtArgs a;
+        SimtArgs a = {};
         a.e = e;
         a.K = static_cast<int>(K);
         a.A = A; a.sam = a_stride_m; a.sak = a_stride_k;
@@ -680,7 +692,7 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
     const int max_clusters = device_max_clusters(dev, ab_dtype, c_dtype);
     CUtensorMap tcm;
     std::memset(&tcm, 0, sizeof(tcm));
-    const bool c_tma = encode_c(&tcm, c_dtype, C, M, N, ldc);
+    const bool c_tma = !direct_c && encode_c(&tcm, c_dtype, C, M, N, ldc);
     const int order = g_operand_order.load();
     bool swap = c_tma && c_dtype != GEMM_F32 && order != GEMM_ORDER_AS_GIVEN &&
                 (order == GEMM_ORDER_TRANSPOSED ||
@@ -690,7 +702,11 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
         tc = choose_tile(N, M, dev->num_sms, max_clusters, g_tile_policy.load(), g_tile_policy_bn.load());
         if (tc.kind != 2) swap = false;  // the one-SM kernel runs the problem as given
     }
-    if (!swap) tc = choose_tile(M, N, dev->num_sms, max_clusters, g_tile_policy.load(), g_tile_policy_bn.load());
+    if (!swap) {
+        // E4M3 outputs are built for the pair kernel only.
+        const int policy = c_dtype == GEMM_E4M3 ? GEMM_TILE_PAIR : g_tile_policy.load();
+        tc = choose_tile(M, N, dev->num_sms, max_clusters, policy, g_tile_policy_bn.load());
+    }
     // The kernel's problem: Mk x Nk, first operand (Mk x K), second (Nk x K).
     const int64_t Mk = swap ? N : M, Nk = swap ? M : N;
     const Operand &op1 = swap ? plan.b : plan.a, &op2 = swap ? plan.a : plan.b;
@@ -722,7 +738,7 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
         if ((st = encode_operand(&tb, ab_dtype, B, plan.b, N, K, b_stride_n, b_stride_k, b_box)) != GEMM_OK)
             return st;
     }
-    TcArgs t;
+    TcArgs t = {};
     t.e = e;
     t.K = static_cast<int>(K);
     t.tiles_m = static_cast<int>(tiles_m);
@@ -796,6 +812,7 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
                    int64_t a_stride_k, const void *B, int64_t b_stride_k, int64_t b_stride_n, void *C, int64_t ldc,
                    gemm_dtype_t c_dtype, float alpha, float beta, const float *bias, gemm_epilogue_t epilogue,
                    void *workspace, size_t workspace_bytes, gemm_stream_t stream) {
+    if (c_dtype == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;  // fp8 outputs: gemm_ex (with their scale and amax)
     return gemm_ex(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc, c_dtype, alpha,
                    beta, bias, epilogue, nullptr, workspace, workspace_bytes, stream);
 }
@@ -881,7 +898,7 @@ gemm_status_t gemm_baseline(gemm_baseline_t kind, int64_t M, int64_t N, int64_t 
         return launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     if ((st = check_range(A, span_bytes(M, K, a_stride_m, a_stride_k, es))) != GEMM_OK) return st;
     if ((st = check_range(B, span_bytes(K, N, b_stride_k, b_stride_n, es))) != GEMM_OK) return st;
-    SimtArgs a;
+    SimtArgs a = {};
     a.e = e;
     a.K = static_cast<int>(K);
     a.A = A; a.sam = a_stride_m; a.sak = a_stride_k;
@@ -924,7 +941,7 @@ gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, con
     if ((st = check_range(Wq, static_cast<size_t>(N) * static_cast<size_t>(K / 8) * 4)) != GEMM_OK) return st;
     if ((st = check_range(scale_bias, static_cast<size_t>(N) * static_cast<size_t>(K / 64) * 4)) != GEMM_OK)
         return st;
-    Q4Args a;
+    Q4Args a = {};
     a.e = e;
     a.K = static_cast<int>(K);
     a.X = X;

@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtArgs 
     }
 
     OutT *C = static_cast<OutT *>(a.e.C);
+    float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = m0 + ty + 16 * i;
@@ -87,11 +88,13 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtArgs 
             const int col = n0 + tx + 16 * j;
             if (col < N) {
                 const float b = (a.e.epilogue != kEpiNone) ? a.e.bias[col] : 0.0f;
-                epilogue_store_one<OUT>(acc[i][j] * product_scale(a.e, row, col), C + (long long)row * a.e.ldc + col,
-                                        b, a.e);
+                const float y = epilogue_store_one<OUT>(acc[i][j] * product_scale(a.e, row, col),
+                                                        C + (long long)row * a.e.ldc + col, b, a.e);
+                amax = fmaxf(amax, fabsf(y));
             }
         }
     }
+    if (a.e.amax) amax_push(amax, a.e.amax);
 }
 
 template <int OUT>
@@ -99,12 +102,14 @@ __global__ void epilogue_only_kernel(const EpiParams e) {
     using OutT = typename Elem<OUT>::T;
     OutT *C = static_cast<OutT *>(e.C);
     const long long total = (long long)e.M * e.N;
+    float amax = 0.0f;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         const long long i = idx / e.N, j = idx - i * e.N;
         const float b = (e.epilogue != kEpiNone) ? e.bias[j] : 0.0f;
-        epilogue_store_one<OUT>(0.0f, C + i * e.ldc + j, b, e);
+        amax = fmaxf(amax, fabsf(epilogue_store_one<OUT>(0.0f, C + i * e.ldc + j, b, e)));
     }
+    if (e.amax) amax_push(amax, e.amax);
 }
 
 template <int OUT>
@@ -170,6 +175,9 @@ cudaError_t launch_simt(int ab, int out, const SimtArgs &a, cudaStream_t s) {
     case kDtBF16 * 4 + kDtF16: return launch_simt_t<kDtBF16, kDtF16>(a, s);
     case kDtE4M3 * 4 + kDtBF16: return launch_simt_t<kDtE4M3, kDtBF16>(a, s);
     case kDtE4M3 * 4 + kDtF32: return launch_simt_t<kDtE4M3, kDtF32>(a, s);
+    case kDtF16 * 4 + kDtE4M3: return launch_simt_t<kDtF16, kDtE4M3>(a, s);
+    case kDtBF16 * 4 + kDtE4M3: return launch_simt_t<kDtBF16, kDtE4M3>(a, s);
+    case kDtE4M3 * 4 + kDtE4M3: return launch_simt_t<kDtE4M3, kDtE4M3>(a, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -181,6 +189,7 @@ cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t s) {
     case kDtF32: epilogue_only_kernel<kDtF32><<<grid, threads, 0, s>>>(e); break;
     case kDtF16: epilogue_only_kernel<kDtF16><<<grid, threads, 0, s>>>(e); break;
     case kDtBF16: epilogue_only_kernel<kDtBF16><<<grid, threads, 0, s>>>(e); break;
+    case kDtE4M3: epilogue_only_kernel<kDtE4M3><<<grid, threads, 0, s>>>(e); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

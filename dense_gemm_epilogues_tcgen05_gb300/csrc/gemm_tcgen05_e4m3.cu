@@ -21,10 +21,12 @@ cudaError_t launch_pair_e4m3(int out, int cl, const CUtensorMap &ta, const CUten
     if (cl == 4) {
         if (out == kDtBF16) return launch_pair_cfg<kDtE4M3, kDtBF16, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
         if (out == kDtF32) return launch_pair_cfg<kDtE4M3, kDtF32, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
+        if (out == kDtE4M3) return launch_pair_cfg<kDtE4M3, kDtE4M3, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
         return cudaErrorInvalidValue;
     }
     if (out == kDtBF16) return launch_pair_cfg<kDtE4M3, kDtBF16, 6>(ta, tb, tc, args, clusters, stream);
     if (out == kDtF32) return launch_pair_cfg<kDtE4M3, kDtF32, 6>(ta, tb, tc, args, clusters, stream);
+    if (out == kDtE4M3) return launch_pair_cfg<kDtE4M3, kDtE4M3, 6>(ta, tb, tc, args, clusters, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -32,10 +34,12 @@ int pair_max_clusters_e4m3(int out, int cl) {
     if (cl == 4) {
         if (out == kDtBF16) return pair_max_clusters<kDtE4M3, kDtBF16, 6, 128, 4>();
         if (out == kDtF32) return pair_max_clusters<kDtE4M3, kDtF32, 6, 128, 4>();
+        if (out == kDtE4M3) return pair_max_clusters<kDtE4M3, kDtE4M3, 6, 128, 4>();
         return 0;
     }
     if (out == kDtBF16) return pair_max_clusters<kDtE4M3, kDtBF16, 6>();
     if (out == kDtF32) return pair_max_clusters<kDtE4M3, kDtF32, 6>();
+    if (out == kDtE4M3) return pair_max_clusters<kDtE4M3, kDtE4M3, 6>();
     return 0;
 }
 

@@ -24,11 +24,13 @@ cudaError_t launch_pair_f16(int out, int cl, const CUtensorMap &ta, const CUtens
         if (out == kDtF16) return launch_pair_cfg<kDtF16, kDtF16, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
         if (out == kDtF32) return launch_pair_cfg<kDtF16, kDtF32, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
         if (out == kDtBF16) return launch_pair_cfg<kDtF16, kDtBF16, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
+        if (out == kDtE4M3) return launch_pair_cfg<kDtF16, kDtE4M3, 6, 128, 4>(ta, tb, tc, args, clusters, stream);
         return cudaErrorInvalidValue;
     }
     if (out == kDtF16) return launch_pair_cfg<kDtF16, kDtF16, 6>(ta, tb, tc, args, clusters, stream);
     if (out == kDtF32) return launch_pair_cfg<kDtF16, kDtF32, 6>(ta, tb, tc, args, clusters, stream);
     if (out == kDtBF16) return launch_pair_cfg<kDtF16, kDtBF16, 6>(ta, tb, tc, args, clusters, stream);
+    if (out == kDtE4M3) return launch_pair_cfg<kDtF16, kDtE4M3, 6>(ta, tb, tc, args, clusters, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -37,11 +39,13 @@ int pair_max_clusters_f16(int out, int cl) {
         if (out == kDtF16) return pair_max_clusters<kDtF16, kDtF16, 6, 128, 4>();
         if (out == kDtF32) return pair_max_clusters<kDtF16, kDtF32, 6, 128, 4>();
         if (out == kDtBF16) return pair_max_clusters<kDtF16, kDtBF16, 6, 128, 4>();
+        if (out == kDtE4M3) return pair_max_clusters<kDtF16, kDtE4M3, 6, 128, 4>();
         return 0;
     }
     if (out == kDtF16) return pair_max_clusters<kDtF16, kDtF16, 6>();
     if (out == kDtF32) return pair_max_clusters<kDtF16, kDtF32, 6>();
     if (out == kDtBF16) return pair_max_clusters<kDtF16, kDtBF16, 6>();
+    if (out == kDtE4M3) return pair_max_clusters<kDtF16, kDtE4M3, 6>();
     return 0;
 }
 

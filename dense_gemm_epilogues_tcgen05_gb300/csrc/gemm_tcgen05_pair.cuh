@@ -229,16 +229,20 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
             }
         }
         const int col0 = col_base + i * 32;
-        if (!e.c_tma) product_scale_chunk<SC>(v, e, row, col0, false);  // the TMA path scales in epilogue_chunk32_tma
-        if (e.c_tma) {
-            if (ok && row0 < (e.swap ? e.N : e.M))
-                ok = epilogue_chunk32_tma<OUT, SC>(v, col0, row0, bias_base + i * 32, bias_lane, e, tmC, cbuf, cbar,
-                                               cphase, abort_flag, status);
+        // E4M3 outputs never move through shared memory (the host gives them no C map).
+        const bool staged = OUT != kDtE4M3 && e.c_tma;
+        if (!staged) product_scale_chunk<SC>(v, e, row, col0, false);  // the TMA path scales in epilogue_chunk32_tma
+        if (staged) {
+            if constexpr (OUT != kDtE4M3) {
+                if (ok && row0 < (e.swap ? e.N : e.M))
+                    ok = epilogue_chunk32_tma<OUT, SC>(v, col0, row0, bias_base + i * 32, bias_lane, e, tmC, cbuf,
+                                                       cbar, cphase, abort_flag, status);
+            }
         } else if (row_ok) {
             if (e.c_vec && col0 + 32 <= e.N)
-                epilogue_chunk32_fast<OUT>(v, crow + col0, bias_base + i * 32, e);
+                epilogue_chunk32_fast<OUT, SC>(v, crow + col0, bias_base + i * 32, e);
             else
-                epilogue_chunk32_safe<OUT>(v, crow + col0, col0, e);
+                epilogue_chunk32_safe<OUT, SC>(v, crow + col0, col0, e);
         }
     }
     __syncwarp();
@@ -503,15 +507,20 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             if (left < nvalid) nvalid = left;
             bool fail = false;
             if (seg.kind == kSegFull) {
-                if (!e.c_tma)
+                if (OUT == kDtE4M3 || !e.c_tma) {
                     epilogue_row_chunks<OUT, 4, SC>(t_row + c_begin * 32, col_base, nvalid, row, row_ok, bias_s, e);
-                else if (row0 < lane_extent && last)
-                    fail = !epilogue_rows_tma_burst<OUT, SC>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s,
-                                                         bias_lane, e, &tmC, smem + ew * Cfg::BURST_BYTES_PER_WARP,
-                                                         &cbar[ew], cphase, abort_flag, args.status);
-                else if (row0 < lane_extent)
-                    fail = !epilogue_rows_tma<OUT, SC>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s, bias_lane, e,
-                                                   &tmC, cbuf, &cbar[ew], cphase, abort_flag, args.status);
+                } else {
+                    if constexpr (OUT != kDtE4M3) {
+                        if (row0 < lane_extent && last)
+                            fail = !epilogue_rows_tma_burst<OUT, SC>(
+                                t_row + c_begin * 32, col_base, nvalid, row0, bias_s, bias_lane, e, &tmC,
+                                smem + ew * Cfg::BURST_BYTES_PER_WARP, &cbar[ew], cphase, abort_flag, args.status);
+                        else if (row0 < lane_extent)
+                            fail = !epilogue_rows_tma<OUT, SC>(t_row + c_begin * 32, col_base, nvalid, row0, bias_s,
+                                                               bias_lane, e, &tmC, cbuf, &cbar[ew], cphase, abort_flag,
+                                                               args.status);
+                    }
+                }
             } else if (seg.kind == kSegPart) {
                 float *slot = args.partial + (static_cast<long long>(cluster) * CL + rank) * kPartialFloatsPerCta;
                 store_partial_chunks(t_row + c_begin * 32, c_begin, nvalid, r, slot);
@@ -574,8 +583,11 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     if (args.stage_tx > static_cast<uint32_t>(Cfg::STAGE_BYTES)) return cudaErrorInvalidValue;
     // Two pairs split each CTA's A rows between them: whole boxes only.
     if (CL == 4 && args.a_mn_major && (Cfg::BM / Cfg::SWZ) % 2 != 0) return cudaErrorInvalidValue;
-    auto kern = args.e.scaled ? gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, true>
-                              : gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, false>;
+    // E4M3 outputs always run the build with scales (the host marks them scaled).
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, true>;
+    if constexpr (OUT != kDtE4M3) {
+        if (!args.e.scaled) kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, false>;
+    }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -601,7 +613,8 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
 template <int AB, int OUT, int STAGES, int BNH = 128, int CL = 2>
 int pair_max_clusters() {
     using Cfg = PairConfig<AB, STAGES, BNH>;
-    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, false>;  // the scaled build has the same footprint
+    // Both builds have the same footprint; E4M3 outputs exist only with scales.
+    auto kern = gemm_tcgen05_pair_kernel<AB, OUT, STAGES, BNH, CL, OUT == kDtE4M3>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};

@@ -30,8 +30,10 @@ struct EpiParams {
     int swap;         // pair kernel: the MMA computes C^T = B^T A^T (TMEM lanes are output columns)
     // Product scales (gemm_ex), device pointers, each NULL when absent: the product
     // term is alpha * alpha_scale[0] * row_scale[i] * col_scale[j] * acc.
-    int scaled;       // any of the three is present
+    int scaled;       // any product scale, out_scale or amax is present, or the output is E4M3
     const float *alpha_scale, *row_scale, *col_scale;
+    const float *out_scale;  // E4M3 output: stores y / out_scale[0] (NULL = 1)
+    float *amax;             // atomically raised to max |y| over the outputs (NULL = not kept)
 };
 
 // Most clusters a stream-K schedule spreads over (the cut table's size).

@@ -134,28 +134,38 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K,
                    gemm_stream_t stream);
 
 /*
- * Product scales of gemm_ex, each a DEVICE pointer read when the kernel runs
- * (so a scale computed by an earlier kernel needs no host round trip), each
- * optional (NULL = 1):
- *   alpha_scale  fp32[1]  per-tensor, e.g. s_a * s_b of fp8 operands;
+ * Scales of gemm_ex, each a DEVICE pointer read when the kernel runs (so a
+ * scale computed by an earlier kernel needs no host round trip), each
+ * optional (NULL = absent):
+ *   alpha_scale  fp32[1]  per-tensor product scale, e.g. s_a * s_b of fp8 operands;
  *   row_scale    fp32[M]  per row of A / C (per token);
- *   col_scale    fp32[N]  per column of B / C (per output channel).
+ *   col_scale    fp32[N]  per column of B / C (per output channel);
+ *   out_scale    fp32[1]  E4M3 output only: C stores y / out_scale[0] (NULL = 1),
+ *                         rounded to nearest even and saturated to +-448;
+ *   amax         fp32[1]  raised atomically to max |y| over the M x N outputs,
+ *                         y being the activated value before out_scale and the
+ *                         cast; the caller sets it (e.g. to 0) beforehand.
  * The product term becomes alpha * alpha_scale[0] * row_scale[i] *
  * col_scale[j] * sum_k A[i][k] B[k][j]; beta*C and the bias are not scaled.
  * ("Case Study: Steel's BlockMMA": the epilogue is a functor applied to every
- * accumulator before the store; these are its per-row / per-column forms.)
+ * accumulator before the store; these are its per-row / per-column forms, and
+ * the fp8 output with its amax the quantising store of a low-precision path.)
  */
 typedef struct {
     const float *alpha_scale;
     const float *row_scale;
     const float *col_scale;
+    const float *out_scale;
+    float *amax;
 } gemm_scales_t;
 
 /*
- * gemm_ex -- gemm() with product scales (scales may be NULL: then exactly
- * gemm()).  Same arguments, conventions and errors; the scale arrays are
- * checked against their device allocations like every other buffer.  With
- * K == 0 or alpha == 0 the scales are not read.
+ * gemm_ex -- gemm() with the scales above (scales may be NULL: then exactly
+ * gemm()).  Same arguments, conventions and errors, plus c_dtype E4M3 (fp8
+ * output, from F16, BF16 or E4M3 inputs, beta == 0; otherwise
+ * GEMM_ERR_UNSUPPORTED).  The scale arrays are checked against their device
+ * allocations like every other buffer.  With K == 0 or alpha == 0 the
+ * product scales are not read (out_scale and amax still apply).
  */
 gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K,
                       gemm_dtype_t ab_dtype,
