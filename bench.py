@@ -50,6 +50,8 @@ def _args(argv=None):
     ap.add_argument("--q4-decode", type=int, default=0, metavar="M",
                     help="only the quantized decode cell with M rows of x (for profiling); prints its JSON")
     ap.add_argument("--q4-reps", type=int, default=50, help="timed calls of the --q4-decode cell")
+    ap.add_argument("--q4-kernel", choices=("auto", "ffma", "mma"), default="auto",
+                    help="decode kernel of the --q4-decode cell")
     return ap.parse_args(argv)
 
 
@@ -435,8 +437,16 @@ def extra_cells(g, stream):
                                "fused_cost_pct": round(100 * (plain["median_tflops"] / fused["median_tflops"] - 1),
                                                        2)}
     cells["baseline_gate_fp16_4096"] = baseline_gate(g, stream)
-    for M in (1, 8):
+    for M in (1, 2, 8):
         cells[f"q4_decode_M{M}_16384"] = q4_decode_cell(g, stream, M)
+        # the two decode kernels side by side (AUTO above picks one of them)
+        for name, kind in (("ffma", g.Q4_FFMA), ("mma", g.Q4_MMA)):
+            g.gemm_set_q4_kernel(kind)
+            try:
+                r = q4_decode_cell(g, stream, M, reps=30)
+            finally:
+                g.gemm_set_q4_kernel(g.Q4_AUTO)
+            cells[f"q4_decode_M{M}_16384"][f"kernel_{name}"] = {k: r[k] for k in ("median_gbs", "ci95", "mean_us")}
     return cells
 
 
@@ -564,6 +574,7 @@ def main(argv=None):
     if a.q4_decode:
         import torch
         import dense_gemm_epilogues_tcgen05_gb300 as g
+        g.gemm_set_q4_kernel({"auto": g.Q4_AUTO, "ffma": g.Q4_FFMA, "mma": g.Q4_MMA}[a.q4_kernel])
         print(json.dumps(q4_decode_cell(g, torch.cuda.current_stream(), a.q4_decode, reps=a.q4_reps)), flush=True)
     elif a.impl == "reference":
         run_reference(a)

@@ -25,6 +25,7 @@ __all__ = [
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K", "ORDER_AUTO", "ORDER_AS_GIVEN", "ORDER_TRANSPOSED",
     "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast", "gemm_last_launch",
     "BASELINE_SIMT", "BASELINE_MMA_SYNC", "gemm_baseline", "gemm_q4", "gemm_q4_dequantize", "Q4_MAX_ROWS",
+    "Q4_AUTO", "Q4_FFMA", "Q4_MMA", "gemm_set_q4_kernel",
     "gemm_ex",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
@@ -48,6 +49,8 @@ MCAST_AUTO, MCAST_OFF, MCAST_ON = 0, 1, 2
 BASELINE_SIMT, BASELINE_MMA_SYNC = 0, 1
 # gemm_q4 takes at most this many rows of x (decode)
 Q4_MAX_ROWS = 8
+# gemm_q4_kernel_t
+Q4_AUTO, Q4_FFMA, Q4_MMA = 0, 1, 2
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -106,6 +109,8 @@ class _Scales(ctypes.Structure):
 lib.gemm_ex.restype = _int
 lib.gemm_ex.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _int,
                         _f32, _f32, _vp, _int, ctypes.POINTER(_Scales), _vp, _sz, _vp]
+lib.gemm_set_q4_kernel.restype = _int
+lib.gemm_set_q4_kernel.argtypes = [_int]
 lib.gemm_q4.restype = _int
 lib.gemm_q4.argtypes = [_i64, _i64, _i64, _int, ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p,
                         ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
@@ -240,6 +245,11 @@ def gemm_ex(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_strid
                      _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue, ctypes.byref(sc), _ptr(workspace),
                      workspace_bytes, _stream(stream))
     return _check(st, "gemm_ex")
+
+
+def gemm_set_q4_kernel(kind) -> int:
+    """Process-wide kernel of gemm_q4 (Q4_*): AUTO, the CUDA-core kernel, or the tensor-core one."""
+    return _check(lib.gemm_set_q4_kernel(kind), "gemm_set_q4_kernel")
 
 
 def gemm_q4(M, N, K, x_dtype, X, ldx, Wq, scale_bias, C, ldc, c_dtype, alpha, beta, bias, epilogue,

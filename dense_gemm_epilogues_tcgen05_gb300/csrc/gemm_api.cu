@@ -295,6 +295,7 @@ std::atomic<int> g_tile_policy_bn{0};
 std::atomic<int> g_schedule{GEMM_SCHED_AUTO};
 std::atomic<int> g_operand_order{GEMM_ORDER_AUTO};
 std::atomic<int> g_multicast{GEMM_MCAST_AUTO};
+std::atomic<int> g_q4_kernel{GEMM_Q4_AUTO};
 std::atomic<unsigned int> g_epoch{0};
 
 // The calling thread's last successful gemm() launch (gemm_last_launch).
@@ -908,6 +909,19 @@ gemm_status_t gemm_baseline(gemm_baseline_t kind, int64_t M, int64_t N, int64_t 
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// AUTO's choice of decode kernel for M rows of x, from 1 x / 8 x 16384 x 16384 on
+// GB300: one row is HBM-streaming FFMA work (3.07 TB/s against 2.09 for the
+// tensor-core kernel, whose integer unpacking then bounds it); from two rows
+// on, the FFMA kernel re-reads x for every pair of weight rows (0.40 TB/s at
+// eight rows) while the tensor-core kernel stays near 2 TB/s.
+bool q4_auto_mma(int64_t M) { return M >= 2; }
+
+gemm_status_t gemm_set_q4_kernel(gemm_q4_kernel_t kind) {
+    if (kind < GEMM_Q4_AUTO || kind > GEMM_Q4_MMA) return GEMM_ERR_INVALID_ARG;
+    g_q4_kernel.store(kind);
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, const void *X, int64_t ldx,
                       const uint32_t *Wq, const void *scale_bias, void *C, int64_t ldc, gemm_dtype_t c_dtype,
                       float alpha, float beta, const float *bias, gemm_epilogue_t epilogue, gemm_stream_t stream) {
@@ -948,7 +962,22 @@ gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, con
     a.ldx = ldx;
     a.Wq = Wq;
     a.SB = static_cast<const uint32_t *>(scale_bias);
-    return launch_q4_gemv(x_dtype, c_dtype, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    a.status = dev->status;
+    const int kind = g_q4_kernel.load();
+    if (!(kind == GEMM_Q4_MMA || (kind == GEMM_Q4_AUTO && q4_auto_mma(M))))
+        return launch_q4_gemv(x_dtype, c_dtype, nullptr, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    // The tensor-core kernel's weight boxes: 32 rows x min(160, K/2) bytes of codes.
+    a.w_pitch = static_cast<int>(K / 2 < 160 ? K / 2 : 160);
+    CUtensorMap tmW;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(a.w_pitch), 32u};
+    cuuint32_t estr[2] = {1, 1};
+    if (driver_fns().encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(Wq), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return GEMM_ERR_CUDA;
+    return launch_q4_gemv(x_dtype, c_dtype, &tmW, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 gemm_status_t gemm_q4_dequantize(int64_t N, int64_t K, const uint32_t *Wq, const void *scale_bias, void *W,

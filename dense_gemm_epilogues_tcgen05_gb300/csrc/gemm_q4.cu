@@ -225,6 +225,257 @@ __global__ void __launch_bounds__(kQ4Warps * 32) q4_gemv_kernel(const Q4Args a) 
     }
 }
 
+// ---------------------------------------------------------------------------
+// q4_mma_kernel (decode on the tensor cores, M <= 8 rows of x).
+//
+// The codes (one 2-D TMA box of the block's rows per stage) and x (one bulk
+// copy per row) reach shared memory on an mbarrier ring that one producer
+// warp keeps full, so each SM holds tens of KB of HBM reads in flight without
+// spending registers on them.  Four consumer warps
+// turn the codes into exact 16-bit integers and multiply them with x by
+// mma.sync.m16n8k16: the instruction's 16 rows are weight rows and its 8
+// columns the rows of x, so one x fragment serves all of a warp's weight rows.
+//
+// A block owns kQmRows weight rows.  A stage holds kQmChunk consecutive k of
+// those rows and of every row of x; consumer warp w takes group w (64 k) of
+// every stage.  The weight box is 160 bytes wide although a stage uses 128:
+// rows then sit 160 bytes apart in shared memory, where the consumers' reads
+// meet no bank conflicts, and the extra 32 bytes (the next stage's first
+// codes) come again from L2, not from HBM.  Scale and bias are fixed within a group, so
+// sum_k x (s q + b) = s * (sum_k x q) + b * (sum_k x): the MMA sums x q over
+// the group in fp32, and s and b are applied once per group.
+//
+// The sum over k does not depend on the order of the k, so the MMA's k
+// positions are matched to memory by a permutation both operands share: the
+// thread that supplies k-pair (2t, 2t+1) of a weight row supplies codes j and
+// j + 4 of one 32-bit word, which one mask-and-or puts in the two halves of a
+// 16-bit pair (exponent of 1024 for fp16 or 128 for bf16, then that constant
+// subtracted: exact), and the x fragment is permuted alike by byte permutes.
+constexpr int kQmRows = 32;                              // weight rows per block (two 16-row MMA tiles)
+constexpr int kQmChunk = 256;                            // k per stage (four groups)
+constexpr int kQmWPitch = 160;                           // weight box width in bytes (128 of this stage's codes)
+constexpr int kQmXPitch = 528;                           // bytes per x row in a stage (512 of values)
+constexpr int kQmConsumers = 4;                          // one per group of a stage
+constexpr int kQmThreads = (kQmConsumers + 1) * 32;      // + the producer warp
+
+template <int MM>
+struct QmCfg {
+    static constexpr int STAGES = MM == 8 ? 5 : 6;
+    static constexpr int W_BYTES = kQmRows * kQmWPitch;
+    static constexpr int STAGE_BYTES = (W_BYTES + MM * kQmXPitch + 127) / 128 * 128;  // boxes 128-byte aligned
+    static constexpr int PART_OFF = STAGES * STAGE_BYTES;                  // per-warp partial sums
+    static constexpr int BAR_OFF = PART_OFF + kQmConsumers * kQmRows * 8 * 4;
+    static constexpr int SMEM = BAR_OFF + 2 * STAGES * 8 + 16 + 128;       // + the abort flag, + alignment slack
+};
+// Pitches: the weight rows' 8-byte reads of a half-warp and the x rows'
+// 16-byte reads of a quarter-warp each fall in distinct banks.
+static_assert(kQmWPitch % 16 == 0 && kQmXPitch % 16 == 0, "bulk copy destinations are 16-byte aligned");
+static_assert(QmCfg<8>::SMEM * 4 + 4 * 1024 <= 228 * 1024, "four blocks of the widest build fit on an SM");
+
+// Nibbles at bits 0-3 and 16-19 of w as an exact 16-bit pair of type XT.
+template <int XT>
+__device__ __forceinline__ uint32_t code_pair_16(uint32_t w) {
+    uint32_t r;
+    if constexpr (XT == kDtF16) {
+        const uint32_t h = (w & 0x000F000Fu) | 0x64006400u;  // 1024 + code, twice
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64006400u));
+    } else {
+        const uint32_t h = (w & 0x000F000Fu) | 0x43004300u;  // 128 + code, twice
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x43004300u));
+    }
+    return r;
+}
+
+template <int XT>
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (XT == kDtF16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int XT, int OUT, int MM>
+__global__ void __launch_bounds__(kQmThreads, 4)
+    q4_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ Q4Args a) {
+    using Cfg = QmCfg<MM>;
+    using OutT = typename Elem<OUT>::T;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFF);
+    uint64_t *empty = full + Cfg::STAGES;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + Cfg::STAGES);
+    float *part = reinterpret_cast<float *>(smem + Cfg::PART_OFF);  // [warp][row][column of x]
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int M = a.e.M, N = a.e.N, K = a.K;
+    const int n0 = blockIdx.x * kQmRows;
+    const int nvalid = min(kQmRows, N - n0);
+    const int nchunks = (K + kQmChunk - 1) / kQmChunk;
+    const int wp = a.w_pitch;  // bytes per weight row in a stage: the box width, min(160, K / 2)
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmW);
+        for (int st = 0; st < Cfg::STAGES; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], kQmConsumers);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kQmConsumers) {
+        // Producer: lane 0 loads the weight box (rows past N and bytes past K / 2
+        // read as zero), lanes below M copy the rows of x.
+        const uint8_t *xg = static_cast<const uint8_t *>(a.X);
+        const long long xrow = a.ldx * 2;  // bytes per row of x
+        int issued = 0;
+        for (int i = 0; i < nchunks; ++i) {
+            const int st = i % Cfg::STAGES;
+            if (i >= Cfg::STAGES) {
+                const bool ok = mbar_wait_bounded(&empty[st], ((i / Cfg::STAGES) & 1) ^ 1, abort_flag, a.status);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            const int kc = min(kQmChunk, K - i * kQmChunk);
+            const uint32_t xb = kc * 2;
+            uint8_t *stage = smem + st * Cfg::STAGE_BYTES;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[st], kQmRows * wp + M * xb);
+                tma_load_2d(stage, &tmW, &full[st], i * (kQmChunk / 2), n0);
+            }
+            __syncwarp();
+            if (lane < M)
+                bulk_load_1d(stage + Cfg::W_BYTES + lane * kQmXPitch,
+                             xg + (long long)lane * xrow + (long long)i * (kQmChunk * 2), xb, &full[st]);
+            issued = i + 1;
+        }
+        // After an abort, let the copies already issued land before the block exits.
+        if (*abort_flag && lane == 0)
+            for (int j = max(0, issued - Cfg::STAGES); j < issued; ++j)
+                mbar_drain_wait(&full[j % Cfg::STAGES], (j / Cfg::STAGES) & 1, kWaitLimitNs);
+    } else {
+        const int w = warp, g = lane >> 2, t = lane & 3;
+        const long long gpr = K / 64;  // groups per weight row
+        // This thread's rows: 16R + g (j = 2R) and 16R + g + 8 (j = 2R + 1).
+        const uint32_t *sbrow[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = (j >> 1) * 16 + (j & 1) * 8 + g;
+            sbrow[j] = a.SB + (long long)(n0 + (r < nvalid ? r : 0)) * gpr;
+        }
+        // Scale and bias of group w of a chunk, two chunks ahead.
+        uint32_t sbc[4], sbn[4];
+        auto load_sb = [&](int i, uint32_t (&d)[4]) {
+            const long long G = 4LL * i + w;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d[j] = (i < nchunks && G < gpr) ? __ldg(sbrow[j] + G) : 0u;
+        };
+        load_sb(0, sbc);
+        load_sb(1, sbn);
+        float tot[2][4];
+#pragma unroll
+        for (int R = 0; R < 2; ++R)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tot[R][c] = 0.0f;
+
+        for (int i = 0; i < nchunks; ++i) {
+            const int st = i % Cfg::STAGES;
+            const bool ok = mbar_wait_bounded(&full[st], (i / Cfg::STAGES) & 1, abort_flag, a.status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const int ngroups = min(kQmChunk, K - i * kQmChunk) / 64;
+            if (w < ngroups) {
+                const uint8_t *stage = smem + st * Cfg::STAGE_BYTES;
+                // x row g, k 16t .. 16t + 15 of group w (zero for rows past M)
+                uint32_t v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = 0u;
+                if (g < M) {
+                    const uint8_t *xp = stage + Cfg::W_BYTES + g * kQmXPitch + 128 * w + 32 * t;
+                    const uint4 p0 = *reinterpret_cast<const uint4 *>(xp);
+                    const uint4 p1 = *reinterpret_cast<const uint4 *>(xp + 16);
+                    v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
+                    v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+                }
+                // sum over the group of x row g (fp32), then the sums of rows 2t and 2t + 1
+                uint64_t s2 = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) s2 = f2_add(s2, x_pair_f2<XT>(v[q]));
+                float xs0, xs1;
+                f2_unpack(s2, xs0, xs1);
+                float xs = xs0 + xs1;
+                xs += __shfl_xor_sync(0xffffffffu, xs, 1);
+                xs += __shfl_xor_sync(0xffffffffu, xs, 2);
+                const float xc0 = __shfl_sync(0xffffffffu, xs, 8 * t);
+                const float xc1 = __shfl_sync(0xffffffffu, xs, 8 * t + 4);
+                // B fragments of MMA h: (x_p, x_p+4) and (x_p+1, x_p+5), p = 8 (h / 2) + 2 (h % 2)
+                uint32_t bf[4][2];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t lo = v[4 * (h >> 1) + (h & 1)], hi = v[4 * (h >> 1) + (h & 1) + 2];
+                    bf[h][0] = __byte_perm(lo, hi, 0x5410);
+                    bf[h][1] = __byte_perm(lo, hi, 0x7632);
+                }
+#pragma unroll
+                for (int R = 0; R < 2; ++R) {
+                    const uint8_t *wrow = stage + (16 * R + g) * wp + 32 * w + 8 * t;
+                    const uint2 wa = *reinterpret_cast<const uint2 *>(wrow);           // row 16R + g
+                    const uint2 wb = *reinterpret_cast<const uint2 *>(wrow + 8 * wp);  // row 16R + g + 8
+                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint32_t ua = h < 2 ? wa.x : wa.y, ub = h < 2 ? wb.x : wb.y;
+                        const int sh = (h & 1) * 8;
+                        const uint32_t af[4] = {code_pair_16<XT>(ua >> sh), code_pair_16<XT>(ub >> sh),
+                                                code_pair_16<XT>(ua >> (sh + 4)), code_pair_16<XT>(ub >> (sh + 4))};
+                        mma_m16n8k16<XT>(d, af, bf[h][0], bf[h][1]);
+                    }
+                    const float2 sb0 = __half22float2(*reinterpret_cast<const __half2 *>(&sbc[2 * R]));
+                    const float2 sb1 = __half22float2(*reinterpret_cast<const __half2 *>(&sbc[2 * R + 1]));
+                    tot[R][0] = fmaf(sb0.x, d[0], fmaf(sb0.y, xc0, tot[R][0]));
+                    tot[R][1] = fmaf(sb0.x, d[1], fmaf(sb0.y, xc1, tot[R][1]));
+                    tot[R][2] = fmaf(sb1.x, d[2], fmaf(sb1.y, xc0, tot[R][2]));
+                    tot[R][3] = fmaf(sb1.x, d[3], fmaf(sb1.y, xc1, tot[R][3]));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sbc[j] = sbn[j];
+            load_sb(i + 2, sbn);
+        }
+        // D fragment: (row g, x rows 2t, 2t + 1) and (row g + 8, same)
+#pragma unroll
+        for (int R = 0; R < 2; ++R) {
+            float *p0 = part + (w * kQmRows + 16 * R + g) * 8 + 2 * t;
+            p0[0] = tot[R][0];
+            p0[1] = tot[R][1];
+            p0[8 * 8] = tot[R][2];
+            p0[8 * 8 + 1] = tot[R][3];
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) return;
+    // Sum the warps' partials in warp order; consecutive threads take consecutive n.
+    for (int idx = threadIdx.x; idx < kQmRows * M; idx += blockDim.x) {
+        const int r = idx % kQmRows, m = idx / kQmRows;
+        if (r >= nvalid) continue;
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kQmConsumers; ++w) v += part[(w * kQmRows + r) * 8 + m];
+        const int n = n0 + r;
+        const float b = (a.e.epilogue != kEpiNone) ? a.e.bias[n] : 0.0f;
+        epilogue_store_one<OUT>(v, static_cast<OutT *>(a.e.C) + (long long)m * a.e.ldc + n, b, a.e);
+    }
+}
+
 template <int OUT>
 __global__ void q4_dequantize_kernel(long long N, long long K, const uint32_t *__restrict__ Wq,
                                      const uint32_t *__restrict__ SB, typename Elem<OUT>::T *__restrict__ W) {
@@ -266,17 +517,42 @@ cudaError_t launch_gemv_rows(const Q4Args &a, cudaStream_t s) {
     return launch_gemv_mm<XT, OUT, 8>(a, s);
 }
 
+// One block per kQmRows weight rows; the smallest x staging that holds M rows.
+template <int XT, int OUT, int MM>
+cudaError_t launch_mma_mm(const CUtensorMap &tmW, const Q4Args &a, cudaStream_t s) {
+    using Cfg = QmCfg<MM>;
+    auto kern = q4_mma_kernel<XT, OUT, MM>;
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (err != cudaSuccess) return err;
+    const long long blocks = (static_cast<long long>(a.e.N) + kQmRows - 1) / kQmRows;
+    if (blocks > 2147483647LL) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(blocks), kQmThreads, Cfg::SMEM, s>>>(tmW, a);
+    return cudaGetLastError();
+}
+
+template <int XT, int OUT>
+cudaError_t launch_rows(const CUtensorMap *tmW, const Q4Args &a, cudaStream_t s) {
+    const int M = a.e.M;
+    if (tmW != nullptr) {
+        if (M <= 1) return launch_mma_mm<XT, OUT, 1>(*tmW, a, s);
+        if (M <= 2) return launch_mma_mm<XT, OUT, 2>(*tmW, a, s);
+        if (M <= 4) return launch_mma_mm<XT, OUT, 4>(*tmW, a, s);
+        return launch_mma_mm<XT, OUT, 8>(*tmW, a, s);
+    }
+    return launch_gemv_rows<XT, OUT>(a, s);
+}
+
 }  // namespace
 
-cudaError_t launch_q4_gemv(int x_dtype, int out, const Q4Args &a, cudaStream_t s) {
+cudaError_t launch_q4_gemv(int x_dtype, int out, const CUtensorMap *tmW, const Q4Args &a, cudaStream_t s) {
     if (a.e.M < 1 || a.e.M > kQ4MaxRows) return cudaErrorInvalidValue;
     switch (x_dtype * 4 + out) {
-    case kDtF16 * 4 + kDtF16: return launch_gemv_rows<kDtF16, kDtF16>(a, s);
-    case kDtF16 * 4 + kDtBF16: return launch_gemv_rows<kDtF16, kDtBF16>(a, s);
-    case kDtF16 * 4 + kDtF32: return launch_gemv_rows<kDtF16, kDtF32>(a, s);
-    case kDtBF16 * 4 + kDtF16: return launch_gemv_rows<kDtBF16, kDtF16>(a, s);
-    case kDtBF16 * 4 + kDtBF16: return launch_gemv_rows<kDtBF16, kDtBF16>(a, s);
-    case kDtBF16 * 4 + kDtF32: return launch_gemv_rows<kDtBF16, kDtF32>(a, s);
+    case kDtF16 * 4 + kDtF16: return launch_rows<kDtF16, kDtF16>(tmW, a, s);
+    case kDtF16 * 4 + kDtBF16: return launch_rows<kDtF16, kDtBF16>(tmW, a, s);
+    case kDtF16 * 4 + kDtF32: return launch_rows<kDtF16, kDtF32>(tmW, a, s);
+    case kDtBF16 * 4 + kDtF16: return launch_rows<kDtBF16, kDtF16>(tmW, a, s);
+    case kDtBF16 * 4 + kDtBF16: return launch_rows<kDtBF16, kDtBF16>(tmW, a, s);
+    case kDtBF16 * 4 + kDtF32: return launch_rows<kDtBF16, kDtF32>(tmW, a, s);
     default: return cudaErrorInvalidValue;
     }
 }

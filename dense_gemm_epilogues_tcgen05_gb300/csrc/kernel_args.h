@@ -85,6 +85,8 @@ struct Q4Args {
     long long ldx;
     const uint32_t *Wq;       // N * K/8 words: code of (n, k) in bits 4*(k%8) of word n*K/8 + k/8
     const uint32_t *SB;       // N * K/64 words: binary16 scale (low half) and bias (high half) of group (n, g)
+    unsigned int *status;     // device status word (timeouts of the tensor-core kernel's waits)
+    int w_pitch;              // tensor-core kernel: width in bytes of its weight box, min(160, K / 2)
 };
 
 // Launchers (each returns the launch's cudaError_t), defined by the kernel files.
@@ -122,7 +124,9 @@ cudaError_t launch_epilogue_only(int out, const EpiParams &e, cudaStream_t strea
 cudaError_t launch_bias_gelu(int out, const EpiParams &e, cudaStream_t stream);
 //   4-bit quantized product for up to kQ4MaxRows rows of x, and the dequantisation pass:
 constexpr int kQ4MaxRows = 8;
-cudaError_t launch_q4_gemv(int x_dtype, int out, const Q4Args &args, cudaStream_t stream);
+//   4-bit decode: with a map of the codes (K/2 bytes x N rows, box w_pitch x 32 rows) the tensor-core
+//   kernel (TMA staging, mma.sync), without one (nullptr) the CUDA-core kernel
+cudaError_t launch_q4_gemv(int x_dtype, int out, const CUtensorMap *tmW, const Q4Args &args, cudaStream_t stream);
 cudaError_t launch_q4_dequantize(int out, long long N, long long K, const uint32_t *Wq, const uint32_t *SB, void *W,
                                  cudaStream_t stream);
 cudaError_t launch_wait_selftest(const unsigned int *never_set, unsigned long long limit_ns, unsigned int *status,

@@ -127,6 +127,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
 }
 
 // Close the current bulk async-group of this thread.
+// Untiled bulk copy global -> this CTA's shared memory, counted as `bytes`
+// transaction bytes on `bar`.  Both addresses 16-byte aligned, `bytes` a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load_1d(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's bulk groups still read their shared-memory source.

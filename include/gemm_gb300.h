@@ -409,6 +409,25 @@ gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype,
                       gemm_stream_t stream);
 
 /*
+ * The kernel behind gemm_q4.  Both compute the same sums (per 64-k group,
+ * s * sum_k x q + b * sum_k x, in fp32) and meet the same tolerances; they
+ * differ in how the weights move and where the products are formed.
+ */
+typedef enum {
+    GEMM_Q4_AUTO = 0,   /* the one measured faster for the number of rows of x */
+    GEMM_Q4_FFMA = 1,   /* CUDA-core kernel: 16-byte loads into registers, codes to fp32, f32x2 multiply-add */
+    GEMM_Q4_MMA = 2     /* tensor-core kernel: codes and x staged in shared memory by bulk copies, exact
+                           16-bit codes times x by mma.sync.m16n8k16 (rows of x as the 8 columns) */
+} gemm_q4_kernel_t;
+
+/*
+ * gemm_set_q4_kernel -- kernel of later gemm_q4() calls, for every thread of
+ * the process.  Meant for tuning and tests.  GEMM_ERR_INVALID_ARG for an
+ * unknown value; never touches the device.
+ */
+gemm_status_t gemm_set_q4_kernel(gemm_q4_kernel_t kind);
+
+/*
  * gemm_q4_dequantize -- W[n][k] = round(s*q + b) into the N x K row-major
  * device array W of type w_dtype (F16 or BF16; 16-byte aligned), for
  * gemm(M, N, K, w_dtype, X, ldx, 1, W, 1, K, ...) to multiply (W^T as B,

@@ -39,7 +39,7 @@ def test_header_declares_the_entry_points():
     assert {"gemm", "gemm_workspace_size", "gemm_query_path", "gemm_bias_gelu", "gemm_device_status",
             "gemm_status_string", "gemm_version", "gemm_set_tile_policy", "gemm_query_tile",
             "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest", "gemm_set_multicast",
-            "gemm_last_launch"} <= names
+            "gemm_last_launch", "gemm_q4", "gemm_set_q4_kernel"} <= names
 
 
 def test_library_exports_every_declared_symbol(g):
@@ -79,6 +79,15 @@ def test_operand_order_validation(g):
         with pytest.raises(g.GemmError):
             g.gemm_set_operand_order(v)
     g.gemm_set_operand_order(g.ORDER_AUTO)
+
+
+def test_q4_kernel_validation(g):
+    for v in (g.Q4_AUTO, g.Q4_FFMA, g.Q4_MMA):
+        assert g.gemm_set_q4_kernel(v) == 0
+    for v in (-1, 3):
+        with pytest.raises(g.GemmError):
+            g.gemm_set_q4_kernel(v)
+    g.gemm_set_q4_kernel(g.Q4_AUTO)
 
 
 def test_last_launch_records_only_successful_calls(g):

@@ -7,8 +7,10 @@ against the float64 oracle (oracle.q4), through the C ABI.
   1024-deep step.
 * Realistic problems (N(0, 0.02^2) weights quantized per group, x ~ N(0,1))
   meet the normalised tolerance for every output type and epilogue.
-* The full-size decode workload (1 x 16384 x 16384) is checked on sampled
-  output columns, from the oracle on those weight rows alone.
+* The full-size decode workloads (1 and 8 x 16384 x 16384) are checked on
+  sampled output columns, from the oracle on those weight rows alone.
+* Every kernel-dependent test runs on both decode kernels (CUDA-core FFMA and
+  tensor-core mma.sync), chosen with gemm_set_q4_kernel.
 * The dequantisation pass is exact (rounding of s*q + b, which fp32 holds
   exactly for these inputs), and dequantise-then-gemm() meets the tolerance.
 Every call also checks that nothing outside the M x N block of C was written.
@@ -23,6 +25,15 @@ from gpu_util import CANARY, GUARD
 from oracle import q4
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["ffma", "mma"])
+def q4k(request, cuda_lib):
+    """Each test runs on both decode kernels: CUDA-core FFMA and tensor-core mma.sync."""
+    g = cuda_lib
+    g.gemm_set_q4_kernel(g.Q4_FFMA if request.param == "ffma" else g.Q4_MMA)
+    yield g
+    g.gemm_set_q4_kernel(g.Q4_AUTO)
 
 
 def run_q4(g, p):
@@ -48,11 +59,13 @@ def run_q4(g, p):
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
-@pytest.mark.parametrize("N,K", [(1, 64), (7, 1088), (64, 1024), (129, 4096)], ids=lambda v: str(v))
+@pytest.mark.parametrize("N,K", [(1, 64), (7, 1088), (64, 1024), (129, 4096), (45, 320)], ids=lambda v: str(v))
 @pytest.mark.parametrize("xd", [wl.F16, wl.BF16], ids=["f16", "bf16"])
-def test_integer_exact(cuda_lib, M, N, K, xd):
+def test_integer_exact(q4k, M, N, K, xd):
+    """Ragged N (a block's 32 rows part-filled), K not a multiple of a stage's 256 k
+    (1088, 320: a last stage of one group) or of a warp's 1024-k step."""
     p = wl.q4_problem(100 + M + N + K, M, N, K, xd, wl.F32, integer=True, ldc_pad=3)
-    out = run_q4(cuda_lib, p)
+    out = run_q4(q4k, p)
     y, _ = q4.q4_reference(**p.oracle_args())
     got = oracle.output_values(out, p.M, p.N, p.ldc, p.c_dtype)
     assert np.array_equal(got, y)
@@ -61,11 +74,11 @@ def test_integer_exact(cuda_lib, M, N, K, xd):
 @pytest.mark.parametrize("cd", [wl.F16, wl.BF16, wl.F32], ids=["f16", "bf16", "f32"])
 @pytest.mark.parametrize("epi", [wl.EPI_NONE, wl.EPI_BIAS, wl.EPI_BIAS_GELU, wl.EPI_BIAS_SILU],
                          ids=["none", "bias", "gelu", "silu"])
-def test_realistic_tolerance(cuda_lib, cd, epi):
-    for M, xd in ((1, wl.F16), (4, wl.BF16), (8, wl.F16)):
+def test_realistic_tolerance(q4k, cd, epi):
+    for M, xd in ((1, wl.F16), (4, wl.BF16), (8, wl.F16), (6, wl.BF16)):
         p = wl.q4_problem(7 + M, M, 320, 2048, xd, cd, alpha=1.25, beta=0.5 if epi == wl.EPI_NONE else 0.0,
                           epilogue=epi)
-        res = q4.check(p.oracle_args(), run_q4(cuda_lib, p))
+        res = q4.check(p.oracle_args(), run_q4(q4k, p))
         assert res["pass"], (M, res)
 
 
@@ -85,20 +98,21 @@ def test_degenerate(cuda_lib):
     assert e.value.status == g.ERR_UNSUPPORTED
 
 
-def test_decode_workload_sampled_columns(cuda_lib):
-    """1 x 16384 x 16384 (the bench's decode cell) on 96 sampled outputs, against the
+@pytest.mark.parametrize("M", [1, 8])
+def test_decode_workload_sampled_columns(q4k, M):
+    """M x 16384 x 16384 (the bench's decode cells) on 96 sampled outputs, against the
     oracle run on just those weight rows (an output column needs only its row of W)."""
     N = K = 16384
-    p = wl.q4_problem(41, 1, N, K, wl.F16, wl.F16)
-    out = run_q4(cuda_lib, p)
+    p = wl.q4_problem(41, M, N, K, wl.F16, wl.F16)
+    out = run_q4(q4k, p)
     rng = np.random.default_rng(7)
     cols = np.unique(np.concatenate([[0, 1, N - 1], rng.integers(0, N, 93)]))
     a = p.oracle_args()
     wq = a["Wq"].reshape(N, K // 8)[cols].reshape(-1)
     sb = a["scale_bias"].reshape(N, K // 64 * 2)[cols].reshape(-1)
-    sub = dict(a, N=len(cols), Wq=wq, scale_bias=sb, ldc=len(cols), C=np.zeros(len(cols), np.int16))
+    sub = dict(a, N=len(cols), Wq=wq, scale_bias=sb, ldc=len(cols), C=np.zeros(M * len(cols), np.int16))
     y, D = q4.q4_reference(**sub)
-    got = oracle.output_values(out, 1, N, p.ldc, p.c_dtype)[:, cols]
+    got = oracle.output_values(out, M, N, p.ldc, p.c_dtype)[:, cols]
     err = oracle.max_normalized_error(got, y, D, wl.EPI_NONE)
     assert err <= oracle.tolerance(wl.F16, wl.F16), err
 
