@@ -472,3 +472,37 @@ def test_amax_reference():
     ones = wl.make_problem("ones", 3, 4, 16, wl.F16, wl.F32, torch.ones(3, 16), torch.ones(16, 4), alpha=1.0,
                            bias=torch.tensor([1.0, -40.0, 2.0, 0.0]), epilogue=wl.EPI_BIAS)
     assert oracle.amax_reference(ones.oracle_args())[0] == 24.0
+
+
+def _e4m3_table():
+    """Every finite E4M3 value, by PyTorch's CPU decode of all 256 codes (a library routine)."""
+    t = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return np.unique(t[np.isfinite(t)])
+
+
+@pytest.mark.parametrize("mistake", [None, "flush_subnormals", "truncate"])
+def test_fp8_output_check_subnormal_range(mistake):
+    """K = 1 makes y = a exactly and D = |a|, so a mis-rounded tiny value cannot hide behind a
+    large error scale.  a spans E4M3's subnormals (steps of 2^-9 below 2^-6) on an eighth-step
+    grid, ties included, plus normal and saturating values.  The right codes pass; flushing the
+    subnormals to zero or truncating toward zero instead of rounding to nearest even fails."""
+    vals = np.array([k * 2.0 ** -12 for k in range(-72, 73) if k != 0] + [0.3, -5.0, 447.0, -500.0])
+    M = len(vals)
+    p = wl.make_problem("e4m3_subnormals", M, 1, 1, wl.F16, wl.F32, torch.tensor(vals, dtype=torch.float32)
+                        .reshape(M, 1), torch.ones(1, 1))
+    a = p.oracle_args()
+    y, D = oracle.gemm_reference(**a)
+    assert np.array_equal(y.reshape(-1), vals.astype(np.float16).astype(np.float64))  # exact in fp16
+    q = y.reshape(-1)
+    if mistake is None:
+        codes = _e4m3_codes(q)
+    elif mistake == "flush_subnormals":
+        codes = _e4m3_codes(np.where(np.abs(q) < 2.0 ** -6, 0.0, q))
+    else:
+        table = _e4m3_table()
+        mag = np.minimum(np.abs(q), 448.0)
+        down = np.array([table[table <= m].max() for m in mag])
+        codes = _e4m3_codes(np.sign(q) * down)
+    ax = dict(a, c_dtype=wl.E4M3, C=codes)
+    res = oracle.check_fp8_output(ax, codes, 1.0)
+    assert res["pass"] == (mistake is None), res
