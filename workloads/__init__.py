@@ -431,3 +431,126 @@ def with_product_scales(p: Problem, seed: int, *, alpha_scale: bool = True, row:
     if col:
         ps["col_scale"] = draw(p.N)
     return dataclasses.replace(p, product_scales=ps, recipe=p.recipe + f" scales(seed={seed}, dyadic={dyadic})")
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled (MX) inputs.  Quantisation as the OCP Microscaling Formats (MX)
+# Specification v1.0 describes it -- input preparation, not the product: each
+# block of 32 consecutive k of a row shares the scale X = 2^E with
+# E = floor(log2(amax of the block)) - emax(element type), and each element is
+# x / X rounded to nearest even in the element type, saturating at its largest
+# normal.  E4M3 elements one per byte; E2M1 elements two per byte (even k in
+# the low nibble); scales as E8M0 codes (E + 127).
+# ---------------------------------------------------------------------------
+
+MX_BLOCK = 32
+MX_E4M3, MX_E2M1 = "e4m3", "e2m1"
+MX_EMAX = {MX_E4M3: 8, MX_E2M1: 2}          # exponent of each element type's largest normal
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)   # codes 0..7
+
+
+def e2m1_codes(v: torch.Tensor) -> torch.Tensor:
+    """Round-to-nearest-even, saturating FP4 E2M1 codes (0..15, int64) of float values."""
+    grid = torch.tensor(E2M1_MAGNITUDES, dtype=torch.float64)
+    mag = v.to(torch.float64).abs().clamp(max=E2M1_MAGNITUDES[-1])
+    d = (mag[..., None] - grid).abs()
+    tie = d == d.min(dim=-1, keepdim=True).values
+    idx = torch.arange(8)
+    # among the nearest magnitudes (two at a tie, neighbours) take the even code
+    code = torch.where(tie, idx % 2, torch.full_like(idx, 2)).argmin(dim=-1)
+    return torch.where(v < 0, code + 8, code)
+
+
+def mx_quantize(x: torch.Tensor, elem: str):
+    """Quantise a rows x K float matrix (K a multiple of 32) to MX element and scale codes.
+
+    Returns (codes, scales): uint8 tensors, rows x K (E4M3) or rows x K/2 (E2M1,
+    packed) and rows x K/32."""
+    rows, K = x.shape
+    blocks = x.to(torch.float32).reshape(rows, K // MX_BLOCK, MX_BLOCK)
+    amax = blocks.abs().amax(dim=-1)
+    _, e2 = torch.frexp(amax)                      # amax = m * 2^e2, m in [0.5, 1)
+    floor_log2 = (e2 - 1).to(torch.int64)
+    E = torch.where(amax > 0, floor_log2 - MX_EMAX[elem], torch.full_like(floor_log2, -127)).clamp(-127, 127)
+    scaled = blocks / torch.pow(2.0, E.to(torch.float64)).to(torch.float32)[..., None]
+    if elem == MX_E4M3:
+        codes = scaled.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, K)
+    elif elem == MX_E2M1:
+        c = e2m1_codes(scaled).reshape(rows, K)
+        codes = (c[:, 0::2] | (c[:, 1::2] << 4)).to(torch.uint8)
+    else:
+        raise ValueError("unknown element type")
+    return codes.contiguous(), (E + 127).to(torch.uint8).contiguous()
+
+
+@dataclasses.dataclass
+class MXProblem:
+    """One block-scaled call: y = cast(act(alpha * A @ B + beta*C + bias)), A given as M x K
+    element codes (row pitch lda elements) with M x K/32 scales, B as its transpose, N x K
+    (pitch ldb) with N x K/32 scales."""
+
+    name: str
+    M: int
+    N: int
+    K: int
+    elem: str
+    A: torch.Tensor
+    lda: int
+    SA: torch.Tensor
+    B: torch.Tensor
+    ldb: int
+    SB: torch.Tensor
+    c_dtype: int
+    C: torch.Tensor
+    ldc: int
+    alpha: float
+    beta: float
+    bias: Optional[torch.Tensor]
+    epilogue: int
+    recipe: str
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    def oracle_args(self) -> dict:
+        return dict(M=self.M, N=self.N, K=self.K, elem=self.elem,
+                    A=self.A.numpy(), lda=self.lda, a_scale=self.SA.numpy(),
+                    B=self.B.numpy(), ldb=self.ldb, b_scale=self.SB.numpy(),
+                    C=self.C.view(CODE_VIEW[self.c_dtype]).numpy(), ldc=self.ldc, c_dtype=self.c_dtype,
+                    alpha=self.alpha, beta=self.beta,
+                    bias=None if self.bias is None else self.bias.numpy(), epilogue=self.epilogue)
+
+
+def mx_problem(seed: int, M: int, N: int, K: int, elem: str = MX_E4M3, c_dtype: int = BF16, *,
+               alpha: float = 1.0, beta: float = 0.0, epilogue: int = EPI_NONE, integer: bool = False,
+               ldc_pad: int = 0) -> MXProblem:
+    """Seeded block-scaled problem.  A, B ~ N(0, 1) quantised by mx_quantize.  With
+    ``integer``: elements are integers in [-4, 4] (exact in both element types) and
+    scales 2^-1 .. 2^1, so every product and partial sum is exact in fp32."""
+    if integer:
+        # the integers are the element values themselves; the scales alone carry 2^-1 .. 2^1
+        qa = _integer_elements(small_integers(seed, M, K, bound=4), elem)
+        qb = _integer_elements(small_integers(seed + 1, N, K, bound=4), elem)
+        sa = torch.randint(126, 129, (M, K // MX_BLOCK), generator=_gen(seed + 2)).to(torch.uint8)
+        sb = torch.randint(126, 129, (N, K // MX_BLOCK), generator=_gen(seed + 3)).to(torch.uint8)
+    else:
+        qa, sa = mx_quantize(normal(seed, M, K), elem)
+        qb, sb = mx_quantize(normal(seed + 1, N, K), elem)
+    c = normal(seed + 4, M, N) if beta != 0 else None
+    ldc = N + ldc_pad
+    C = lay_out_c(None if c is None else c.to(TORCH_DTYPE[c_dtype]), M, N, ldc, c_dtype)
+    bvec = normal(seed + 5, 1, N, std=0.1).reshape(N) if epilogue != EPI_NONE else None
+    return MXProblem(name=f"mx_{elem}_s{seed}_{M}x{N}x{K}_{DTYPE_NAME[c_dtype]}", M=M, N=N, K=K, elem=elem,
+                     A=qa.reshape(-1), lda=K, SA=sa.reshape(-1), B=qb.reshape(-1), ldb=K, SB=sb.reshape(-1),
+                     c_dtype=c_dtype, C=C, ldc=ldc, alpha=alpha, beta=beta, bias=bvec, epilogue=epilogue,
+                     recipe=f"mx {elem} seed={seed} {M}x{N}x{K} c={c_dtype} int={integer}")
+
+
+def _integer_elements(v: torch.Tensor, elem: str) -> torch.Tensor:
+    """Element codes of integer values in [-4, 4] (exact in E4M3 and E2M1), unscaled."""
+    rows, K = v.shape
+    if elem == MX_E4M3:
+        return v.to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, K).contiguous()
+    c = e2m1_codes(v)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).to(torch.uint8).contiguous()
