@@ -214,7 +214,8 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
                    bias: Optional[np.ndarray], epilogue: int,
                    rows: Optional[Sequence[int]] = None,
                    alpha_scale: Optional[np.ndarray] = None, row_scale: Optional[np.ndarray] = None,
-                   col_scale: Optional[np.ndarray] = None):
+                   col_scale: Optional[np.ndarray] = None,
+                   residual: Optional[np.ndarray] = None, ldr: int = 0, r_dtype: Optional[int] = None):
     """Reference output y (float64, not rounded to the output type) and scale D.
 
     A, B, C are raw code arrays (flat) in the given element types; ``bias`` is
@@ -229,6 +230,11 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
     from device memory; each absent one is 1): the product term becomes
     alpha * alpha_scale[0] * row_scale[i] * col_scale[j] * sum_k a_ik b_kj,
     and D's first term takes the same factors in absolute value.
+
+    Optional residual (raw codes of an M x ldr row-major array of r_dtype,
+    the output type when r_dtype is None): added after the activation,
+    y_ij = act(z_ij) + r_ij, the post-activation residual of a transformer
+    block; D takes |r_ij| too.
     """
     if min(M, N, K) < 0:
         raise ValueError("negative size")
@@ -262,6 +268,10 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
         D += np.abs(bvals)[None, :]
     act = ACTIVATIONS.get(epilogue)
     y = act(z) if act is not None else z
+    if residual is not None and R > 0 and N > 0:
+        r = decode(strided_codes(residual, M, N, ldr, 1, row_sel), c_dtype if r_dtype is None else r_dtype)
+        y = y + r
+        D += np.abs(r)
     return y, D
 
 

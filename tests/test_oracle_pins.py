@@ -506,3 +506,50 @@ def test_fp8_output_check_subnormal_range(mistake):
     ax = dict(a, c_dtype=wl.E4M3, C=codes)
     res = oracle.check_fp8_output(ax, codes, 1.0)
     assert res["pass"] == (mistake is None), res
+
+
+# ------------------------------------------------------- post-activation residual --
+
+def _residual_codes(seed, M, N, ldr, dtype):
+    """Small integers as an M x ldr array of dtype codes (padding columns hold NaN codes)."""
+    r = wl.small_integers(seed, M, N, bound=5)
+    full = torch.full((M, ldr), float("nan"))
+    full[:, :N] = r
+    return full.to(wl.TORCH_DTYPE[dtype]).view(wl.CODE_VIEW[dtype]).reshape(-1).numpy(), r
+
+
+@pytest.mark.parametrize("layout", ["NN", "TT"])
+def test_residual_after_relu_brute_force_exact(layout):
+    """y = ReLU(z) + r exactly, with z the exact rational brute force; a residual added
+    before the activation (a planted mistake) differs wherever z < 0 and r != 0.  The
+    ldr padding holds NaN and must never be read."""
+    seed = 1300
+    for M, N, K in itertools.product(range(1, 4), repeat=3):
+        seed += 3
+        p = wl.random_problem(seed, M, N, K, wl.F16, wl.F32, layout=layout, alpha=-1.5, beta=0.5,
+                              epilogue=wl.EPI_BIAS_RELU, integer=True, ldc_pad=1)
+        rc, r = _residual_codes(seed + 1, M, N, N + 2, wl.BF16)
+        y, D = oracle.gemm_reference(**p.oracle_args(), residual=rc, ldr=N + 2, r_dtype=wl.BF16)
+        y0, D0 = oracle.gemm_reference(**p.oracle_args())
+        exact = _frac_ref(p)
+        for i in range(M):
+            for j in range(N):
+                want = max(exact[i][j], Fraction(0)) + Fraction(float(r[i, j]))
+                assert Fraction(float(y[i, j])) == want, (M, N, K, i, j)
+                assert D[i, j] == D0[i, j] + abs(float(r[i, j]))
+                pre = max(exact[i][j] + Fraction(float(r[i, j])), Fraction(0))
+                if exact[i][j] < 0 and r[i, j] != 0:
+                    assert pre != want
+
+
+def test_residual_zero_and_absent_agree():
+    """A zero residual changes neither y nor D; the residual defaults to the output type."""
+    p = wl.random_problem(77, 9, 11, 40, wl.BF16, wl.F16, alpha=1.25, epilogue=wl.EPI_BIAS_GELU)
+    a = p.oracle_args()
+    zeros = np.zeros(9 * 11, np.int16)
+    y, D = oracle.gemm_reference(**a, residual=zeros, ldr=11)
+    y0, D0 = oracle.gemm_reference(**a)
+    assert np.array_equal(y, y0) and np.array_equal(D, D0)
+    ones = torch.ones(9 * 11, dtype=torch.float16).view(torch.int16).numpy()
+    y1, _ = oracle.gemm_reference(**a, residual=ones, ldr=11)
+    assert np.array_equal(y1, y0 + 1.0)
