@@ -7,15 +7,26 @@ tile scheduler, TMA producer, tcgen05 MMA, fused epilogue and store):
     accumulation, A, B ~ N(0,1)/sqrt(K), C ~ N(0,1) (seeded, synthetic).
 Metric: TFLOP/s (2*M*N*K per step) and % of the GB300 dense tensor peak.
 
-Timing: W untimed warm-up steps, then exactly K steps between a barrier +
-device synchronisation on both sides, each step bracketed by CUDA events on
-the launch stream.  Three input sets (288 MiB, more than the 129 MB L2) are
-used in rotation, so a step does not find its operands in L2.  Under torchrun
-every rank runs its own replica (no data-path collective: independent GEMMs),
-the time is the max over ranks and ``value`` is the whole job's throughput.
+Timing: W untimed warm-up steps, then exactly K steps between a device
+synchronisation on both sides, each step bracketed by CUDA events on the
+launch stream.  Three input sets (288 MiB, more than the 129 MB L2) are used
+in rotation, so a step does not find its operands in L2.
+
+The library runs on one GPU: the path needs no exchange between GPUs (output
+tiles are independent), so a multi-GPU job would be independent replicas, and
+the pair kernel's TMA multicast is meant for single-GPU processes.  The bench
+therefore refuses --gpus other than 1 and any torchrun launch with more than
+one rank.
+
+Besides the headline, the line carries one cell per workload configuration
+(each timed as its own sequence of calls: median and bootstrap 95% CI of the
+per-call TFLOP/s, inputs rotated through more than L2), the fused-vs-unfused
+bias+GELU comparison, the cheap-baseline gate, the quantized decode cells, and
+a short summary at its end.  Per-call samples of every cell go to a JSON file
+beside the line (``--samples``).
 
 ``--impl reference`` times the float64 CPU oracle on the host cores on a
-bounded row sample of the same workload instead (rank 0 only).
+bounded row sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -23,6 +34,7 @@ import argparse
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -36,6 +48,7 @@ METRIC = "GEMM TFLOP/s at 4096³ (bf16/fp16, fp8) and % of GB300 dense tensor pe
 NOMINAL_PEAK_TFLOPS = {"f16": 2250.0, "bf16": 2250.0, "e4m3": 4500.0}
 FALLBACK_BF16_TFLOPS = 1900.0
 WORKLOAD = "fp16 GEMM M=N=K=4096, C=1.5*A*B+0.5*C, fp16 out, fp32 accumulation"
+L2_BYTES = 129 * 10 ** 6  # GB300 L2 (the device property is used when a GPU is present)
 
 
 def _args(argv=None):
@@ -45,14 +58,35 @@ def _args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--size", type=int, default=4096)
-    ap.add_argument("--no-cells", action="store_true", help="skip the extra per-dtype cells")
+    ap.add_argument("--no-cells", action="store_true", help="skip the per-configuration cells")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    ap.add_argument("--samples", default=None,
+                    help="file for the per-call samples of every cell (default: gpurun_out/bench_samples.json "
+                         "when that folder exists)")
     ap.add_argument("--q4-decode", type=int, default=0, metavar="M",
                     help="only the quantized decode cell with M rows of x (for profiling); prints its JSON")
     ap.add_argument("--q4-reps", type=int, default=50, help="timed calls of the --q4-decode cell")
     ap.add_argument("--q4-kernel", choices=("auto", "ffma", "mma"), default="auto",
                     help="decode kernel of the --q4-decode cell")
     return ap.parse_args(argv)
+
+
+def workload_config(n):
+    """The headline workload's description, the same for both arms."""
+    mib = 3 * 3 * n * n * 2 / 2 ** 20
+    return {"workload": WORKLOAD, "M": n, "N": n, "K": n, "layout": "A row-major (K-major), B row-major",
+            "l2": f"3 rotating input sets ({mib:.0f} MiB, more than the 129 MB L2)", "parallelism": "single process"}
+
+
+def refuse_multi_gpu(a, env=None):
+    """The reason this process must not run (more than one GPU asked for), or None."""
+    env = os.environ if env is None else env
+    world = int(env.get("WORLD_SIZE", "1") or "1")
+    if a.gpus != 1 or world != 1:
+        return (f"bench.py runs on one GPU (asked: --gpus {a.gpus}, WORLD_SIZE {world}); the GEMM has no "
+                f"exchange between GPUs, so N GPUs would be N independent replicas, and its TMA multicast "
+                f"kernels are for single-GPU processes only")
+    return None
 
 
 # ----------------------------------------------------------------- helpers --
@@ -67,6 +101,37 @@ def bootstrap_ci(samples, reps=10000, seed=0, q=(2.5, 97.5)):
     idx = rng.integers(0, x.size, size=(reps, x.size))
     meds = np.median(x[idx], axis=1)
     return float(np.median(x)), [float(np.percentile(meds, q[0])), float(np.percentile(meds, q[1]))]
+
+
+def bimodality(samples, min_share=0.05, min_sep=4.0, min_rel=0.02):
+    """Two-mode test of per-call samples (Rigel section 3: clock states split small sizes into two
+    modes).  The best split of the sorted samples into a low and a high group (least pooled
+    variance) counts as two modes when each group holds at least `min_share` of the samples and
+    the gap between their means exceeds `min_sep` pooled standard deviations and `min_rel` of the
+    median.  Returns {"bimodal", "modes", "share"}."""
+    import numpy as np
+    x = np.sort(np.asarray(samples, dtype=np.float64))
+    n = x.size
+    if n < 10:
+        return {"bimodal": False, "modes": [float(np.median(x))] if n else [], "share": [1.0] if n else []}
+    c1, c2 = np.cumsum(x), np.cumsum(x * x)
+    best = None
+    lo_n = max(1, int(math.ceil(min_share * n)))
+    for k in range(lo_n, n - lo_n + 1):
+        m1, m2 = c1[k - 1] / k, (c1[-1] - c1[k - 1]) / (n - k)
+        v1 = c2[k - 1] / k - m1 * m1
+        v2 = (c2[-1] - c2[k - 1]) / (n - k) - m2 * m2
+        pooled = (k * max(v1, 0.0) + (n - k) * max(v2, 0.0)) / n
+        if best is None or pooled < best[0]:
+            best = (pooled, k, m1, m2)
+    pooled, k, m1, m2 = best
+    sd = math.sqrt(pooled)
+    med = float(np.median(x))
+    two = (m2 - m1) > min_sep * sd and (m2 - m1) > min_rel * abs(med)
+    if not two:
+        return {"bimodal": False, "modes": [med], "share": [1.0]}
+    return {"bimodal": True, "modes": [round(float(m1), 2), round(float(m2), 2)],
+            "share": [round(k / n, 3), round((n - k) / n, 3)]}
 
 
 def measured_peaks():
@@ -102,7 +167,9 @@ def recorded_traffic(kernel_tag):
 
 def aggregate(local_seconds, flops_per_step, steps, dist=None, device="cpu"):
     """Whole-job throughput: every rank ran `steps` steps of `flops_per_step`;
-    the job's time is the slowest rank's.  Returns (TFLOP/s, max seconds)."""
+    the job's time is the slowest rank's.  Returns (TFLOP/s, max seconds).
+    (The GEMM itself runs on one GPU; this is the aggregation rule a replica
+    job would follow, kept with its CPU test.)"""
     import torch
     world = 1
     t = float(local_seconds)
@@ -112,6 +179,42 @@ def aggregate(local_seconds, flops_per_step, steps, dist=None, device="cpu"):
         dist.all_reduce(x, op=dist.ReduceOp.MAX)
         t = float(x.item())
     return flops_per_step * steps * world / t / 1e12, t
+
+
+def provenance(problem=None):
+    """Where a number came from (Rigel section 3): source fingerprint, commit when
+    the tree has one, input recipe and its hash, device, driver, CUDA and
+    library versions, host cores."""
+    import __graft_entry__
+    out = {"sources": __graft_entry__.build_module().source_fingerprint()[:16]}
+    try:
+        r = subprocess.run(["git", "-C", REPO, "rev-parse", "--short=12", "HEAD"], capture_output=True, text=True,
+                           timeout=5)
+        if r.returncode == 0 and r.stdout.strip():
+            out["commit"] = r.stdout.strip()
+    except Exception:
+        pass
+    if problem is not None:
+        out["recipe"] = problem.recipe
+        out["recipe_hash"] = problem.recipe_hash()
+    try:
+        import torch
+        out["torch"] = torch.__version__
+        out["cuda"] = torch.version.cuda
+        if torch.cuda.is_available():
+            out["device"] = torch.cuda.get_device_name(0)
+    except Exception:
+        pass
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=10)
+        if r.returncode == 0:
+            out["driver"] = r.stdout.strip().splitlines()[0]
+    except Exception:
+        pass
+    out["host"] = platform.machine()
+    out["cores"] = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return out
 
 
 class ClockSampler:
@@ -193,44 +296,58 @@ def _workspace(g, device, nbytes=0):
     return _WS[key]
 
 
+def set_bytes(p):
+    """Device bytes of one input set of problem p (A, B, C, bias)."""
+    n = p.A.numel() * p.A.element_size() + p.B.numel() * p.B.element_size() + p.C.numel() * p.C.element_size()
+    return n + (0 if p.bias is None else p.bias.numel() * 4)
+
+
+def sets_beyond_l2(p, l2_bytes=L2_BYTES, factor=1.5, cap=160):
+    """How many input sets of p to rotate so their total exceeds factor x L2 (at least 2)."""
+    return max(2, min(cap, int(math.ceil(factor * l2_bytes / max(1, set_bytes(p))))))
+
+
 def _make_sets(problem, n_sets, device):
-    sets = []
-    for _ in range(n_sets):
-        sets.append((problem.A.to(device), problem.B.to(device), problem.C.clone().to(device),
-                     None if problem.bias is None else problem.bias.to(device)))
+    import torch
+    A, B, C = problem.A.to(device), problem.B.to(device), problem.C.to(device)
+    bias = None if problem.bias is None else problem.bias.to(device)
+    sets = [(A, B, C, bias)]
+    for _ in range(n_sets - 1):
+        sets.append((torch.empty_like(A).copy_(A), torch.empty_like(B).copy_(B), torch.empty_like(C).copy_(C),
+                     None if bias is None else torch.empty_like(bias).copy_(bias)))
     return sets
 
 
-def _call(g, p, s, stream, baseline=None):
+def _call(g, p, s, stream, baseline=None, mode="fused"):
     A, B, C, bias = s
     if baseline is not None:
         g.gemm_baseline(baseline, p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k,
                         p.b_stride_n, C, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue, stream=stream)
         return
     ws = _workspace(g, C.device, g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype))
+    epi = p.epilogue if mode == "fused" else g.EPI_NONE
     g.gemm(p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k, p.b_stride_n, C, p.ldc,
-           p.c_dtype, p.alpha, p.beta, bias, p.epilogue, workspace=ws, workspace_bytes=ws.numel(), stream=stream)
+           p.c_dtype, p.alpha, p.beta, bias, epi, workspace=ws, workspace_bytes=ws.numel(), stream=stream)
+    if mode == "decomposed":
+        # the unfused path: the plain GEMM, then the separate bias+GELU pass over C
+        g.gemm_bias_gelu(p.M, p.N, C, p.ldc, p.c_dtype, bias, stream=stream)
 
 
-def time_steps(g, p, sets, steps, warmup, stream, sampler=None, dist=None, baseline=None):
+def time_steps(g, p, sets, steps, warmup, stream, sampler=None, baseline=None, mode="fused"):
     """Warm up, then time `steps` calls; returns (per-step ms list, total ms)."""
     import torch
     for i in range(warmup):
-        _call(g, p, sets[i % len(sets)], stream, baseline)
+        _call(g, p, sets[i % len(sets)], stream, baseline, mode)
     torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     ctx = sampler if sampler is not None else _Null()
     with ctx:
         torch.cuda.synchronize()
         ev[0].record(stream)
         for i in range(steps):
-            _call(g, p, sets[i % len(sets)], stream, baseline)
+            _call(g, p, sets[i % len(sets)], stream, baseline, mode)
             ev[i + 1].record(stream)
         torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     return per, ev[0].elapsed_time(ev[steps])
 
@@ -243,16 +360,25 @@ class _Null:
         return False
 
 
-def cell(g, p, steps, warmup, stream, n_sets=3, baseline=None):
+SAMPLES = {}
+
+
+def cell(g, p, steps, warmup, stream, n_sets=None, baseline=None, mode="fused", name=None, l2=L2_BYTES):
+    """Time `steps` calls of problem p (inputs rotated through more than L2);
+    returns the median per-call TFLOP/s with its bootstrap CI.  The samples are
+    kept under `name` for the samples file."""
     import torch
+    n_sets = sets_beyond_l2(p, l2) if n_sets is None else n_sets
     sets = _make_sets(p, n_sets, torch.device("cuda", torch.cuda.current_device()))
-    per, total = time_steps(g, p, sets, steps, warmup, stream, baseline=baseline)
+    per, total = time_steps(g, p, sets, steps, warmup, stream, baseline=baseline, mode=mode)
     tf = [p.flops / (t * 1e-3) / 1e12 for t in per]
     med, ci = bootstrap_ci(tf)
     del sets
     torch.cuda.empty_cache()
-    return {"median_tflops": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)],
-            "mean_ms": round(total / steps, 5), "reps": steps}
+    if name is not None:
+        SAMPLES[name] = [round(x, 2) for x in tf]
+    return {"tflops": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)], "ms": round(total / steps, 4),
+            "n": steps}
 
 
 def describe_launch(info):
@@ -267,6 +393,29 @@ def describe_launch(info):
     if info.get("kind") == 1:
         return f"gemm_tcgen05_kernel 128x{info['bn']} tiles, {info['grid_ctas']} CTAs"
     return f"path {info.get('path')}"
+
+
+def host_link_gbs(nbytes_in, nbytes_out, reps=10):
+    """Measured pinned-host <-> device copy bandwidth (GB/s) for copies of these sizes, each
+    direction alone (the bound an end-to-end step cannot beat)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    h_in = torch.empty(nbytes_in, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes_in, dtype=torch.uint8, device=dev)
+    h_out = torch.empty(nbytes_out, dtype=torch.uint8).pin_memory()
+    d_out = torch.empty(nbytes_out, dtype=torch.uint8, device=dev)
+    res = {}
+    for name, dst, src, nb in (("h2d", d_in, h_in, nbytes_in), ("d2h", h_out, d_out, nbytes_out)):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = nb * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    return res
 
 
 def e2e_measure(g, p, steps, stream):
@@ -324,9 +473,14 @@ def e2e_measure(g, p, steps, stream):
     ms = e0.elapsed_time(e1) / steps
     h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + hC.numel() * hC.element_size()
     d2h = h_out[0].numel() * h_out[0].element_size()
+    link = host_link_gbs(h2d, d2h)
+    h2d_gbs = h2d / (ms * 1e-3) / 1e9
     return {"value": round(p.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "pipelined": "copy-in / GEMM / copy-out streams, two device buffer sets"}
+            "pipelined": "copy-in / GEMM / copy-out streams, two device buffer sets",
+            "host_link": {"h2d_gbs": round(h2d_gbs, 1), "h2d_peak_gbs": round(link["h2d"], 1),
+                          "frac": round(h2d_gbs / link["h2d"], 3), "d2h_peak_gbs": round(link["d2h"], 1),
+                          "peak_source": "pinned copies of the same sizes, each direction alone"}}
 
 
 def cpu_baseline(p, seconds, single_sample=False):
@@ -354,17 +508,9 @@ def cpu_baseline(p, seconds, single_sample=False):
 
 def run_ours(a):
     import torch
-    import torch.distributed as tdist
     import workloads as wl
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        tdist.init_process_group("nccl")
-        dist = tdist
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     import __graft_entry__
     __graft_entry__.build()
     import dense_gemm_epilogues_tcgen05_gb300 as g
@@ -373,12 +519,12 @@ def run_ours(a):
     p = wl.fp16_alpha_beta(n)
     stream = torch.cuda.current_stream()
     sets = _make_sets(p, 3, dev)
-    sampler = ClockSampler(local)
-    per, total = time_steps(g, p, sets, a.steps, a.warmup, stream, sampler=sampler, dist=dist)
+    sampler = ClockSampler(0)
+    per, total = time_steps(g, p, sets, a.steps, a.warmup, stream, sampler=sampler)
     st = g.gemm_device_status()
     if st != 0:
         raise RuntimeError(f"device status after timing: {g.gemm_status_string(st)}")
-    value, total_s = aggregate(total * 1e-3, p.flops, a.steps, dist, dev)
+    value, total_s = aggregate(total * 1e-3, p.flops, a.steps)
     tf = [p.flops / (t * 1e-3) / 1e12 for t in per]
     med, ci = bootstrap_ci(tf)
     peaks = measured_peaks()
@@ -388,12 +534,11 @@ def run_ours(a):
     kernel = describe_launch(launch)
     traffic = recorded_traffic("tcgen05_f16_4096")
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": round(total_s * 1e3 / a.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic: seeded A,B ~ N(0,1)/sqrt(K) fp16, C ~ N(0,1) fp16",
-        "config": {"workload": WORKLOAD, "M": n, "N": n, "K": n, "layout": "A row-major (K-major), B row-major",
-                   "l2": "3 rotating input sets (288 MiB > 129 MB L2)", "parallelism": f"replicas x{world}"},
+        "config": workload_config(n),
         "median_tflops": round(med, 2), "ci95": [round(ci[0], 2), round(ci[1], 2)],
         "pct_of_nominal_peak": round(100 * med / NOMINAL_PEAK_TFLOPS["f16"], 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
@@ -403,54 +548,100 @@ def run_ours(a):
         "clocks": sampler.summary(),
         "gpu_launches": a.steps,
         "launch": launch,
+        "provenance": provenance(p),
     }
-    if rank == 0:
-        out["e2e"] = e2e_measure(g, p, 30, stream)
-        del sets
-        torch.cuda.empty_cache()
-        if not a.no_cells and world == 1:
-            out["cells"] = extra_cells(g, stream)
-        out["cpu_baseline"] = cpu_baseline(p, a.cpu_seconds)
-        print(json.dumps(out), flush=True)
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
+    SAMPLES["headline"] = [round(x, 2) for x in tf]
+    out["e2e"] = e2e_measure(g, p, 30, stream)
+    del sets
+    torch.cuda.empty_cache()
+    if not a.no_cells:
+        cells, summary = extra_cells(g, stream, peaks)
+        out["cells"] = cells
+    else:
+        summary = {}
+    out["cpu_baseline"] = cpu_baseline(p, a.cpu_seconds)
+    summary["headline_tflops"] = round(value, 1)
+    summary["headline_frac"] = out["roofline"]["frac"]
+    out["summary"] = summary
+    path = a.samples
+    if path is None and os.path.isdir(os.path.join(REPO, "gpurun_out")):
+        path = os.path.join(REPO, "gpurun_out", "bench_samples.json")
+    if path:
+        try:
+            with open(path, "w") as f:
+                json.dump({"unit": "TFLOP/s per call (GB/s for q4 cells)", "samples": SAMPLES}, f)
+            out["samples_file"] = os.path.relpath(path, REPO)
+        except OSError:
+            pass
+    print(json.dumps(out), flush=True)
 
 
-def extra_cells(g, stream):
-    """Per-dtype cells of the headline metric: bf16 and fp8 at 4096^3 (fp8 against
-    its fp16 twin), bf16 8192^3, and the cost of the fused bias+GELU epilogue."""
+def extra_cells(g, stream, peaks):
+    """One cell per workload configuration (SURVEY configs 1-5), the fused-vs-unfused
+    bias+GELU comparison, the cheap-baseline gate and the quantized decode cells.
+    Returns (cells, summary); the summary repeats the per-dtype headline figures."""
+    import torch
     import workloads as wl
-    cells = {}
-    cells["bf16_4096_nn"] = cell(g, wl.bf16_nn_large(4096), 30, 5, stream)
-    cells["fp8_4096_bf16out"] = cell(g, wl.fp8_e4m3(4096), 30, 5, stream)
-    cells["fp16_twin_4096_bf16out"] = cell(g, wl.fp16_twin_of_fp8(4096), 30, 5, stream)
-    cells["fp8_over_fp16"] = round(cells["fp8_4096_bf16out"]["median_tflops"] /
-                                   cells["fp16_twin_4096_bf16out"]["median_tflops"], 3)
-    cells["bf16_8192_nn"] = cell(g, wl.bf16_nn_large(8192), 10, 3, stream, n_sets=2)
-    cells["fp32_4096_NN_3xtf32"] = cell(g, wl.fp32_layout("NN", 4096), 20, 3, stream, n_sets=2)
-    cells["fp32_4096_TT_3xtf32"] = cell(g, wl.fp32_layout("TT", 4096), 20, 3, stream, n_sets=2)
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES
+    cells, summary = {}, {}
+
+    def run(name, p, steps=30, warmup=5, **kw):
+        c = cell(g, p, steps, warmup, stream, name=name, l2=l2, **kw)
+        cells[name] = c
+        return c
+
+    # config 1: fp32 256^3 (3xTF32 with the workspace), latency-bound
+    run("fp32_256", wl.fp32_square(256), steps=100, warmup=10)
+    # config 2: fp16 alpha/beta sweep with ragged 1000^3; small sizes keep per-call samples and the two-mode test
+    for n, reps in ((512, 300), (1024, 300), (2048, 100), (1000, 100)):
+        c = run(f"fp16_{n}", wl.fp16_alpha_beta(n), steps=reps, warmup=20)
+        if n in (512, 1024):
+            c.update(bimodality(SAMPLES[f"fp16_{n}"]))
+    # config 3: fused bias+GELU against the plain GEMM and against GEMM + the separate bias+GELU pass
+    gelu_cost, fusion_gain = {}, {}
     for M in (512, 2048, 8192):
-        fused = cell(g, wl.bf16_bias_gelu(M), 30, 5, stream)
-        plain = cell(g, wl.bf16_bias_gelu(M, epilogue=wl.EPI_NONE), 30, 5, stream)
-        cells[f"gelu_M{M}"] = {"fused": fused, "none": plain,
-                               "fused_cost_pct": round(100 * (plain["median_tflops"] / fused["median_tflops"] - 1),
-                                                       2)}
-    cells["baseline_gate_fp16_4096"] = baseline_gate(g, stream)
+        p = wl.bf16_bias_gelu(M)
+        fused = cell(g, p, 30, 5, stream, name=f"gelu_M{M}_fused", l2=l2)
+        plain = cell(g, wl.bf16_bias_gelu(M, epilogue=wl.EPI_NONE), 30, 5, stream, name=f"gelu_M{M}_none", l2=l2)
+        unfused = cell(g, p, 30, 5, stream, mode="decomposed", name=f"gelu_M{M}_decomposed", l2=l2)
+        cost = round(100 * (plain["tflops"] / fused["tflops"] - 1), 2)
+        gain = round(100 * (fused["tflops"] / unfused["tflops"] - 1), 2)
+        cells[f"gelu_M{M}"] = {"fused": fused, "none": plain, "decomposed": unfused, "fused_cost_pct": cost,
+                               "fusion_gain_pct": gain}
+        gelu_cost[M], fusion_gain[M] = cost, gain
+    # config 5: fp32 layouts (3xTF32) with ldc padding, and bf16 8192^3 NN
+    for lay in ("NN", "NT", "TN", "TT"):
+        run(f"fp32_4096_{lay}", wl.fp32_layout(lay, 4096), steps=20, warmup=3)
+    cells["baseline_gate_fp16_4096"] = baseline_gate(g, stream, l2)
     for M in (1, 2, 8):
-        cells[f"q4_decode_M{M}_16384"] = q4_decode_cell(g, stream, M)
-        # the two decode kernels side by side (AUTO above picks one of them)
-        for name, kind in (("ffma", g.Q4_FFMA), ("mma", g.Q4_MMA)):
-            g.gemm_set_q4_kernel(kind)
-            try:
-                r = q4_decode_cell(g, stream, M, reps=30)
-            finally:
-                g.gemm_set_q4_kernel(g.Q4_AUTO)
-            cells[f"q4_decode_M{M}_16384"][f"kernel_{name}"] = {k: r[k] for k in ("median_gbs", "ci95", "mean_us")}
-    return cells
+        cells[f"q4_decode_M{M}"] = q4_decode_cell(g, stream, M, compact=True)
+    # config 4 (fp8 with its fp16 twins, bf16 output, and an fp32-output cell) and the large
+    # bf16 cells last, so that the tail of the line carries them
+    fp8 = {}
+    for n in (2048, 4096, 8192):
+        steps = 30 if n < 8192 else 10
+        c8 = run(f"fp8_{n}", wl.fp8_e4m3(n), steps=steps, warmup=3)
+        c16 = run(f"fp16_twin_{n}", wl.fp16_twin_of_fp8(n), steps=steps, warmup=3)
+        c8["over_fp16"] = round(c8["tflops"] / c16["tflops"], 3)
+        c8["frac_of_2x_bf16_peak"] = round(c8["tflops"] / (2 * peaks["bf16_tflops"]), 4)
+        fp8[n] = c8
+    run("fp8_4096_f32out", wl.fp8_e4m3(4096, c_dtype=wl.F32), steps=30, warmup=3)
+    bf = run("bf16_4096_nn", wl.bf16_nn_large(4096), steps=30, warmup=3)
+    b8 = run("bf16_8192_nn", wl.bf16_nn_large(8192), steps=10, warmup=3)
+    summary.update({
+        "fp16_4096_gate_cell": cells["baseline_gate_fp16_4096"]["tcgen05"]["tflops"],
+        "bf16_4096": bf["tflops"], "bf16_8192": b8["tflops"],
+        "bf16_8192_frac": round(b8["tflops"] / peaks["bf16_tflops"], 4),
+        "fp8_2048": fp8[2048]["tflops"], "fp8_4096": fp8[4096]["tflops"], "fp8_8192": fp8[8192]["tflops"],
+        "fp8_over_fp16": {n: fp8[n]["over_fp16"] for n in fp8},
+        "fp8_4096_frac_of_2x_bf16": fp8[4096]["frac_of_2x_bf16_peak"],
+        "gelu_fused_cost_pct": gelu_cost, "gelu_fusion_gain_pct": fusion_gain,
+        "q4_decode_frac": {M: cells[f"q4_decode_M{M}"]["frac"] for M in (1, 2, 8)},
+    })
+    return cells, summary
 
 
-def q4_decode_cell(g, stream, M, N=16384, K=16384, reps=50):
+def q4_decode_cell(g, stream, M, N=16384, K=16384, reps=50, compact=False):
     """Decode with 4-bit group-quantized weights (gemm_q4): M rows of x against an
     N x K weight matrix, HBM-bound.  Two weight sets (2 x 151 MB > L2) alternate;
     codes and scale/bias are seeded random (uniform codes 0..15, scales in
@@ -492,6 +683,10 @@ def q4_decode_cell(g, stream, M, N=16384, K=16384, reps=50):
     peak = measured_peaks()["hbm_gbs"]
     del sets
     torch.cuda.empty_cache()
+    SAMPLES[f"q4_decode_M{M}"] = [round(x, 1) for x in gbs]
+    if compact:
+        return {"shape": f"{M}x{N}x{K}", "gbs": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)],
+                "us": round(mean_ms * 1e3, 2), "frac": round(achieved / peak, 4), "n": reps, "status": st}
     return {"M": M, "N": N, "K": K, "bytes_per_call": nbytes, "median_gbs": round(med, 1),
             "ci95": [round(ci[0], 1), round(ci[1], 1)], "mean_us": round(mean_ms * 1e3, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -514,22 +709,21 @@ def gate_verdict(tcgen05, alu, simt, mma_sync, win=1.10):
             "threshold": win, "win": bool(ratio >= win)}
 
 
-def baseline_gate(g, stream):
+def baseline_gate(g, stream, l2=L2_BYTES):
     """The cheap-baseline gate (Rigel section 3; section 4, signal 2) on the headline
     workload: the tcgen05 kernel against (A) the CUDA-core fp16 roofline, (B) the
     SIMT kernel and (C) the warp-level mma.sync kernel, all through the C ABI."""
     import torch
     import workloads as wl
     p = wl.fp16_alpha_beta(4096)
-    tc = cell(g, p, 30, 5, stream)
-    simt = cell(g, p, 5, 1, stream, n_sets=2, baseline=g.BASELINE_SIMT)
-    ms = cell(g, p, 30, 5, stream, baseline=g.BASELINE_MMA_SYNC)
+    tc = cell(g, p, 30, 5, stream, name="gate_tcgen05", l2=l2)
+    simt = cell(g, p, 5, 1, stream, n_sets=2, baseline=g.BASELINE_SIMT, name="gate_simt", l2=l2)
+    ms = cell(g, p, 30, 5, stream, baseline=g.BASELINE_MMA_SYNC, name="gate_mma_sync", l2=l2)
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     mhz = measured_peaks()["sm_max_mhz"]
     alu = alu_fp16_roofline_tflops(sms, mhz)
-    out = {"workload": "fp16 4096^3, C = 1.5*A*B + 0.5*C", "tcgen05": tc, "simt": simt, "mma_sync": ms,
-           "alu_fp16_roofline_tflops": round(alu, 1)}
-    out.update(gate_verdict(tc["median_tflops"], alu, simt["median_tflops"], ms["median_tflops"]))
+    out = {"tcgen05": tc, "simt": simt, "mma_sync": ms, "alu_fp16_roofline_tflops": round(alu, 1)}
+    out.update(gate_verdict(tc["tflops"], alu, simt["tflops"], ms["tflops"]))
     return out
 
 
@@ -559,8 +753,7 @@ def run_reference(a):
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(1e3 * wall / a.steps, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic: seeded A,B ~ N(0,1)/sqrt(K) fp16, C ~ N(0,1) fp16",
-           "config": {"workload": WORKLOAD, "M": a.size, "N": a.size, "K": a.size,
-                      "parallelism": "host cores (oracle)"},
+           "config": workload_config(a.size),
            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
            "gpu_launches": 0}
@@ -569,15 +762,20 @@ def run_reference(a):
 
 def main(argv=None):
     a = _args(argv)
-    if a.warmup < 3 and a.impl == "ours":
+    if a.impl == "reference":
+        run_reference(a)
+        return
+    why = refuse_multi_gpu(a)
+    if why:
+        print(why, file=sys.stderr, flush=True)
+        raise SystemExit(2)
+    if a.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if a.q4_decode:
         import torch
         import dense_gemm_epilogues_tcgen05_gb300 as g
         g.gemm_set_q4_kernel({"auto": g.Q4_AUTO, "ffma": g.Q4_FFMA, "mma": g.Q4_MMA}[a.q4_kernel])
         print(json.dumps(q4_decode_cell(g, torch.cuda.current_stream(), a.q4_decode, reps=a.q4_reps)), flush=True)
-    elif a.impl == "reference":
-        run_reference(a)
     else:
         run_ours(a)
 

@@ -26,7 +26,7 @@ __all__ = [
     "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast", "gemm_last_launch",
     "BASELINE_SIMT", "BASELINE_MMA_SYNC", "gemm_baseline", "gemm_q4", "gemm_q4_dequantize", "Q4_MAX_ROWS",
     "Q4_AUTO", "Q4_FFMA", "Q4_MMA", "gemm_set_q4_kernel",
-    "gemm_ex",
+    "gemm_ex", "gemm_get_tuning",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
@@ -111,6 +111,16 @@ lib.gemm_ex.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64
                         _f32, _f32, _vp, _int, ctypes.POINTER(_Scales), _vp, _sz, _vp]
 lib.gemm_set_q4_kernel.restype = _int
 lib.gemm_set_q4_kernel.argtypes = [_int]
+
+
+class _Tuning(ctypes.Structure):
+    """gemm_tuning_t"""
+    _fields_ = [(n, _int) for n in ("tile_policy", "tile_bn", "schedule", "operand_order", "multicast",
+                                    "q4_kernel")]
+
+
+lib.gemm_get_tuning.restype = _int
+lib.gemm_get_tuning.argtypes = [ctypes.POINTER(_Tuning)]
 lib.gemm_q4.restype = _int
 lib.gemm_q4.argtypes = [_i64, _i64, _i64, _int, ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p,
                         ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
@@ -208,22 +218,23 @@ def gemm_bias_gelu(M, N, C, ldc, c_dtype, bias, stream=None) -> int:
 
 
 def gemm_set_tile_policy(policy, bn=0) -> int:
-    """Process-wide tile policy of the tcgen05 path (TILE_*); bn only with TILE_PAIR."""
+    """The calling thread's tile policy of the tcgen05 path (TILE_*); bn only with TILE_PAIR."""
     return _check(lib.gemm_set_tile_policy(policy, bn), "gemm_set_tile_policy")
 
 
 def gemm_set_schedule(schedule) -> int:
-    """Process-wide schedule of the pair kernel (SCHED_*)."""
+    """The calling thread's schedule of the pair kernel (SCHED_*)."""
     return _check(lib.gemm_set_schedule(schedule), "gemm_set_schedule")
 
 
 def gemm_set_operand_order(order) -> int:
-    """Process-wide operand order of the pair kernel (ORDER_*): whether it may compute C^T = B^T A^T."""
+    """The calling thread's operand order of the pair kernel (ORDER_*): whether it may compute C^T = B^T A^T."""
     return _check(lib.gemm_set_operand_order(order), "gemm_set_operand_order")
 
 
 def gemm_set_multicast(mode) -> int:
-    """Process-wide cluster shape of the pair kernel (MCAST_*): two SM pairs sharing A by TMA multicast, or one."""
+    """The calling thread's cluster shape of the pair kernel (MCAST_*): two SM pairs sharing A by TMA
+    multicast (only over this device's own memory), or one."""
     return _check(lib.gemm_set_multicast(mode), "gemm_set_multicast")
 
 
@@ -248,7 +259,7 @@ def gemm_ex(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_strid
 
 
 def gemm_set_q4_kernel(kind) -> int:
-    """Process-wide kernel of gemm_q4 (Q4_*): AUTO, the CUDA-core kernel, or the tensor-core one."""
+    """The calling thread's kernel of gemm_q4 (Q4_*): AUTO, the CUDA-core kernel, or the tensor-core one."""
     return _check(lib.gemm_set_q4_kernel(kind), "gemm_set_q4_kernel")
 
 
@@ -264,6 +275,13 @@ def gemm_q4_dequantize(N, K, Wq, scale_bias, W, w_dtype, stream=None) -> int:
     """W = round(s*q + b) as an N x K row-major fp16 / bf16 array (prefill: then gemm())."""
     st = lib.gemm_q4_dequantize(N, K, _ptr(Wq), _ptr(scale_bias), _ptr(W), w_dtype, _stream(stream))
     return _check(st, "gemm_q4_dequantize")
+
+
+def gemm_get_tuning() -> dict:
+    """The calling thread's tuning settings (gemm_tuning_t as a dict)."""
+    t = _Tuning()
+    _check(lib.gemm_get_tuning(ctypes.byref(t)), "gemm_get_tuning")
+    return {n: getattr(t, n) for n, _ in _Tuning._fields_}
 
 
 def gemm_last_launch() -> dict:

@@ -40,10 +40,12 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 typedef CUresult (*AddrRangeFn)(CUdeviceptr *, size_t *, CUdeviceptr);
+typedef CUresult (*PtrAttrFn)(void *, CUpointer_attribute, CUdeviceptr);
 
 struct DriverFns {
     EncodeTiledFn encode = nullptr;
     AddrRangeFn addr_range = nullptr;
+    PtrAttrFn ptr_attr = nullptr;  // optional: extents of host allocations
     bool ok = false;
 };
 
@@ -62,6 +64,11 @@ const DriverFns &driver_fns() {
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fns.addr_range = reinterpret_cast<AddrRangeFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fns.ptr_attr = reinterpret_cast<PtrAttrFn>(p);
         fns.ok = fns.encode != nullptr && fns.addr_range != nullptr;
     });
     return fns;
@@ -71,6 +78,7 @@ const DriverFns &driver_fns() {
 
 struct DeviceState {
     bool ready = false;
+    int ordinal = -1;
     int num_sms = 0;
     unsigned int *status = nullptr;
     // Resident clusters of the pair kernel by (cluster of 2 or 4 CTAs, ab incl.
@@ -93,6 +101,7 @@ gemm_status_t device_state(DeviceState **out) {
             return GEMM_ERR_CUDA;
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_gemm_status_word) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
+        d.ordinal = dev;
         d.num_sms = sms;
         d.status = static_cast<unsigned int *>(p);
         for (auto &plane : d.max_clusters)
@@ -177,10 +186,16 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int ab, const void *A, 
 
 // ------------------------------------------------------- pointer checks --
 
-// The byte range [p, p + bytes) must lie inside one device allocation, or in
-// host memory the device can address (pinned or managed).  Plain pageable
-// host pointers are rejected: a kernel given one would fault.
-gemm_status_t check_range(const void *p, size_t bytes) {
+// The byte range [p, p + bytes) must lie inside one allocation the device can
+// address: device memory, or pinned / managed host memory.  Plain pageable
+// host pointers are rejected: a kernel given one would fault.  Where the
+// driver reports the allocation's extent (device memory always; host
+// allocations where it knows them) the range must fit inside it.  When
+// `local` is given it is set to whether the range is device memory of the
+// device `ordinal` (the current one) -- the only memory a multicast tensor
+// map may cover.
+gemm_status_t check_range(const void *p, size_t bytes, int ordinal = -1, bool *local = nullptr) {
+    if (local != nullptr) *local = false;
     if (bytes == 0) return GEMM_OK;
     if (p == nullptr) return GEMM_ERR_INVALID_ARG;
     cudaPointerAttributes attr;
@@ -189,13 +204,25 @@ gemm_status_t check_range(const void *p, size_t bytes) {
         return GEMM_ERR_INVALID_ARG;
     }
     if (attr.type == cudaMemoryTypeUnregistered) return GEMM_ERR_INVALID_ARG;
-    if (attr.type != cudaMemoryTypeDevice) return GEMM_OK;
     const DriverFns &fns = driver_fns();
     CUdeviceptr base = 0;
     size_t size = 0;
-    if (fns.addr_range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return GEMM_OK;
-    const uint64_t start = reinterpret_cast<uint64_t>(p);
-    if (start < base || start + bytes > base + size) return GEMM_ERR_INVALID_ARG;
+    if (attr.type == cudaMemoryTypeDevice) {
+        if (fns.addr_range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) size = 0;
+    } else if (fns.ptr_attr != nullptr) {
+        // pinned or managed host memory: its extent as the driver recorded it, if it did
+        void *start = nullptr;
+        if (fns.ptr_attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, reinterpret_cast<CUdeviceptr>(p)) !=
+                CUDA_SUCCESS ||
+            fns.ptr_attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS)
+            size = 0;
+        base = reinterpret_cast<CUdeviceptr>(start);
+    }
+    if (size > 0) {
+        const uint64_t first = reinterpret_cast<uint64_t>(p);
+        if (first < base || first + bytes > base + size) return GEMM_ERR_INVALID_ARG;
+    }
+    if (local != nullptr) *local = attr.type == cudaMemoryTypeDevice && attr.device == ordinal;
     return GEMM_OK;
 }
 
@@ -290,12 +317,18 @@ size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 // ------------------------------------------------------------ tile choice --
 
-std::atomic<int> g_tile_policy{GEMM_TILE_AUTO};
-std::atomic<int> g_tile_policy_bn{0};
-std::atomic<int> g_schedule{GEMM_SCHED_AUTO};
-std::atomic<int> g_operand_order{GEMM_ORDER_AUTO};
-std::atomic<int> g_multicast{GEMM_MCAST_AUTO};
-std::atomic<int> g_q4_kernel{GEMM_Q4_AUTO};
+// Tuning settings (gemm_set_*): each thread has its own, so a test or tuning
+// call in one thread never changes the kernel another thread's call runs.
+struct Tuning {
+    int tile_policy = GEMM_TILE_AUTO;
+    int tile_policy_bn = 0;
+    int schedule = GEMM_SCHED_AUTO;
+    int operand_order = GEMM_ORDER_AUTO;
+    int multicast = GEMM_MCAST_AUTO;
+    int q4_kernel = GEMM_Q4_AUTO;
+};
+thread_local Tuning t_tuning;
+
 std::atomic<unsigned int> g_epoch{0};
 
 // The calling thread's last successful gemm() launch (gemm_last_launch).
@@ -614,7 +647,7 @@ size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtyp
 
 gemm_status_t gemm_set_schedule(gemm_schedule_t schedule) {
     if (schedule < GEMM_SCHED_AUTO || schedule > GEMM_SCHED_STREAM_K) return GEMM_ERR_INVALID_ARG;
-    g_schedule.store(schedule);
+    t_tuning.schedule = schedule;
     return GEMM_OK;
 }
 
@@ -662,8 +695,11 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
     if (plan.path == GEMM_PATH_EPILOGUE_ONLY)
         return record(launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA, info);
 
-    if ((st = check_range(A, span_bytes(M, K, a_stride_m, a_stride_k, es))) != GEMM_OK) return st;
-    if ((st = check_range(B, span_bytes(K, N, b_stride_k, b_stride_n, es))) != GEMM_OK) return st;
+    bool a_local = false, b_local = false;  // device memory of this device (multicast needs it)
+    if ((st = check_range(A, span_bytes(M, K, a_stride_m, a_stride_k, es), dev->ordinal, &a_local)) != GEMM_OK)
+        return st;
+    if ((st = check_range(B, span_bytes(K, N, b_stride_k, b_stride_n, es), dev->ordinal, &b_local)) != GEMM_OK)
+        return st;
 
     if (plan.path == GEMM_PATH_SIMT && ab_dtype == GEMM_F32) {
         // fp32 inputs: 3xTF32 on the tensor cores when the caller's workspace
@@ -694,19 +730,19 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
     CUtensorMap tcm;
     std::memset(&tcm, 0, sizeof(tcm));
     const bool c_tma = !direct_c && encode_c(&tcm, c_dtype, C, M, N, ldc);
-    const int order = g_operand_order.load();
+    const int order = t_tuning.operand_order;
     bool swap = c_tma && c_dtype != GEMM_F32 && order != GEMM_ORDER_AS_GIVEN &&
                 (order == GEMM_ORDER_TRANSPOSED ||
                  (plan.b.mn_major && !plan.a.mn_major && ab_dtype != GEMM_E4M3));
     TileChoice tc;
     if (swap) {
-        tc = choose_tile(N, M, dev->num_sms, max_clusters, g_tile_policy.load(), g_tile_policy_bn.load());
+        tc = choose_tile(N, M, dev->num_sms, max_clusters, t_tuning.tile_policy, t_tuning.tile_policy_bn);
         if (tc.kind != 2) swap = false;  // the one-SM kernel runs the problem as given
     }
     if (!swap) {
         // E4M3 outputs are built for the pair kernel only.
-        const int policy = c_dtype == GEMM_E4M3 ? GEMM_TILE_PAIR : g_tile_policy.load();
-        tc = choose_tile(M, N, dev->num_sms, max_clusters, policy, g_tile_policy_bn.load());
+        const int policy = c_dtype == GEMM_E4M3 ? GEMM_TILE_PAIR : t_tuning.tile_policy;
+        tc = choose_tile(M, N, dev->num_sms, max_clusters, policy, t_tuning.tile_policy_bn);
     }
     // The kernel's problem: Mk x Nk, first operand (Mk x K), second (Nk x K).
     const int64_t Mk = swap ? N : M, Nk = swap ? M : N;
@@ -718,12 +754,17 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
     // The second operand's box covers this SM's columns: the whole tile (one SM) or half of it (pair).
     const uint32_t b_box = static_cast<uint32_t>(tc.kind == 2 ? tc.bn / 2 : tc.bn);
     // Pair kernel: clusters of one pair, or of two pairs that each fetch half
-    // of a CTA's A rows (a 64-row box when A is K-contiguous).
+    // of a CTA's A rows (a 64-row box when A is K-contiguous) and multicast
+    // them.  A multicast tensor map covers only this device's own memory: the
+    // kernel's first operand must be a device allocation of the current
+    // device, or the call runs one-pair clusters (no multicast).
     int cl = 2, max_quads = 0;
     if (tc.kind == 2) {
-        const int mode = g_multicast.load();
+        const int mode = t_tuning.multicast;
         const bool a_splits = !op1.mn_major || es == 2;
-        if (mode != GEMM_MCAST_OFF && a_splits) max_quads = device_max_clusters(dev, ab_dtype, c_dtype, 4);
+        const bool op1_local = swap ? b_local : a_local;
+        if (mode != GEMM_MCAST_OFF && a_splits && op1_local)
+            max_quads = device_max_clusters(dev, ab_dtype, c_dtype, 4);
         cl = choose_cluster(tiles_m * tiles_n, tiles_n, max_clusters, max_quads, a_splits, mode);
     }
     const uint32_t a_box = cl == 4 ? 64u : 128u;
@@ -775,7 +816,7 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
         const bool have_ws = workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 &&
                              workspace_bytes >= workspace_bytes_for(slot_pairs);
         int clusters = 0;
-        choose_schedule(t.num_tiles, t.num_kb, max_units, have_ws, g_schedule.load(), t.bn, &t.dp_tiles,
+        choose_schedule(t.num_tiles, t.num_kb, max_units, have_ws, t_tuning.schedule, t.bn, &t.dp_tiles,
                         &t.sk_units, t.sk_cut, &clusters);
         if (t.sk_units > 0) {
             if ((st = check_range(workspace, workspace_bytes_for(slot_pairs))) != GEMM_OK) return st;
@@ -820,21 +861,21 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, const
 
 gemm_status_t gemm_set_operand_order(gemm_operand_order_t order) {
     if (order < GEMM_ORDER_AUTO || order > GEMM_ORDER_TRANSPOSED) return GEMM_ERR_INVALID_ARG;
-    g_operand_order.store(order);
+    t_tuning.operand_order = order;
     return GEMM_OK;
 }
 
 gemm_status_t gemm_set_multicast(gemm_multicast_t mode) {
     if (mode < GEMM_MCAST_AUTO || mode > GEMM_MCAST_ON) return GEMM_ERR_INVALID_ARG;
-    g_multicast.store(mode);
+    t_tuning.multicast = mode;
     return GEMM_OK;
 }
 
 gemm_status_t gemm_set_tile_policy(gemm_tile_policy_t policy, int bn) {
     if (policy < GEMM_TILE_AUTO || policy > GEMM_TILE_PAIR) return GEMM_ERR_INVALID_ARG;
     if (bn != 0 && (policy != GEMM_TILE_PAIR || bn < 128 || bn > 256 || bn % 32 != 0)) return GEMM_ERR_INVALID_ARG;
-    g_tile_policy_bn.store(bn);
-    g_tile_policy.store(policy);
+    t_tuning.tile_policy_bn = bn;
+    t_tuning.tile_policy = policy;
     return GEMM_OK;
 }
 
@@ -848,8 +889,8 @@ gemm_status_t gemm_query_tile(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_d
     gemm_status_t st = device_state(&dev);
     if (st != GEMM_OK) return st;
     const int max_clusters = device_max_clusters(dev, ab_dtype, c_dtype);
-    const TileChoice tc = choose_tile(M, N, dev->num_sms, max_clusters, g_tile_policy.load(),
-                                      g_tile_policy_bn.load());
+    const TileChoice tc = choose_tile(M, N, dev->num_sms, max_clusters, t_tuning.tile_policy,
+                                      t_tuning.tile_policy_bn);
     *kind = tc.kind;
     *bn = tc.bn;
     *units = tc.kind == 2 ? max_clusters : dev->num_sms;
@@ -918,7 +959,18 @@ bool q4_auto_mma(int64_t M) { return M >= 2; }
 
 gemm_status_t gemm_set_q4_kernel(gemm_q4_kernel_t kind) {
     if (kind < GEMM_Q4_AUTO || kind > GEMM_Q4_MMA) return GEMM_ERR_INVALID_ARG;
-    g_q4_kernel.store(kind);
+    t_tuning.q4_kernel = kind;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_get_tuning(gemm_tuning_t *out) {
+    if (out == nullptr) return GEMM_ERR_INVALID_ARG;
+    out->tile_policy = t_tuning.tile_policy;
+    out->tile_bn = t_tuning.tile_policy_bn;
+    out->schedule = t_tuning.schedule;
+    out->operand_order = t_tuning.operand_order;
+    out->multicast = t_tuning.multicast;
+    out->q4_kernel = t_tuning.q4_kernel;
     return GEMM_OK;
 }
 
@@ -963,7 +1015,7 @@ gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, con
     a.Wq = Wq;
     a.SB = static_cast<const uint32_t *>(scale_bias);
     a.status = dev->status;
-    const int kind = g_q4_kernel.load();
+    const int kind = t_tuning.q4_kernel;
     if (!(kind == GEMM_Q4_MMA || (kind == GEMM_Q4_AUTO && q4_auto_mma(M))))
         return launch_q4_gemv(x_dtype, c_dtype, nullptr, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     // The tensor-core kernel's weight boxes: 32 rows x min(160, K/2) bytes of codes.

@@ -190,7 +190,7 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K,
  */
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype);
 
-/* How the tcgen05 pair kernel distributes tiles (process-wide). */
+/* How the tcgen05 pair kernel distributes tiles (a per-thread setting). */
 typedef enum {
     GEMM_SCHED_AUTO = 0,     /* stream-K for the last waves when the tiles do not divide evenly */
     GEMM_SCHED_TILES = 1,    /* whole tiles only */
@@ -198,10 +198,10 @@ typedef enum {
 } gemm_schedule_t;
 
 /*
- * gemm_set_schedule -- schedule of later gemm() calls on the pair kernel, for
- * every thread of the process (stream-K still needs a large enough
- * workspace).  Meant for tuning and tests.  GEMM_ERR_INVALID_ARG for an
- * unknown value; never touches the device.
+ * gemm_set_schedule -- schedule of the calling thread's later gemm() calls on
+ * the pair kernel (stream-K still needs a large enough workspace); other
+ * threads keep their own setting.  Meant for tuning and tests.
+ * GEMM_ERR_INVALID_ARG for an unknown value; never touches the device.
  */
 gemm_status_t gemm_set_schedule(gemm_schedule_t schedule);
 
@@ -224,9 +224,10 @@ typedef enum {
 } gemm_operand_order_t;
 
 /*
- * gemm_set_operand_order -- operand order of later gemm() calls on the pair
- * kernel, for every thread of the process.  Meant for tuning and tests.
- * GEMM_ERR_INVALID_ARG for an unknown value; never touches the device.
+ * gemm_set_operand_order -- operand order of the calling thread's later
+ * gemm() calls on the pair kernel; other threads keep their own setting.
+ * Meant for tuning and tests.  GEMM_ERR_INVALID_ARG for an unknown value;
+ * never touches the device.
  */
 gemm_status_t gemm_set_operand_order(gemm_operand_order_t order);
 
@@ -245,6 +246,12 @@ gemm_status_t gemm_set_operand_order(gemm_operand_order_t order);
  * two-pair clusters wherever A splits, even with an odd number of tile
  * columns (the last pair then computes a tile outside the matrix and stores
  * nothing).
+ *
+ * A multicast load's tensor map may cover only the calling GPU's own memory:
+ * the pair kernel's first operand (A, or B when it computes C^T = B^T A^T)
+ * must be a device allocation of the current device, else the call runs
+ * one-pair clusters whatever the setting (pinned host memory or another
+ * GPU's memory is read by plain per-CTA TMA loads).
  */
 typedef enum {
     GEMM_MCAST_AUTO = 0,   /* two-pair clusters where they measured faster (above) */
@@ -253,9 +260,10 @@ typedef enum {
 } gemm_multicast_t;
 
 /*
- * gemm_set_multicast -- cluster shape of later gemm() calls on the pair
- * kernel, for every thread of the process.  Meant for tuning and tests.
- * GEMM_ERR_INVALID_ARG for an unknown value; never touches the device.
+ * gemm_set_multicast -- cluster shape of the calling thread's later gemm()
+ * calls on the pair kernel; other threads keep their own setting.  Meant for
+ * tuning and tests.  GEMM_ERR_INVALID_ARG for an unknown value; never touches
+ * the device.
  */
 gemm_status_t gemm_set_multicast(gemm_multicast_t mode);
 
@@ -274,7 +282,7 @@ gemm_status_t gemm_query_path(int64_t M, int64_t N, int64_t K,
                               const float *bias, gemm_epilogue_t epilogue,
                               gemm_path_t *path);
 
-/* Tile policy of the tcgen05 path (process-wide; see gemm_set_tile_policy). */
+/* Tile policy of the tcgen05 path (a per-thread setting; see gemm_set_tile_policy). */
 typedef enum {
     GEMM_TILE_AUTO = 0,     /* cost model: wave balance over the SMs and shared-memory bandwidth */
     GEMM_TILE_1SM_256 = 1,  /* one SM per 128 x 256 output tile */
@@ -283,8 +291,9 @@ typedef enum {
 } gemm_tile_policy_t;
 
 /*
- * gemm_set_tile_policy -- choose how later gemm() calls tile the output on the
- * tcgen05 path, for every thread of the process.  `bn` is used with
+ * gemm_set_tile_policy -- choose how the calling thread's later gemm() calls
+ * tile the output on the tcgen05 path; other threads keep their own setting.
+ * `bn` is used with
  * GEMM_TILE_PAIR only: a multiple of 32 in 128..256, or 0 to let the cost
  * model pick the width.  Meant for tuning and tests; GEMM_TILE_AUTO (the
  * default) is the right choice otherwise.  Returns GEMM_ERR_INVALID_ARG for an
@@ -421,11 +430,31 @@ typedef enum {
 } gemm_q4_kernel_t;
 
 /*
- * gemm_set_q4_kernel -- kernel of later gemm_q4() calls, for every thread of
- * the process.  Meant for tuning and tests.  GEMM_ERR_INVALID_ARG for an
- * unknown value; never touches the device.
+ * gemm_set_q4_kernel -- kernel of the calling thread's later gemm_q4() calls;
+ * other threads keep their own setting.  Meant for tuning and tests.
+ * GEMM_ERR_INVALID_ARG for an unknown value; never touches the device.
  */
 gemm_status_t gemm_set_q4_kernel(gemm_q4_kernel_t kind);
+
+/*
+ * The calling thread's tuning settings, as the gemm_set_* calls left them
+ * (every thread starts with all of them AUTO and bn 0).  No counterpart on
+ * the pages.
+ */
+typedef struct {
+    int tile_policy;    /* gemm_tile_policy_t */
+    int tile_bn;        /* pair tile width forced with GEMM_TILE_PAIR, 0 = cost model */
+    int schedule;       /* gemm_schedule_t */
+    int operand_order;  /* gemm_operand_order_t */
+    int multicast;      /* gemm_multicast_t */
+    int q4_kernel;      /* gemm_q4_kernel_t */
+} gemm_tuning_t;
+
+/*
+ * gemm_get_tuning -- copy the calling thread's settings into *out (host
+ * pointer).  GEMM_ERR_INVALID_ARG for out == NULL; touches no device.
+ */
+gemm_status_t gemm_get_tuning(gemm_tuning_t *out);
 
 /*
  * gemm_q4_dequantize -- W[n][k] = round(s*q + b) into the N x K row-major

@@ -39,7 +39,7 @@ def test_header_declares_the_entry_points():
     assert {"gemm", "gemm_workspace_size", "gemm_query_path", "gemm_bias_gelu", "gemm_device_status",
             "gemm_status_string", "gemm_version", "gemm_set_tile_policy", "gemm_query_tile",
             "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest", "gemm_set_multicast",
-            "gemm_last_launch", "gemm_q4", "gemm_set_q4_kernel"} <= names
+            "gemm_last_launch", "gemm_q4", "gemm_set_q4_kernel", "gemm_get_tuning"} <= names
 
 
 def test_library_exports_every_declared_symbol(g):
@@ -109,6 +109,40 @@ def test_multicast_validation(g):
         with pytest.raises(g.GemmError):
             g.gemm_set_multicast(v)
     g.gemm_set_multicast(g.MCAST_AUTO)
+
+
+def test_tuning_settings_are_per_thread(g):
+    """A setting made in one thread leaves every other thread on AUTO (its own defaults)."""
+    import threading
+    auto = {"tile_policy": g.TILE_AUTO, "tile_bn": 0, "schedule": g.SCHED_AUTO, "operand_order": g.ORDER_AUTO,
+            "multicast": g.MCAST_AUTO, "q4_kernel": g.Q4_AUTO}
+    assert g.gemm_get_tuning() == auto
+    seen = {}
+    ready, release = threading.Event(), threading.Event()
+
+    def tuner():
+        g.gemm_set_tile_policy(g.TILE_PAIR, 192)
+        g.gemm_set_schedule(g.SCHED_STREAM_K)
+        g.gemm_set_operand_order(g.ORDER_TRANSPOSED)
+        g.gemm_set_multicast(g.MCAST_OFF)
+        g.gemm_set_q4_kernel(g.Q4_MMA)
+        seen["tuner"] = g.gemm_get_tuning()
+        ready.set()
+        release.wait(10)
+
+    def other():
+        ready.wait(10)
+        seen["other"] = g.gemm_get_tuning()
+
+    t1, t2 = threading.Thread(target=tuner), threading.Thread(target=other)
+    t1.start(); t2.start()
+    t2.join(10)
+    release.set()
+    t1.join(10)
+    assert seen["tuner"] == {"tile_policy": g.TILE_PAIR, "tile_bn": 192, "schedule": g.SCHED_STREAM_K,
+                             "operand_order": g.ORDER_TRANSPOSED, "multicast": g.MCAST_OFF, "q4_kernel": g.Q4_MMA}
+    assert seen["other"] == auto
+    assert g.gemm_get_tuning() == auto  # this thread too
 
 
 # Fake, aligned device addresses: query_path never dereferences them.

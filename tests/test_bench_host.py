@@ -129,3 +129,50 @@ def test_baseline_gate_arithmetic():
     assert v["win"] is False and v["over_strongest"] == 1.05
     # the strongest explanation may be the roofline itself
     assert bench.gate_verdict(170.0, 161.1, 30.0, 100.0)["over_strongest"] == round(170.0 / 161.1, 3)
+
+
+def test_bench_refuses_more_than_one_gpu():
+    """The library is single-GPU (the pair kernel's TMA multicast is for single-GPU processes):
+    bench.py exits with an error for --gpus 2 or a multi-rank launch, before touching a GPU."""
+    for argv, env in ((["--gpus", "2"], {}), (["--gpus", "1"], {"WORLD_SIZE": "2", "RANK": "0"})):
+        r = subprocess.run([sys.executable, os.path.join(REPO, "bench.py"), "--steps", "3", "--warmup", "3"] + argv,
+                           capture_output=True, text=True, timeout=120, cwd=REPO, env=dict(os.environ, **env))
+        assert r.returncode == 2, (r.returncode, r.stderr)
+        assert "one GPU" in r.stderr and r.stdout.strip() == ""
+    a = bench._args(["--gpus", "1"])
+    assert bench.refuse_multi_gpu(a, env={}) is None
+    assert bench.refuse_multi_gpu(a, env={"WORLD_SIZE": "4"}) is not None
+
+
+def test_bench_has_no_collective_backend():
+    """No NCCL process group: nothing in the timed path talks to another GPU."""
+    text = open(os.path.join(REPO, "bench.py")).read()
+    assert 'init_process_group("nccl")' not in text and "init_process_group('nccl')" not in text
+
+
+def test_bimodality_flags_two_clock_states():
+    rng = np.random.default_rng(3)
+    two = np.concatenate([rng.normal(4.65, 0.05, 145), rng.normal(6.5, 0.05, 155)])
+    r = bench.bimodality(two)
+    assert r["bimodal"] and r["modes"][0] == pytest.approx(4.65, abs=0.05) and r["share"][0] == pytest.approx(
+        145 / 300, abs=0.01)
+    assert not bench.bimodality(rng.normal(100.0, 1.0, 300))["bimodal"]
+    # a few stragglers (under 5 %) are not a second mode
+    assert not bench.bimodality(np.concatenate([rng.normal(100, 0.5, 295), [60.0] * 5]))["bimodal"]
+
+
+def test_reference_arm_shares_the_workload_config():
+    r = subprocess.run([sys.executable, os.path.join(REPO, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "1", "--size", "256", "--cpu-seconds", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=REPO)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["config"] == bench.workload_config(256)
+
+
+def test_cells_rotate_inputs_beyond_l2():
+    import workloads as wl
+    p = wl.fp16_alpha_beta(512)
+    n = bench.sets_beyond_l2(p, l2_bytes=129 * 10 ** 6)
+    assert n * bench.set_bytes(p) > 129 * 10 ** 6
+    assert bench.sets_beyond_l2(wl.fp32_square(256)) >= 2

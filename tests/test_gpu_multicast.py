@@ -166,3 +166,42 @@ def test_launch_record_fp32_paths(cuda_lib):
     run_gemm(g, p, use_workspace=False)
     info = g.gemm_last_launch()
     assert info["path"] == g.PATH_SIMT and info["tf32x3"] == 0 and info["grid_ctas"] == 0
+
+
+def _run_placed(g, p, pinned):
+    """Run p with the operands named in `pinned` ("A", "B") in pinned host memory, the rest on the device."""
+    A = p.A.pin_memory() if "A" in pinned else p.A.cuda()
+    B = p.B.pin_memory() if "B" in pinned else p.B.cuda()
+    C = p.C.clone().cuda()
+    ws = torch.empty(g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype), dtype=torch.uint8, device="cuda")
+    g.gemm(p.M, p.N, p.K, p.ab_dtype, A, p.a_stride_m, p.a_stride_k, B, p.b_stride_k, p.b_stride_n, C, p.ldc,
+           p.c_dtype, p.alpha, p.beta, None, p.epilogue, workspace=ws, workspace_bytes=ws.numel())
+    info = g.gemm_last_launch()
+    assert g.gemm_device_status() == 0
+    torch.cuda.synchronize()
+    return info, oracle.output_values(C.cpu().view(wl.CODE_VIEW[p.c_dtype]).numpy(), p.M, p.N, p.ldc, p.c_dtype)
+
+
+@pytest.mark.parametrize("pinned, order, want_cl", [
+    ("A", "given", 2),        # the multicast operand is host memory: one-pair clusters
+    ("B", "given", 4),        # B is not multicast; A (device memory) may be
+    ("B", "transposed", 2),   # C^T = B^T A^T: B is now the multicast operand
+    ("", "given", 4),         # both on the device
+])
+def test_multicast_only_over_this_devices_memory(cuda_lib, mcast_on, pinned, order, want_cl):
+    """A multicast tensor map covers only this GPU's own memory: when the pair kernel's first
+    operand lives in pinned host memory the call runs one-pair clusters even under MCAST_ON, and
+    the result is the same exact product."""
+    g = cuda_lib
+    g.gemm_set_operand_order(g.ORDER_AS_GIVEN if order == "given" else g.ORDER_TRANSPOSED)
+    c_dtype = wl.F32 if order == "given" else wl.BF16  # the transposed order needs a 16-bit output
+    p = wl.random_problem(431, 512, 1024, 320, wl.BF16, c_dtype, alpha=1.0, beta=0.0, integer=True)
+    info, got = _run_placed(g, p, pinned)
+    assert info["kind"] == 2 and info["transposed"] == (order == "transposed")
+    assert info["cluster_ctas"] == want_cl
+    y, _ = oracle.gemm_reference(**p.oracle_args())
+    if c_dtype == wl.F32:
+        assert np.array_equal(got, y)
+    else:
+        want = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float32).to(torch.bfloat16)
+        assert np.array_equal(got, want.to(torch.float64).numpy())
