@@ -103,7 +103,8 @@ lib.gemm_last_launch.argtypes = [ctypes.POINTER(_LaunchInfo)]
 class _Scales(ctypes.Structure):
     """gemm_scales_t"""
     _fields_ = [("alpha_scale", ctypes.c_void_p), ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p),
-                ("out_scale", ctypes.c_void_p), ("amax", ctypes.c_void_p)]
+                ("out_scale", ctypes.c_void_p), ("amax", ctypes.c_void_p), ("residual", ctypes.c_void_p),
+                ("ldr", ctypes.c_int64)]
 
 
 lib.gemm_ex.restype = _int
@@ -248,10 +249,12 @@ def gemm_baseline(kind, M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_strid
 
 def gemm_ex(M, N, K, ab_dtype, A, a_stride_m, a_stride_k, B, b_stride_k, b_stride_n, C, ldc, c_dtype,
             alpha, beta, bias, epilogue, alpha_scale=None, row_scale=None, col_scale=None, out_scale=None,
-            amax=None, workspace=None, workspace_bytes=0, stream=None) -> int:
+            amax=None, residual=None, ldr=0, workspace=None, workspace_bytes=0, stream=None) -> int:
     """gemm() with scales (device fp32 arrays: alpha_scale[1], row_scale[M], col_scale[N], out_scale[1] for
-    an E4M3 output, amax[1] raised to max |y|; None = absent)."""
-    sc = _Scales(_ptr(alpha_scale), _ptr(row_scale), _ptr(col_scale), _ptr(out_scale), _ptr(amax))
+    an E4M3 output, amax[1] raised to max |y|) and a post-activation residual (M x ldr array of the output
+    type, added after the activation); None = absent."""
+    sc = _Scales(_ptr(alpha_scale), _ptr(row_scale), _ptr(col_scale), _ptr(out_scale), _ptr(amax),
+                 _ptr(residual), ldr)
     st = lib.gemm_ex(M, N, K, ab_dtype, _ptr(A), a_stride_m, a_stride_k, _ptr(B), b_stride_k, b_stride_n,
                      _ptr(C), ldc, c_dtype, alpha, beta, _ptr(bias), epilogue, ctypes.byref(sc), _ptr(workspace),
                      workspace_bytes, _stream(stream))

@@ -2,6 +2,7 @@
 //
 // For each output element the accumulator `acc` (fp32) becomes
 //     z = alpha*acc + beta*C_in + bias[j];  y = GELU(z) (bias+GELU only);
+//     y += R[i][j] (post-activation residual, extended calls only);
 //     C[i][j] = round_to_nearest_even(y) in the output type
 // applied in registers before the single store ("Case Study: Steel's
 // BlockMMA", the paragraph on store_result / apply_epilogue; "Case Study: The
@@ -237,17 +238,27 @@ __device__ __forceinline__ void amax_push(float local, float *amax) {
         atomicMax(reinterpret_cast<unsigned int *>(amax), v);
 }
 
-// Scalar epilogue of one element (used by the safe path and the SIMT kernel).
-// Returns the activated value before any output scaling (for amax).
+// Residual row `row` of the output (NULL without a residual).
+template <int OUT>
+__device__ __forceinline__ const typename Elem<OUT>::T *residual_row(const EpiParams &e, int row) {
+    return e.residual ? reinterpret_cast<const typename Elem<OUT>::T *>(e.residual) + (long long)row * e.ldr
+                      : nullptr;
+}
+
+// Scalar epilogue of one element (used by the safe path and the SIMT kernel);
+// `r` is the element's residual (NULL: none).  Returns the activated value
+// (plus the residual) before any output scaling (for amax).
 template <int OUT>
 __device__ __forceinline__ float epilogue_store_one(float acc, typename Elem<OUT>::T *c, float bias_j,
-                                                    const EpiParams &e) {
+                                                    const EpiParams &e,
+                                                    const typename Elem<OUT>::T *r = nullptr) {
     float z = e.alpha * acc;
     if constexpr (OUT != kDtE4M3) {
         if (e.beta != 0.0f) z = fmaf(e.beta, Elem<OUT>::load(c), z);  // E4M3 outputs are written only
     }
     if (e.epilogue != kEpiNone) z += bias_j;
     z = activate(z, e.epilogue);
+    if (r != nullptr) z += Elem<OUT>::load(r);
     if constexpr (OUT == kDtE4M3)
         *c = Elem<OUT>::cvt(e.out_scale ? z / *e.out_scale : z);
     else
@@ -336,12 +347,34 @@ template <> struct Vec16<kDtE4M3> {
     }
 };
 
+// Add the residual of 32 in-range columns (rchunk: their first element).
+template <int OUT>
+__device__ __forceinline__ void add_residual32(float (&v)[32], const typename Elem<OUT>::T *rchunk,
+                                               const EpiParams &e) {
+    constexpr int PV = Vec16<OUT>::kPerVec;
+    if (e.r_vec) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(rchunk);
+#pragma unroll
+        for (int q = 0; q < 32 / PV; ++q) {
+            float r[PV];
+            Vec16<OUT>::unpack(__ldg(src + q), r);
+#pragma unroll
+            for (int t = 0; t < PV; ++t) v[q * PV + t] += r[t];
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += Elem<OUT>::load(rchunk + j);
+    }
+}
+
 // Fast path: 32 in-range columns of one row, C and bias 16-byte aligned.
 // `bias_chunk` may point to global or shared memory (generic loads).  With SC,
-// also the amax reduction and (E4M3 output) the output scale.
+// also the residual (rchunk: R at the chunk's first column, or NULL), the amax
+// reduction and (E4M3 output) the output scale.
 template <int OUT, bool SC = true>
 __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename Elem<OUT>::T *crow,
-                                                      const float *bias_chunk, const EpiParams &e) {
+                                                      const float *bias_chunk, const EpiParams &e,
+                                                      const typename Elem<OUT>::T *rchunk = nullptr) {
     constexpr int PV = Vec16<OUT>::kPerVec;
     constexpr int NV = 32 / PV;
     const uint64_t alpha2 = f2_splat(e.alpha);
@@ -373,6 +406,7 @@ __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename E
         }
     }
     if constexpr (SC) {
+        if (rchunk != nullptr) add_residual32<OUT>(v, rchunk, e);
         if (e.amax) {
             float m = 0.0f;
 #pragma unroll
@@ -392,16 +426,19 @@ __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename E
     for (int q = 0; q < NV; ++q) dst[q] = Vec16<OUT>::pack(&v[q * PV]);
 }
 
-// Safe path: columns col0 .. col0+31, of which only those < N are touched.
+// Safe path: columns col0 .. col0+31, of which only those < N are touched
+// (rchunk: the residual at column col0, or NULL).
 template <int OUT, bool SC = true>
 __device__ __forceinline__ void epilogue_chunk32_safe(const float (&v)[32], typename Elem<OUT>::T *crow, int col0,
-                                                      const EpiParams &e) {
+                                                      const EpiParams &e,
+                                                      const typename Elem<OUT>::T *rchunk = nullptr) {
     float m = 0.0f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         if (col0 + j < e.N) {
             const float b = (e.epilogue != kEpiNone) ? e.bias[col0 + j] : 0.0f;
-            m = fmaxf(m, fabsf(epilogue_store_one<OUT>(v[j], crow + j, b, e)));
+            const typename Elem<OUT>::T *r = (SC && rchunk != nullptr) ? rchunk + j : nullptr;
+            m = fmaxf(m, fabsf(epilogue_store_one<OUT>(v[j], crow + j, b, e, r)));
         }
     }
     if constexpr (SC) {
@@ -421,6 +458,7 @@ __device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_bas
     using OutT = typename Elem<OUT>::T;
     if (nvalid <= 0) return;
     OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
+    const OutT *rrow = (SC && row_ok) ? residual_row<OUT>(e, row) : nullptr;
     uint32_t ra[32], rb[32];
     __syncwarp();
     tmem_ld_issue(t_base, ra);
@@ -438,10 +476,11 @@ __device__ __forceinline__ void epilogue_row_chunks(uint32_t t_base, int col_bas
         const int col0 = col_base + i * 32;
         product_scale_chunk<SC>(v, e, row, col0, false);
         if (row_ok) {
+            const OutT *rchunk = rrow != nullptr ? rrow + col0 : nullptr;
             if (e.c_vec && col0 + 32 <= e.N)
-                epilogue_chunk32_fast<OUT, SC>(v, crow + col0, bias_base + i * 32, e);
+                epilogue_chunk32_fast<OUT, SC>(v, crow + col0, bias_base + i * 32, e, rchunk);
             else
-                epilogue_chunk32_safe<OUT, SC>(v, crow + col0, col0, e);
+                epilogue_chunk32_safe<OUT, SC>(v, crow + col0, col0, e, rchunk);
         }
         __syncwarp();  // reconverge after the per-row store before the collective wait
         if (more) tmem_ld_wait(nxt);
@@ -466,11 +505,12 @@ __device__ __forceinline__ uint32_t sw64_offset(int r, int q) {
 
 // Columns h*PER .. h*PER+PER-1 of one 32-column chunk (PER = 64 bytes of
 // output): beta*C with C read from this thread's row of the staged box,
-// bias, GELU, and the result packed back into the same row of the box.
+// bias, GELU, the residual (SC: read from global memory, output row `row`,
+// columns x ..), and the result packed back into the same row of the box.
 // v holds alpha*acc on entry.
-template <int OUT>
+template <int OUT, bool SC = true>
 __device__ __forceinline__ void box_math(float (&v)[32], int h, unsigned char *box, const float *bias_chunk,
-                                         const EpiParams &e) {
+                                         const EpiParams &e, int row, int x) {
     constexpr int PER = 64 / static_cast<int>(sizeof(typename Elem<OUT>::T));
     constexpr int PV = Vec16<OUT>::kPerVec;
     const int lane = threadIdx.x & 31;
@@ -494,6 +534,26 @@ __device__ __forceinline__ void box_math(float (&v)[32], int h, unsigned char *b
         if (e.epilogue >= kEpiBiasGelu) {
 #pragma unroll
             for (int j = 0; j < PER; j += 2) activate2(v[h * PER + j], v[h * PER + j + 1], e.epilogue);
+        }
+    }
+    if constexpr (SC) {
+        if (e.residual != nullptr && row < e.M) {
+            // only columns inside the matrix: the box may reach past N (and R past its allocation)
+            const typename Elem<OUT>::T *rr = residual_row<OUT>(e, row) + x;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c0 = x + q * PV;
+                if (e.r_vec && c0 + PV <= e.N) {
+                    float r[PV];
+                    Vec16<OUT>::unpack(__ldg(reinterpret_cast<const uint4 *>(rr + q * PV)), r);
+#pragma unroll
+                    for (int t = 0; t < PV; ++t) v[h * PER + q * PV + t] += r[t];
+                } else {
+#pragma unroll
+                    for (int t = 0; t < PV; ++t)
+                        if (c0 + t < e.N) v[h * PER + q * PV + t] += Elem<OUT>::load(rr + q * PV + t);
+                }
+            }
         }
     }
 #pragma unroll
@@ -546,9 +606,11 @@ __device__ __forceinline__ float2 unpack2_out(uint32_t w) {
 
 // Transposed counterpart of box_math for one whole chunk (v = alpha*acc of
 // output column n0+lane, rows m0 .. m0+31): beta*C from the box, the column's
-// bias, GELU, and the result written back into the box.
-template <int OUT>
-__device__ __forceinline__ void box_math_t(float (&v)[32], unsigned char *box, float bias_lane, const EpiParams &e) {
+// bias, GELU, the residual (SC; a warp-wide load per row reads 32 consecutive
+// columns), and the result written back into the box.
+template <int OUT, bool SC = true>
+__device__ __forceinline__ void box_math_t(float (&v)[32], unsigned char *box, float bias_lane, const EpiParams &e,
+                                           int n0, int m0) {
     static_assert(OUT == kDtF16 || OUT == kDtBF16, "transposed staging is for 16-bit outputs");
     const int lane = threadIdx.x & 31;
     const uint32_t odd = lane & 1u;
@@ -572,6 +634,15 @@ __device__ __forceinline__ void box_math_t(float (&v)[32], unsigned char *box, f
         if (e.epilogue >= kEpiBiasGelu) {
 #pragma unroll
             for (int j = 0; j < 32; j += 2) activate2(v[j], v[j + 1], e.epilogue);
+        }
+    }
+    if constexpr (SC) {
+        const int n = n0 + lane;
+        if (e.residual != nullptr && n < e.N) {
+            const typename Elem<OUT>::T *rc = reinterpret_cast<const typename Elem<OUT>::T *>(e.residual) + n;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (m0 + j < e.M) v[j] += Elem<OUT>::load(rc + (long long)(m0 + j) * e.ldr);
         }
     }
 #pragma unroll
@@ -617,7 +688,7 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
                 if (!__all_sync(0xffffffffu, got)) return false;
                 cphase ^= 1u;
             }
-            box_math_t<OUT>(v, buf, bias_lane, e);
+            box_math_t<OUT, SC>(v, buf, bias_lane, e, row0, col0);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -642,7 +713,7 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
             if (!__all_sync(0xffffffffu, got)) return false;
             cphase ^= 1u;
         }
-        box_math<OUT>(v, h, buf, bias_chunk, e);
+        box_math<OUT, SC>(v, h, buf, bias_chunk, e, row0 + lane, x);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -717,7 +788,7 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
                 scale_alpha(v, e.alpha);
                 product_scale_chunk<SC>(v, e, row0 + lane, col_base + i * 32, true);
-                box_math_t<OUT>(v, area + i * kStageBoxBytes, bias_lane, e);
+                box_math_t<OUT, SC>(v, area + i * kStageBoxBytes, bias_lane, e, row0, col_base + i * 32);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -760,7 +831,8 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
 #pragma unroll
         for (int h = 0; h < NSUB; ++h) {
             const int x = col_base + i * 32 + h * PER;
-            if (x < e.N) box_math<OUT>(v, h, area + (i * NSUB + h) * kStageBoxBytes, bias_base + i * 32, e);
+            if (x < e.N)
+                box_math<OUT, SC>(v, h, area + (i * NSUB + h) * kStageBoxBytes, bias_base + i * 32, e, row0 + lane, x);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -794,6 +866,11 @@ __device__ __forceinline__ float epilogue_prefetch_t(int col_base, int nchunk, i
             asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
         }
     }
+    if (e.residual != nullptr && row0 < e.N) {
+        const int m_end = min(col_base + nchunk * 32, e.M);
+        for (int m = col_base + lane; m < m_end; m += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(residual_row<OUT>(e, m) + row0));
+    }
     __syncwarp();
     return b;
 }
@@ -818,6 +895,11 @@ __device__ __forceinline__ void epilogue_prefetch(float *bias_s, int col_base, i
         const OutT *crow = reinterpret_cast<const OutT *>(e.C) + (long long)row * e.ldc + col_base;
         const int bytes = ncols * static_cast<int>(sizeof(OutT));
         const char *p = reinterpret_cast<const char *>(crow);
+        for (int off = 0; off < bytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+    }
+    if (e.residual != nullptr && row_ok && ncols > 0) {
+        const char *p = reinterpret_cast<const char *>(residual_row<OUT>(e, row) + col_base);
+        const int bytes = ncols * static_cast<int>(sizeof(OutT));
         for (int off = 0; off < bytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
     }
     __syncwarp();

@@ -559,6 +559,9 @@ EpiParams make_epi(int64_t M, int64_t N, void *C, int64_t ldc, int cd, float alp
     e.alpha_scale = e.row_scale = e.col_scale = nullptr;
     e.out_scale = nullptr;
     e.amax = nullptr;
+    e.residual = nullptr;  // residual: set by gemm_ex
+    e.ldr = 0;
+    e.r_vec = 0;
     return e;
 }
 
@@ -687,8 +690,19 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t ab_dtype, co
         if (scales->amax && (st = check_range(scales->amax, 4)) != GEMM_OK) return st;
         e.out_scale = c_dtype == GEMM_E4M3 ? scales->out_scale : nullptr;
         e.amax = scales->amax;
+        if (scales->residual != nullptr) {
+            // post-activation residual, M x ldr in the output type (not with an E4M3 output)
+            if (c_dtype == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+            if (scales->ldr < N) return GEMM_ERR_INVALID_ARG;
+            if ((st = check_range(scales->residual, span_bytes(M, N, scales->ldr, 1, ces))) != GEMM_OK) return st;
+            e.residual = scales->residual;
+            e.ldr = scales->ldr;
+            e.r_vec = ((reinterpret_cast<uintptr_t>(scales->residual) & 15u) == 0 && (scales->ldr * ces) % 16 == 0)
+                          ? 1 : 0;
+        }
     }
-    e.scaled = (e.alpha_scale || e.row_scale || e.col_scale || e.out_scale || e.amax || c_dtype == GEMM_E4M3) ? 1 : 0;
+    e.scaled = (e.alpha_scale || e.row_scale || e.col_scale || e.out_scale || e.amax || e.residual ||
+                c_dtype == GEMM_E4M3) ? 1 : 0;
     // E4M3 outputs and the amax reduction use the direct stores (no staged C).
     const bool direct_c = c_dtype == GEMM_E4M3 || e.amax != nullptr;
 

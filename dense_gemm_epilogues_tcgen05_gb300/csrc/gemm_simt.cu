@@ -88,8 +88,9 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtArgs 
             const int col = n0 + tx + 16 * j;
             if (col < N) {
                 const float b = (a.e.epilogue != kEpiNone) ? a.e.bias[col] : 0.0f;
+                const OutT *r = a.e.residual ? residual_row<OUT>(a.e, row) + col : nullptr;
                 const float y = epilogue_store_one<OUT>(acc[i][j] * product_scale(a.e, row, col),
-                                                        C + (long long)row * a.e.ldc + col, b, a.e);
+                                                        C + (long long)row * a.e.ldc + col, b, a.e, r);
                 amax = fmaxf(amax, fabsf(y));
             }
         }
@@ -107,7 +108,8 @@ __global__ void epilogue_only_kernel(const EpiParams e) {
          idx += (long long)gridDim.x * blockDim.x) {
         const long long i = idx / e.N, j = idx - i * e.N;
         const float b = (e.epilogue != kEpiNone) ? e.bias[j] : 0.0f;
-        amax = fmaxf(amax, fabsf(epilogue_store_one<OUT>(0.0f, C + i * e.ldc + j, b, e)));
+        const OutT *r = e.residual ? residual_row<OUT>(e, static_cast<int>(i)) + j : nullptr;
+        amax = fmaxf(amax, fabsf(epilogue_store_one<OUT>(0.0f, C + i * e.ldc + j, b, e, r)));
     }
     if (e.amax) amax_push(amax, e.amax);
 }

@@ -209,6 +209,7 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
                                                  unsigned int *status, float bias_lane) {
     using OutT = typename Elem<OUT>::T;
     OutT *crow = reinterpret_cast<OutT *>(e.C) + (long long)(row_ok ? row : 0) * e.ldc;
+    const OutT *rrow = (SC && row_ok) ? residual_row<OUT>(e, row) : nullptr;
     bool ok = true;
 #pragma unroll 1
     for (int i = 0; i < nvalid; ++i) {
@@ -239,10 +240,11 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
                                                        cbar, cphase, abort_flag, status);
             }
         } else if (row_ok) {
+            const OutT *rchunk = rrow != nullptr ? rrow + col0 : nullptr;
             if (e.c_vec && col0 + 32 <= e.N)
-                epilogue_chunk32_fast<OUT, SC>(v, crow + col0, bias_base + i * 32, e);
+                epilogue_chunk32_fast<OUT, SC>(v, crow + col0, bias_base + i * 32, e, rchunk);
             else
-                epilogue_chunk32_safe<OUT, SC>(v, crow + col0, col0, e);
+                epilogue_chunk32_safe<OUT, SC>(v, crow + col0, col0, e, rchunk);
         }
     }
     __syncwarp();
@@ -250,7 +252,12 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
 }
 
 // CL: CTAs per cluster, 2 (one pair) or 4 (two pairs sharing A by multicast).
-// SC: built for calls with product scales (gemm_ex); without, that code is left out.
+// SC: built for calls with product scales, fp8 output, amax or a residual
+// (gemm_ex); without, that code is left out.
+// Registers: an SM's 65,536 registers sit in four sub-partitions of 16,384,
+// and a 10-warp CTA places three warps on two of them, so a thread gets at
+// most 170 (168 in steps of 8).  Built with 200 (__maxnreg__), GB300 reports
+// no resident cluster for the kernel.
 template <int AB, int OUT, int STAGES, int BNH, int CL, bool SC>
 __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
     gemm_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

@@ -34,6 +34,11 @@ struct EpiParams {
     const float *alpha_scale, *row_scale, *col_scale;
     const float *out_scale;  // E4M3 output: stores y / out_scale[0] (NULL = 1)
     float *amax;             // atomically raised to max |y| over the outputs (NULL = not kept)
+    // Post-activation residual (gemm_ex): y = act(z) + R[i][j], R an M x ldr
+    // row-major array of the output type; NULL when absent (then `scaled` may be 0).
+    const void *residual;
+    long long ldr;           // elements
+    int r_vec;               // R's base and row pitch allow 16-byte vector loads
 };
 
 // Most clusters a stream-K schedule spreads over (the cut table's size).
@@ -89,6 +94,27 @@ struct Q4Args {
     int w_pitch;              // tensor-core kernel: width in bytes of its weight box, min(160, K / 2)
 };
 
+// Block-scaled (MX) product: elements of A (M x K) and of B given as its
+// transpose (N x K), both K-contiguous, with one E8M0 scale per 32 consecutive
+// k of a row.  Element types: E4M3 one per byte (MXFP8), E2M1 two per byte,
+// even k in the low nibble (MXFP4).
+enum : int { kMxE4M3 = 0, kMxE2M1 = 1 };
+
+// Scale factors as the kernel reads them (written by the pack pre-pass): for
+// each operand, 512-byte chunks of 128 rows x 4 blocks of 32 k; chunk (rb, kc)
+// at byte (rb * kc_count + kc) * 512, and inside it the scale of row
+// 128 rb + 32 g + l and block 4 kc + j at byte 16 l + 4 g + j -- the layout
+// tcgen05.cp ... 32x128b.warpx4 turns into the tensor-memory scale layout of
+// the block-scaled MMA (row r's scales at lane r, column r / 32, byte j).
+struct MxArgs {
+    EpiParams e;
+    int K;                          // elements
+    int tiles_m, tiles_n, num_tiles, num_kb, group_m;  // num_kb: stages of 128 bytes of K
+    const unsigned char *sfa, *sfb; // chunked scales of A and B
+    int kc_count;                   // chunk columns per 128-row block (a multiple of the chunks per stage)
+    unsigned int *status;
+};
+
 // Launchers (each returns the launch's cudaError_t), defined by the kernel files.
 //   one-SM tcgen05 kernel, `bn` = 256 or 128, `grid` CTAs:
 cudaError_t launch_tcgen05_f16(int out, int bn, const CUtensorMap &, const CUtensorMap &, const TcArgs &, int grid,
@@ -129,6 +155,11 @@ constexpr int kQ4MaxRows = 8;
 cudaError_t launch_q4_gemv(int x_dtype, int out, const CUtensorMap *tmW, const Q4Args &args, cudaStream_t stream);
 cudaError_t launch_q4_dequantize(int out, long long N, long long K, const uint32_t *Wq, const uint32_t *SB, void *W,
                                  cudaStream_t stream);
+//   block-scaled product (one SM per 128 x 128 tile) and its scale-factor pack pre-pass:
+cudaError_t launch_mx(int elem, int out, const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs &args, int grid,
+                      cudaStream_t stream);
+cudaError_t launch_mx_sf_pack(const unsigned char *src, long long rows, long long blocks, unsigned char *dst,
+                              long long row_blocks, long long kc_count, cudaStream_t stream);
 cudaError_t launch_wait_selftest(const unsigned int *never_set, unsigned long long limit_ns, unsigned int *status,
                                  cudaStream_t stream);
 

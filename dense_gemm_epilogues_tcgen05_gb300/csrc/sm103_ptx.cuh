@@ -126,7 +126,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
                  : "memory");
 }
 
-// Close the current bulk async-group of this thread.
 // Untiled bulk copy global -> this CTA's shared memory, counted as `bytes`
 // transaction bytes on `bar`.  Both addresses 16-byte aligned, `bytes` a
 // multiple of 16.
@@ -136,6 +135,7 @@ __device__ __forceinline__ void bulk_load_1d(void *smem_dst, const void *gsrc, u
                  : "memory");
 }
 
+// Close the current bulk async-group of this thread.
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's bulk groups still read their shared-memory source.
@@ -230,6 +230,60 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
             "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
             : "memory");
     }
+}
+
+// ------------------------------------------------ block-scaled MMA (MX) --
+
+// Instruction descriptor of a block-scaled MMA with fp32 accumulation and
+// E8M0 scales: bits 4-5 B scale-factor byte, 7-9 / 10-12 A / B format, 17-22
+// N >> 3, 23 scale type (1 = UE8M0), 24-28 M >> 4, 29-30 A scale-factor
+// byte; both operands K-major.
+__host__ __device__ constexpr uint32_t mma_idesc_bs(uint32_t fmt, uint32_t m, uint32_t n, uint32_t a_sf_id,
+                                                    uint32_t b_sf_id) {
+    return (b_sf_id << 4) | (fmt << 7) | (fmt << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) |
+           (a_sf_id << 29);
+}
+
+enum MxKind { kKindMxf8f6f4 = 0, kKindMxf4 = 1 };
+
+// D[tmem] (+)= (A * scale_A) * (B * scale_B), the scales read from tensor
+// memory at sfa_tmem / sfb_tmem (the bytes chosen by the descriptor):
+// kind::mxf8f6f4 takes one scale per 32 k (K = 32 per instruction, 8-bit
+// elements), kind::mxf4 two (K = 64, packed 4-bit elements).
+template <int KIND>
+__device__ __forceinline__ void tc_mma_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    if constexpr (KIND == kKindMxf8f6f4) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    }
+}
+
+// Shared-memory descriptor of an unswizzled matrix of 16-byte rows stored
+// contiguously (8-row core matrices 128 bytes apart, both strides 128).
+__device__ __forceinline__ uint64_t plain16_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 16;
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Copy 32 rows x 16 bytes from shared memory into 4 tensor-memory columns at
+// `taddr`, the same rows in each of the four 32-lane groups.  Ordered with
+// this thread's later tcgen05.mma.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has

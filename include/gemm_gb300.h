@@ -143,13 +143,22 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K,
  *   out_scale    fp32[1]  E4M3 output only: C stores y / out_scale[0] (NULL = 1),
  *                         rounded to nearest even and saturated to +-448;
  *   amax         fp32[1]  raised atomically to max |y| over the M x N outputs,
- *                         y being the activated value before out_scale and the
- *                         cast; the caller sets it (e.g. to 0) beforehand.
+ *                         y being the activated value (plus the residual)
+ *                         before out_scale and the cast; the caller sets it
+ *                         (e.g. to 0) beforehand.
+ *   residual     M x ldr row-major array of the OUTPUT type (F32, F16 or BF16;
+ *                         not with an E4M3 output), added after the activation:
+ *                         y = act(z) + residual[i][j] -- the post-activation
+ *                         residual of a transformer block.  ldr >= N (elements);
+ *                         columns N..ldr-1 are never read.  It must not overlap
+ *                         C.  NULL = none (ldr ignored).
  * The product term becomes alpha * alpha_scale[0] * row_scale[i] *
- * col_scale[j] * sum_k A[i][k] B[k][j]; beta*C and the bias are not scaled.
- * ("Case Study: Steel's BlockMMA": the epilogue is a functor applied to every
- * accumulator before the store; these are its per-row / per-column forms, and
- * the fp8 output with its amax the quantising store of a low-precision path.)
+ * col_scale[j] * sum_k A[i][k] B[k][j]; beta*C, the bias and the residual are
+ * not scaled.  ("Case Study: Steel's BlockMMA", the paragraph on the ending
+ * where fusion plugs in: the epilogue is a functor applied to every
+ * accumulator before the store; these are its per-row / per-column forms, the
+ * fp8 output with its amax the quantising store of a low-precision path, and
+ * the residual one more input of that functor.)
  */
 typedef struct {
     const float *alpha_scale;
@@ -157,15 +166,19 @@ typedef struct {
     const float *col_scale;
     const float *out_scale;
     float *amax;
+    const void *residual;
+    int64_t ldr;
 } gemm_scales_t;
 
 /*
- * gemm_ex -- gemm() with the scales above (scales may be NULL: then exactly
- * gemm()).  Same arguments, conventions and errors, plus c_dtype E4M3 (fp8
- * output, from F16, BF16 or E4M3 inputs, beta == 0; otherwise
- * GEMM_ERR_UNSUPPORTED).  The scale arrays are checked against their device
- * allocations like every other buffer.  With K == 0 or alpha == 0 the
- * product scales are not read (out_scale and amax still apply).
+ * gemm_ex -- gemm() with the scales and the residual above (scales may be
+ * NULL: then exactly gemm()).  Same arguments, conventions and errors, plus
+ * c_dtype E4M3 (fp8 output, from F16, BF16 or E4M3 inputs, beta == 0;
+ * otherwise GEMM_ERR_UNSUPPORTED).  The scale and residual arrays are checked
+ * against their device allocations like every other buffer; a residual with
+ * an E4M3 output is GEMM_ERR_UNSUPPORTED, ldr < N GEMM_ERR_INVALID_ARG.  With
+ * K == 0 or alpha == 0 the product scales are not read (out_scale, amax and
+ * the residual still apply).
  */
 gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K,
                       gemm_dtype_t ab_dtype,

@@ -44,9 +44,10 @@ def workspace(g, device="cuda", nbytes=0):
 
 
 def run_gemm(g, p, *, nan_c=False, stream=None, a_elem_offset=0, b_elem_offset=0, device="cuda",
-             use_workspace=True, baseline=None):
+             use_workspace=True, baseline=None, extra=None):
     """Run problem ``p`` on the GPU; guards and padding columns must stay intact.  With ``baseline``
-    (a BASELINE_* kind) the call goes to gemm_baseline instead of gemm."""
+    (a BASELINE_* kind) the call goes to gemm_baseline instead of gemm; product scales, a residual
+    or ``extra`` keyword arguments (e.g. amax) go through gemm_ex."""
     view = wl.CODE_VIEW[p.c_dtype]
     n = p.C.numel()
     host = torch.full((2 * GUARD + n,), CANARY[p.c_dtype], dtype=view)
@@ -73,8 +74,11 @@ def run_gemm(g, p, *, nan_c=False, stream=None, a_elem_offset=0, b_elem_offset=0
     path = g.gemm_query_path(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr,
                              p.b_stride_k, p.b_stride_n, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta,
                              bias, p.epilogue)
-    if p.product_scales:
+    if p.product_scales or p.residual is not None or extra:
         sc = {k: v.to(device) for k, v in p.product_scales.items()}
+        if p.residual is not None:
+            sc["residual"], sc["ldr"] = p.residual.to(device), p.ldr
+        sc.update(extra or {})
         ws = workspace(g, device, g.gemm_workspace_size(p.M, p.N, p.K, p.ab_dtype)) if use_workspace else None
         g.gemm_ex(p.M, p.N, p.K, p.ab_dtype, a_ptr, p.a_stride_m, p.a_stride_k, b_ptr, p.b_stride_k, p.b_stride_n,
                   c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias, p.epilogue, workspace=ws,

@@ -82,6 +82,10 @@ class Problem:
     # Product scales of the extended call (gemm_ex): float32 tensors
     # "alpha_scale" (1 value), "row_scale" (M), "col_scale" (N); absent = 1.
     product_scales: dict = dataclasses.field(default_factory=dict)
+    # Post-activation residual of the extended call: 1-D storage of an M x ldr
+    # row-major array of the output type (None = absent).
+    residual: Optional[torch.Tensor] = None
+    ldr: int = 0
 
     @property
     def flops(self) -> float:
@@ -102,7 +106,9 @@ class Problem:
                     alpha=self.alpha, beta=self.beta,
                     bias=None if self.bias is None else self.bias.numpy(),
                     epilogue=self.epilogue,
-                    **{k: v.numpy() for k, v in self.product_scales.items()})
+                    **{k: v.numpy() for k, v in self.product_scales.items()},
+                    **({} if self.residual is None else
+                       {"residual": self.residual.view(CODE_VIEW[self.c_dtype]).numpy(), "ldr": self.ldr}))
 
     def recipe_hash(self) -> str:
         return hashlib.sha256(self.recipe.encode()).hexdigest()[:16]
@@ -431,6 +437,19 @@ def with_product_scales(p: Problem, seed: int, *, alpha_scale: bool = True, row:
     if col:
         ps["col_scale"] = draw(p.N)
     return dataclasses.replace(p, product_scales=ps, recipe=p.recipe + f" scales(seed={seed}, dyadic={dyadic})")
+
+
+def with_residual(p: Problem, seed: int, *, pad: int = 0, integer: bool = False, nan_pad: bool = True) -> Problem:
+    """Attach a seeded residual R (M x ldr, ldr = N + pad, stored in the output
+    type): small integers in [-8, 8] or U[-1, 1].  The padding columns hold NaN
+    (a kernel that read them would show it); with ``nan_pad`` False, zeros."""
+    draw = small_integers if integer else uniform
+    ldr = p.N + pad
+    full = torch.full((p.M, ldr), float("nan") if nan_pad else 0.0, dtype=torch.float32)
+    full[:, :p.N] = draw(seed, p.M, p.N)
+    R = full.to(TORCH_DTYPE[p.c_dtype]).reshape(-1)
+    return dataclasses.replace(p, residual=R, ldr=ldr, name=p.name + "_res",
+                               recipe=p.recipe + f" residual(seed={seed}, pad={pad}, int={integer})")
 
 
 # ---------------------------------------------------------------------------
