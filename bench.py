@@ -647,6 +647,13 @@ def extra_cells(g, stream, peaks):
     cells["baseline_gate_fp16_4096"] = baseline_gate(g, stream, l2)
     for M in (1, 2, 8):
         cells[f"q4_decode_M{M}"] = q4_decode_cell(g, stream, M, compact=True)
+    # block-scaled MXFP8 / MXFP4, against 2x (fp8) and the fp4 rate
+    mx = {}
+    for nm, elem in (("mxfp8", wl.MX_E4M3), ("mxfp4", wl.MX_E2M1)):
+        c = mx_cell(g, stream, elem, 4096, name=f"{nm}_4096")
+        c["frac_of_2x_bf16_peak"] = round(c["tflops"] / (2 * peaks["bf16_tflops"]), 4)
+        cells[f"{nm}_4096"] = c
+        mx[nm] = c["tflops"]
     # config 4 (fp8 with its fp16 twins, bf16 output, and an fp32-output cell) and the large
     # bf16 cells last, so that the tail of the line carries them
     fp8 = {}
@@ -669,8 +676,55 @@ def extra_cells(g, stream, peaks):
         "fp8_4096_frac_of_2x_bf16": fp8[4096]["frac_of_2x_bf16_peak"],
         "gelu_fused_cost_pct": gelu_cost, "gelu_fusion_gain_pct": fusion_gain,
         "q4_decode_frac": {M: cells[f"q4_decode_M{M}"]["frac"] for M in (1, 2, 8)},
+        "mxfp8_4096": mx["mxfp8"], "mxfp4_4096": mx["mxfp4"],
     })
     return cells, summary
+
+
+def mx_cell(g, stream, elem, n, steps=30, warmup=3, name=None):
+    """Block-scaled product (gemm_mx) n^3, bf16 output: A, B ~ N(0,1) quantised to MX
+    (OCP MX v1.0: E8M0 scale per 32 k, E4M3 or E2M1 elements; seeds 971, 972), two
+    input sets rotated.  TFLOP/s back to back and per call, like cell()."""
+    import torch
+    import workloads as wl
+    code = {wl.MX_E4M3: g.MX_E4M3, wl.MX_E2M1: g.MX_E2M1}[elem]
+    p = wl.mx_problem(971, n, n, n, elem=elem, c_dtype=wl.BF16)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sets = [(p.A.to(dev), p.SA.to(dev), p.B.to(dev), p.SB.to(dev), p.C.clone().to(dev)) for _ in range(2)]
+    need = g.gemm_mx_workspace_size(n, n, n, code)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def call(i):
+        A, SA, B, SB, C = sets[i % 2]
+        g.gemm_mx(n, n, n, code, A, p.lda, SA, B, p.ldb, SB, C, n, wl.BF16, 1.0, 0.0, None, wl.EPI_NONE,
+                  workspace=ws, workspace_bytes=need, stream=stream)
+
+    for i in range(warmup):
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    total = e0.elapsed_time(e1)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        call(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    tf = [p.flops / (ev[i].elapsed_time(ev[i + 1]) * 1e-3) / 1e12 for i in range(steps)]
+    med, ci = bootstrap_ci(tf)
+    st = g.gemm_device_status()
+    if name is not None:
+        SAMPLES[name] = [round(x, 2) for x in tf]
+    del sets
+    torch.cuda.empty_cache()
+    return {"tflops": round(p.flops * steps / (total * 1e-3) / 1e12, 1), "ms": round(total / steps, 4),
+            "per_call": {"median": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)]}, "n": steps,
+            "status": st}
 
 
 def q4_decode_cell(g, stream, M, N=16384, K=16384, reps=50, compact=False):

@@ -26,7 +26,7 @@ __all__ = [
     "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast", "gemm_last_launch",
     "BASELINE_SIMT", "BASELINE_MMA_SYNC", "gemm_baseline", "gemm_q4", "gemm_q4_dequantize", "Q4_MAX_ROWS",
     "Q4_AUTO", "Q4_FFMA", "Q4_MMA", "gemm_set_q4_kernel",
-    "gemm_ex", "gemm_get_tuning",
+    "gemm_ex", "gemm_get_tuning", "MX_E4M3", "MX_E2M1", "gemm_mx", "gemm_mx_workspace_size",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
     "gemm_device_status", "gemm_status_string", "gemm_version", "LIB_PATH", "lib",
 ]
@@ -51,6 +51,8 @@ BASELINE_SIMT, BASELINE_MMA_SYNC = 0, 1
 Q4_MAX_ROWS = 8
 # gemm_q4_kernel_t
 Q4_AUTO, Q4_FFMA, Q4_MMA = 0, 1, 2
+# gemm_mx_elem_t
+MX_E4M3, MX_E2M1 = 0, 1
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -133,6 +135,11 @@ lib.gemm_baseline.restype = _int
 lib.gemm_baseline.argtypes = [_int, _i64, _i64, _i64, _int, ctypes.c_void_p, _i64, _i64, ctypes.c_void_p, _i64, _i64,
                               ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
                               ctypes.c_void_p]
+lib.gemm_mx.restype = _int
+lib.gemm_mx.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _i64, _int, _f32, _f32, _vp,
+                        _int, _vp, _sz, _vp]
+lib.gemm_mx_workspace_size.restype = _sz
+lib.gemm_mx_workspace_size.argtypes = [_i64, _i64, _i64, _int]
 lib.gemm_device_status.restype = _int
 lib.gemm_device_status.argtypes = [_vp]
 lib.gemm_status_string.restype = ctypes.c_char_p
@@ -285,6 +292,19 @@ def gemm_get_tuning() -> dict:
     t = _Tuning()
     _check(lib.gemm_get_tuning(ctypes.byref(t)), "gemm_get_tuning")
     return {n: getattr(t, n) for n, _ in _Tuning._fields_}
+
+
+def gemm_mx(M, N, K, elem, A, lda, a_scale, B, ldb, b_scale, C, ldc, c_dtype, alpha, beta, bias, epilogue,
+            workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Block-scaled product (MX_E4M3 / MX_E2M1 elements, E8M0 scales per 32 k): A M x K, B given as its
+    transpose N x K, both K-contiguous; see include/gemm_gb300.h."""
+    st = lib.gemm_mx(M, N, K, elem, _ptr(A), lda, _ptr(a_scale), _ptr(B), ldb, _ptr(b_scale), _ptr(C), ldc, c_dtype,
+                     alpha, beta, _ptr(bias), epilogue, _ptr(workspace), workspace_bytes, _stream(stream))
+    return _check(st, "gemm_mx")
+
+
+def gemm_mx_workspace_size(M, N, K, elem) -> int:
+    return int(lib.gemm_mx_workspace_size(M, N, K, elem))
 
 
 def gemm_last_launch() -> dict:

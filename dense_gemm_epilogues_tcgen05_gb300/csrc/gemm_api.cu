@@ -1070,6 +1070,107 @@ gemm_status_t gemm_q4_dequantize(int64_t N, int64_t K, const uint32_t *Wq, const
                : GEMM_ERR_CUDA;
 }
 
+// ---------------------------------------------------------- block-scaled --
+
+// Chunk columns of the packed scales: 4 blocks of 32 k per chunk, rounded up
+// to whole stages (1 chunk for E4M3 elements, 2 for E2M1).
+static int64_t mx_kc_count(int64_t K, int elem) {
+    const int64_t per_stage = elem == GEMM_MX_E2M1 ? 2 : 1;
+    const int64_t blocks = K / 32;
+    return (blocks + 4 * per_stage - 1) / (4 * per_stage) * per_stage;
+}
+
+static size_t mx_pack_bytes(int64_t rows, int64_t K, int elem) {
+    return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>(mx_kc_count(K, elem)) * 512;
+}
+
+size_t gemm_mx_workspace_size(int64_t M, int64_t N, int64_t K, gemm_mx_elem_t elem) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0 || (elem != GEMM_MX_E4M3 && elem != GEMM_MX_E2M1) ||
+        M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return 0;
+    return round256(mx_pack_bytes(M, K, elem)) + round256(mx_pack_bytes(N, K, elem));
+}
+
+gemm_status_t gemm_mx(int64_t M, int64_t N, int64_t K, gemm_mx_elem_t elem, const void *A, int64_t lda,
+                      const uint8_t *a_scale, const void *B, int64_t ldb, const uint8_t *b_scale, void *C,
+                      int64_t ldc, gemm_dtype_t c_dtype, float alpha, float beta, const float *bias,
+                      gemm_epilogue_t epilogue, void *workspace, size_t workspace_bytes, gemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (elem != GEMM_MX_E4M3 && elem != GEMM_MX_E2M1) return GEMM_ERR_INVALID_ARG;
+    if (!valid_dtype(c_dtype)) return GEMM_ERR_INVALID_ARG;
+    if (c_dtype == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
+    if (K % 32 != 0) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return record(GEMM_OK, gemm_launch_info_t{});
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (epilogue != GEMM_EPI_NONE && bias == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (!driver_fns().ok) return GEMM_ERR_CUDA;
+    DeviceState *dev = nullptr;
+    gemm_status_t st;
+    if ((st = device_state(&dev)) != GEMM_OK) return st;
+    const int ces = elem_bytes(c_dtype);
+    if ((st = check_range(C, span_bytes(M, N, ldc, 1, ces))) != GEMM_OK) return st;
+    if (epilogue != GEMM_EPI_NONE && (st = check_range(bias, static_cast<size_t>(N) * 4)) != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const EpiParams e = make_epi(M, N, C, ldc, c_dtype, alpha, beta, bias, epilogue);
+    gemm_launch_info_t info = {};
+    if (K == 0 || alpha == 0.0f) {
+        info.path = GEMM_PATH_EPILOGUE_ONLY;
+        return record(launch_epilogue_only(c_dtype, e, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA, info);
+    }
+    if (A == nullptr || B == nullptr || a_scale == nullptr || b_scale == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < K) return GEMM_ERR_INVALID_ARG;
+    // Elements per byte, and the row pitches in bytes: whole bytes, TMA-able (16-byte multiples).
+    const int64_t per_byte = elem == GEMM_MX_E2M1 ? 2 : 1;
+    if (lda % per_byte != 0 || ldb % per_byte != 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t a_pitch = lda / per_byte, b_pitch = ldb / per_byte, k_bytes = K / per_byte;
+    if ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0 ||
+        (M > 1 && a_pitch % 16 != 0) || (N > 1 && b_pitch % 16 != 0))
+        return GEMM_ERR_MISALIGNED;
+    if ((st = check_range(A, static_cast<size_t>((M - 1) * a_pitch + k_bytes))) != GEMM_OK) return st;
+    if ((st = check_range(B, static_cast<size_t>((N - 1) * b_pitch + k_bytes))) != GEMM_OK) return st;
+    const int64_t blocks = K / 32;
+    if ((st = check_range(a_scale, static_cast<size_t>(M * blocks))) != GEMM_OK) return st;
+    if ((st = check_range(b_scale, static_cast<size_t>(N * blocks))) != GEMM_OK) return st;
+    const size_t need = gemm_mx_workspace_size(M, N, K, elem);
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+        return GEMM_ERR_WORKSPACE;
+    if ((st = check_range(workspace, need)) != GEMM_OK) return st;
+
+    // Scales into the chunk layout the kernel copies to tensor memory.
+    const int64_t kc = mx_kc_count(K, elem);
+    unsigned char *sfa = static_cast<unsigned char *>(workspace);
+    unsigned char *sfb = sfa + round256(mx_pack_bytes(M, K, elem));
+    if (launch_mx_sf_pack(a_scale, M, blocks, sfa, (M + 127) / 128, kc, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_mx_sf_pack(b_scale, N, blocks, sfb, (N + 127) / 128, kc, s) != cudaSuccess) return GEMM_ERR_CUDA;
+
+    // Operands as bytes: boxes of 128 bytes of K x 128 rows, 128-byte swizzle, zero fill.
+    CUtensorMap ta, tb;
+    if ((st = encode_2d(&ta, GEMM_E4M3, A, k_bytes, M, a_pitch, 128, 128)) != GEMM_OK) return st;
+    if ((st = encode_2d(&tb, GEMM_E4M3, B, k_bytes, N, b_pitch, 128, 128)) != GEMM_OK) return st;
+    MxArgs a = {};
+    a.e = e;
+    a.K = static_cast<int>(K);
+    a.tiles_m = static_cast<int>((M + 127) / 128);
+    a.tiles_n = static_cast<int>((N + 127) / 128);
+    a.num_tiles = a.tiles_m * a.tiles_n;
+    a.num_kb = static_cast<int>((k_bytes + 127) / 128);
+    a.group_m = 8;
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.kc_count = static_cast<int>(kc);
+    a.status = dev->status;
+    const int grid = a.num_tiles < dev->num_sms ? a.num_tiles : dev->num_sms;
+    info.path = GEMM_PATH_TCGEN05;
+    info.kind = 1;
+    info.bn = 128;
+    info.cluster_ctas = 1;
+    info.grid_ctas = grid;
+    info.tiles = a.num_tiles;
+    return record(launch_mx(elem, c_dtype, ta, tb, a, grid, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA, info);
+}
+
 gemm_status_t gemm_wait_selftest(const unsigned int *never_set, uint64_t limit_ns, gemm_stream_t stream) {
     if (never_set == nullptr || limit_ns == 0 || limit_ns > 1000000000ull) return GEMM_ERR_INVALID_ARG;
     if (!driver_fns().ok) return GEMM_ERR_CUDA;

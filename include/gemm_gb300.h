@@ -481,6 +481,62 @@ gemm_status_t gemm_q4_dequantize(int64_t N, int64_t K, const uint32_t *Wq, const
                                  void *W, gemm_dtype_t w_dtype, gemm_stream_t stream);
 
 /*
+ * Block-scaled ("microscaling", MX) products.  Rigel section 1 lists fp4 and
+ * block-scaled MXFP4 next to fp8 among the low-precision rows of the matrix
+ * units without defining them; the formats here are those of the OCP
+ * Microscaling Formats (MX) specification v1.0.  Each block of 32 consecutive
+ * k of a row shares one scale, an E8M0 code c standing for 2^(c - 127) (0xFF:
+ * NaN), and each element is an E4M3 (MXFP8) or E2M1 (MXFP4) number:
+ *
+ *     a[i][k] = 2^(a_scale[i][k/32] - 127) * PA[i][k],  b[k][j] likewise with
+ *     b_scale[j][k/32] and PB[j][k]
+ *     C = cast(epilogue(alpha * sum_k a[i][k] b[k][j] + beta*C + bias))
+ *
+ * with gemm()'s epilogues, output types (F32, F16, BF16) and conventions.
+ */
+typedef enum {
+    GEMM_MX_E4M3 = 0,   /* MXFP8: one E4M3 element per byte */
+    GEMM_MX_E2M1 = 1    /* MXFP4: two E2M1 elements per byte, even k in the low nibble */
+} gemm_mx_elem_t;
+
+/*
+ * gemm_mx -- the block-scaled product above on the tensor cores
+ * (tcgen05.mma kind::mxf8f6f4 / kind::mxf4, scales applied by the MMA).
+ *   K              a multiple of 32 (whole scale blocks); M, N, K >= 0.
+ *   A, lda         M x K elements, row-major (K-contiguous), row pitch lda
+ *                  ELEMENTS (lda >= K; even for E2M1).  16-byte aligned base,
+ *                  row pitch a multiple of 16 bytes, else GEMM_ERR_MISALIGNED.
+ *   a_scale        M x K/32 E8M0 codes, row-major (pitch K/32 bytes), device.
+ *   B, ldb         B given as its transpose: N x K elements, K-contiguous, row
+ *                  pitch ldb elements, same alignment rules.
+ *   b_scale        N x K/32 E8M0 codes, row-major.
+ *   C, ldc, c_dtype, alpha, beta, bias, epilogue: as in gemm() (c_dtype F32,
+ *                  F16 or BF16; alpha == 0 or K == 0 reads neither operands
+ *                  nor scales).
+ *   workspace      device scratch, 256-byte aligned, of at least
+ *                  gemm_mx_workspace_size() bytes (GEMM_ERR_WORKSPACE
+ *                  otherwise): the scales rearranged for the tensor cores.
+ *                  Calls sharing it must not overlap; no initialisation needed.
+ * Asynchronous on `stream`; errors as gemm().
+ */
+gemm_status_t gemm_mx(int64_t M, int64_t N, int64_t K, gemm_mx_elem_t elem,
+                      const void *A, int64_t lda, const uint8_t *a_scale,
+                      const void *B, int64_t ldb, const uint8_t *b_scale,
+                      void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                      float alpha, float beta,
+                      const float *bias, gemm_epilogue_t epilogue,
+                      void *workspace, size_t workspace_bytes,
+                      gemm_stream_t stream);
+
+/*
+ * gemm_mx_workspace_size -- bytes of workspace gemm_mx needs: 512 bytes per
+ * 128 rows of A and of B per 128 (E4M3) or 256 (E2M1) k, each half rounded up
+ * to 256 bytes.  0 for invalid sizes (K not a multiple of 32).  Never fails,
+ * touches no device.
+ */
+size_t gemm_mx_workspace_size(int64_t M, int64_t N, int64_t K, gemm_mx_elem_t elem);
+
+/*
  * Baselines of the cheap-baseline gate (Rigel section 3; section 4, signal
  * 2): a claim that the tensor path is fast stands only once the trivial
  * explanations have run and lost -- a GEMM on the ordinary ALUs, and the

@@ -268,3 +268,22 @@ def test_q4_validation_without_gpu(g):
         g.gemm_q4_dequantize(64, 128, W, SB, C, g.F32, stream=0)
     assert e.value.status == g.ERR_UNSUPPORTED
     assert g.gemm_q4_dequantize(0, 128, W, SB, C, g.F16, stream=0) == 0
+
+
+def test_mx_workspace_size_and_validation_without_gpu(g):
+    """gemm_mx_workspace_size is a pure function of the sizes; argument errors come back before any
+    CUDA call."""
+    # MXFP8: 4 blocks of 32 k per 512-byte chunk of 128 rows; MXFP4 rounds chunk columns to pairs
+    assert g.gemm_mx_workspace_size(128, 128, 128, g.MX_E4M3) == 512 + 512
+    assert g.gemm_mx_workspace_size(4096, 4096, 4096, g.MX_E4M3) == 2 * 32 * 32 * 512
+    assert g.gemm_mx_workspace_size(200, 136, 96, g.MX_E4M3) == 2 * 512 + 2 * 512
+    assert g.gemm_mx_workspace_size(128, 128, 160, g.MX_E2M1) == 2 * 512 + 2 * 512   # 5 blocks -> 2 chunks
+    assert g.gemm_mx_workspace_size(128, 128, 48, g.MX_E4M3) == 0                     # not whole blocks
+    assert g.gemm_mx_workspace_size(0, 128, 128, g.MX_E4M3) == 0
+    args = (PA, 128, PB, PB, 128, PBIAS, PC, 128)
+    for K, cd, elem, status in ((48, g.F32, g.MX_E4M3, g.ERR_INVALID_ARG), (128, g.E4M3, g.MX_E4M3, g.ERR_UNSUPPORTED),
+                                (128, g.F32, 7, g.ERR_INVALID_ARG)):
+        with pytest.raises(g.GemmError) as ei:
+            g.gemm_mx(128, 128, K, elem, *args, cd, 1.0, 0.0, None, g.EPI_NONE, stream=0)
+        assert ei.value.status == status
+    assert g.gemm_mx(0, 128, 128, g.MX_E4M3, *args, g.F32, 1.0, 0.0, None, g.EPI_NONE, stream=0) == 0   # no-op
