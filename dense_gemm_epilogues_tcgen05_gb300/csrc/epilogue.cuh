@@ -125,6 +125,12 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 }
 __device__ __forceinline__ uint64_t f2_splat(float c) { return f2_pack(c, c); }
 
+// v[i .. i+3] += b, two lanes per instruction.
+__device__ __forceinline__ void add4_f2(float (&v)[32], int i, const float4 &b) {
+    f2_unpack(f2_add(f2_pack(v[i], v[i + 1]), f2_pack(b.x, b.y)), v[i], v[i + 1]);
+    f2_unpack(f2_add(f2_pack(v[i + 2], v[i + 3]), f2_pack(b.z, b.w)), v[i + 2], v[i + 3]);
+}
+
 // GELU of two values at once; same operations as gelu_erf, lane by lane.
 __device__ __forceinline__ void gelu_erf2(float &z0, float &z1) {
     using namespace gelu_c;
@@ -175,24 +181,134 @@ __device__ __forceinline__ float silu(float z) {
 // ReLU: max(z, 0), NaN kept.
 __device__ __forceinline__ float relu(float z) { return z < 0.0f ? 0.0f : z; }
 
-// The epilogue's activation of z (identity for kEpiNone / kEpiBias).
-__device__ __forceinline__ float activate(float z, int epi) {
+// --- cheaper forms for 16-bit outputs -----------------------------------------
+// A 16-bit output rounds to 2^-9 (bf16) or 2^-12 (fp16) of its value, and its
+// tolerance is 2e-3 of the error scale D >= |z|; the forms below stay within
+// 3e-4 |z| of the exact activation and cost no more than one special-function
+// operation per element (the accurate forms above cost two).  They serve F16
+// and BF16 outputs only, and not when the call keeps an amax (a reduction held
+// to the fp32 tolerance): fp32 and E4M3 outputs and amax calls take the
+// accurate forms.
+//
+// GELU (erf form): Phi(z) - 1/2 = z P(z^2) on |z| <= 4 (z clamped beyond;
+// Phi(4) = 1 - 3.2e-5), P of degree 6 with the coefficients of a near-minimax
+// fit of the absolute error in Phi (fit_gelu_poly.py beside the package's
+// sources: least squares in the Chebyshev basis, reweighted towards the
+// largest errors).  Largest error 1.1e-4 in Phi in float32, so at most
+// 1.1e-4 |z| in GELU(z) = z Phi(z) -- a twentieth of a bf16 output's own
+// rounding; multiply-adds only (measured on GB300, degree 8 at 2.8e-5 cost
+// 1.2 points more of fused cost at M = 2048, N = K = 4096).
+namespace gelu_p {
+constexpr float kZmax = 4.0f;
+constexpr float kC0 = 0.3985269069671631f, kC1 = -0.06538835167884827f, kC2 = 0.0091129494830966f,
+                kC3 = -0.0008789804996922612f, kC4 = 5.419035005616024e-05f, kC5 = -1.8918872228823602e-06f,
+                kC6 = 2.8160954457234766e-08f;
+}  // namespace gelu_p
+
+__device__ __forceinline__ float gelu_erf_poly(float z) {
+    using namespace gelu_p;
+    const float zc = fminf(fmaxf(z, -kZmax), kZmax);
+    const float s = zc * zc;
+    float p = fmaf(kC6, s, kC5);
+    p = fmaf(p, s, kC4);
+    p = fmaf(p, s, kC3);
+    p = fmaf(p, s, kC2);
+    p = fmaf(p, s, kC1);
+    p = fmaf(p, s, kC0);
+    const float h = zc * p;              // Phi(z) - 1/2
+    return fmaf(z, h, 0.5f * z);         // z (1/2 + h)
+}
+
+// The same operations on two values, two lanes per instruction.
+__device__ __forceinline__ void gelu_erf_poly2(float &z0, float &z1) {
+    using namespace gelu_p;
+    const uint64_t zc = f2_pack(fminf(fmaxf(z0, -kZmax), kZmax), fminf(fmaxf(z1, -kZmax), kZmax));
+    const uint64_t s = f2_mul(zc, zc);
+    uint64_t p = f2_fma(f2_splat(kC6), s, f2_splat(kC5));
+    p = f2_fma(p, s, f2_splat(kC4));
+    p = f2_fma(p, s, f2_splat(kC3));
+    p = f2_fma(p, s, f2_splat(kC2));
+    p = f2_fma(p, s, f2_splat(kC1));
+    p = f2_fma(p, s, f2_splat(kC0));
+    const uint64_t h = f2_mul(zc, p);
+    const uint64_t z = f2_pack(z0, z1);
+    f2_unpack(f2_fma(z, h, f2_mul(f2_splat(0.5f), z)), z0, z1);
+}
+
+// The hardware tanh (tanh.approx.f32, relative error about 2^-11).
+__device__ __forceinline__ float tanh_hw(float u) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(u));
+    return r;
+}
+
+// GELU (tanh form) with the hardware tanh: error up to 0.5 |z| 2^-11.
+__device__ __forceinline__ float gelu_tanh_hw(float z) {
+    constexpr float kSqrt2OverPi = 0.79788456080286535588f;
+    const float u = kSqrt2OverPi * fmaf(0.044715f * z, z * z, z);
+    const float hz = 0.5f * z;
+    return fmaf(hz, tanh_hw(u), hz);
+}
+
+// SiLU as z sigmoid(z) = (z/2) (1 + tanh(z/2)) with the hardware tanh.
+__device__ __forceinline__ float silu_hw(float z) {
+    const float hz = 0.5f * z;
+    return fmaf(hz, tanh_hw(hz), hz);
+}
+
+// Whether output type OUT may take the cheaper forms.
+template <int OUT>
+constexpr bool kCheapActivation = OUT == kDtF16 || OUT == kDtBF16;
+
+// The epilogue's activation of z (identity for kEpiNone / kEpiBias): the
+// cheaper forms above for 16-bit outputs unless `precise`, else the accurate
+// ones.
+template <int OUT>
+__device__ __forceinline__ float activate_one(float z, int epi, bool precise) {
+    const bool kLow = kCheapActivation<OUT> && !precise;
     switch (epi) {
-    case kEpiBiasGelu: return gelu_erf(z);
-    case kEpiBiasGeluTanh: return gelu_tanh(z);
-    case kEpiBiasSilu: return silu(z);
+    case kEpiBiasGelu: return kLow ? gelu_erf_poly(z) : gelu_erf(z);
+    case kEpiBiasGeluTanh: return kLow ? gelu_tanh_hw(z) : gelu_tanh(z);
+    case kEpiBiasSilu: return kLow ? silu_hw(z) : silu(z);
     case kEpiBiasRelu: return relu(z);
     default: return z;
     }
 }
 
-// Activation of two values (erf GELU two lanes per instruction).
-__device__ __forceinline__ void activate2(float &z0, float &z1, int epi) {
+// The activation of v[off] .. v[off + CNT - 1] (CNT even): one branch on the
+// epilogue for the whole run, then the chosen activation straight through --
+// a branch per element (indirect, for a switch) cost more than ReLU itself.
+// Values get exactly what activate_one gives them.
+template <int OUT, int CNT>
+__device__ __forceinline__ void activate_run(float (&v)[32], int off, int epi, bool precise) {
+    const bool kLow = kCheapActivation<OUT> && !precise;
     if (epi == kEpiBiasGelu) {
-        gelu_erf2(z0, z1);
-    } else if (epi > kEpiBiasGelu) {
-        z0 = activate(z0, epi);
-        z1 = activate(z1, epi);
+        if (kLow) {
+#pragma unroll
+            for (int j = 0; j < CNT; j += 2) gelu_erf_poly2(v[off + j], v[off + j + 1]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CNT; j += 2) gelu_erf2(v[off + j], v[off + j + 1]);
+        }
+    } else if (epi == kEpiBiasRelu) {
+#pragma unroll
+        for (int j = 0; j < CNT; ++j) v[off + j] = relu(v[off + j]);
+    } else if (epi == kEpiBiasSilu) {
+        if (kLow) {
+#pragma unroll
+            for (int j = 0; j < CNT; ++j) v[off + j] = silu_hw(v[off + j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CNT; ++j) v[off + j] = silu(v[off + j]);
+        }
+    } else if (epi == kEpiBiasGeluTanh) {
+        if (kLow) {
+#pragma unroll
+            for (int j = 0; j < CNT; ++j) v[off + j] = gelu_tanh_hw(v[off + j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CNT; ++j) v[off + j] = gelu_tanh(v[off + j]);
+        }
     }
 }
 
@@ -257,7 +373,7 @@ __device__ __forceinline__ float epilogue_store_one(float acc, typename Elem<OUT
         if (e.beta != 0.0f) z = fmaf(e.beta, Elem<OUT>::load(c), z);  // E4M3 outputs are written only
     }
     if (e.epilogue != kEpiNone) z += bias_j;
-    z = activate(z, e.epilogue);
+    z = activate_one<OUT>(z, e.epilogue, e.amax != nullptr);
     if (r != nullptr) z += Elem<OUT>::load(r);
     if constexpr (OUT == kDtE4M3)
         *c = Elem<OUT>::cvt(e.out_scale ? z / *e.out_scale : z);
@@ -396,14 +512,8 @@ __device__ __forceinline__ void epilogue_chunk32_fast(float (&v)[32], typename E
     if (e.epilogue != kEpiNone) {
         const float4 *b4 = reinterpret_cast<const float4 *>(bias_chunk);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 b = b4[q];
-            v[4 * q] += b.x; v[4 * q + 1] += b.y; v[4 * q + 2] += b.z; v[4 * q + 3] += b.w;
-        }
-        if (e.epilogue >= kEpiBiasGelu) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) activate2(v[j], v[j + 1], e.epilogue);
-        }
+        for (int q = 0; q < 8; ++q) add4_f2(v, 4 * q, b4[q]);
+        if (e.epilogue >= kEpiBiasGelu) activate_run<OUT, 32>(v, 0, e.epilogue, SC && e.amax != nullptr);
     }
     if constexpr (SC) {
         if (rchunk != nullptr) add_residual32<OUT>(v, rchunk, e);
@@ -526,15 +636,8 @@ __device__ __forceinline__ void box_math(float (&v)[32], int h, unsigned char *b
     if (e.epilogue != kEpiNone) {
         const float4 *b4 = reinterpret_cast<const float4 *>(bias_chunk + h * PER);
 #pragma unroll
-        for (int q = 0; q < PER / 4; ++q) {
-            const float4 b = b4[q];
-            v[h * PER + 4 * q] += b.x; v[h * PER + 4 * q + 1] += b.y;
-            v[h * PER + 4 * q + 2] += b.z; v[h * PER + 4 * q + 3] += b.w;
-        }
-        if (e.epilogue >= kEpiBiasGelu) {
-#pragma unroll
-            for (int j = 0; j < PER; j += 2) activate2(v[h * PER + j], v[h * PER + j + 1], e.epilogue);
-        }
+        for (int q = 0; q < PER / 4; ++q) add4_f2(v, h * PER + 4 * q, b4[q]);
+        if (e.epilogue >= kEpiBiasGelu) activate_run<OUT, PER>(v, h * PER, e.epilogue, SC && e.amax != nullptr);
     }
     if constexpr (SC) {
         if (e.residual != nullptr && row < e.M) {
@@ -629,12 +732,10 @@ __device__ __forceinline__ void box_math_t(float (&v)[32], unsigned char *box, f
         }
     }
     if (e.epilogue != kEpiNone) {
+        const uint64_t b2 = f2_splat(bias_lane);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] += bias_lane;
-        if (e.epilogue >= kEpiBiasGelu) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) activate2(v[j], v[j + 1], e.epilogue);
-        }
+        for (int j = 0; j < 32; j += 2) f2_unpack(f2_add(f2_pack(v[j], v[j + 1]), b2), v[j], v[j + 1]);
+        if (e.epilogue >= kEpiBiasGelu) activate_run<OUT, 32>(v, 0, e.epilogue, SC && e.amax != nullptr);
     }
     if constexpr (SC) {
         const int n = n0 + lane;
@@ -645,14 +746,16 @@ __device__ __forceinline__ void box_math_t(float (&v)[32], unsigned char *box, f
                 if (m0 + j < e.M) v[j] += Elem<OUT>::load(rc + (long long)(m0 + j) * e.ldr);
         }
     }
+    // Each lane writes its column of every row: 2-byte stores, a warp's 32 of
+    // them filling one row's 64 bytes (two lanes per 32-bit word, no bank
+    // conflict).  The 64-byte swizzle permutes a row's 16-byte units by
+    // (row >> 1) & 3, so the lane's unit index takes one of four values.
+    const uint32_t unit = static_cast<uint32_t>(lane) >> 3, within = (static_cast<uint32_t>(lane) & 7u) * 2u;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        // send the row the partner writes, keep the row this lane writes
-        const float send = odd ? v[2 * i] : v[2 * i + 1];
-        const float keep = odd ? v[2 * i + 1] : v[2 * i];
-        const float got = __shfl_xor_sync(0xffffffffu, send, 1);
-        const uint32_t w = odd ? pack2_out<OUT>(got, keep) : pack2_out<OUT>(keep, got);
-        *reinterpret_cast<uint32_t *>(box + sw64_word((2 * i + odd) * 64u + col_bytes)) = w;
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t off = static_cast<uint32_t>(i) * 64u + ((unit ^ ((static_cast<uint32_t>(i) >> 1) & 3u)) << 4) +
+                             within;
+        *reinterpret_cast<typename Elem<OUT>::T *>(box + off) = Elem<OUT>::cvt(v[i]);
     }
 }
 

@@ -123,7 +123,7 @@ __global__ void bias_gelu_kernel(const EpiParams e) {
          idx += (long long)gridDim.x * blockDim.x) {
         const long long i = idx / e.N, j = idx - i * e.N;
         OutT *p = C + i * e.ldc + j;
-        *p = Elem<OUT>::cvt(gelu_erf(Elem<OUT>::load(p) + e.bias[j]));
+        *p = Elem<OUT>::cvt(activate_one<OUT>(Elem<OUT>::load(p) + e.bias[j], kEpiBiasGelu, false));
     }
 }
 

@@ -89,3 +89,43 @@ def test_activation_accuracy_over_range(cuda_lib, epi, ab):
     # the hardware 2^x / reciprocal approximations: ~1e-7 absolute plus ~3e-7 relative
     assert np.all(err <= 2e-7 + 6e-7 * np.abs(z)[None, :]), float((err / (2e-7 + 6e-7 * np.abs(z))).max())
     assert bool(np.all(got[:, z < 0] <= 0.0)) or epi != wl.EPI_BIAS_RELU
+
+
+ALL_ACTS = [wl.EPI_BIAS_GELU, wl.EPI_BIAS_GELU_TANH, wl.EPI_BIAS_SILU, wl.EPI_BIAS_RELU]
+ALL_REF = {**REF, wl.EPI_BIAS_GELU: oracle.gelu}
+# How far the low-precision-output forms may stray from the exact activation, as a multiple of
+# |z|: the degree-6 polynomial normal CDF of erf-GELU (1.1e-4 in Phi), the hardware tanh of the
+# tanh-GELU and SiLU forms (relative error about 2^-11, times |z|/2), ReLU exact.
+LOW_FORM_BOUND = {wl.EPI_BIAS_GELU: 1.2e-4, wl.EPI_BIAS_GELU_TANH: 3e-4, wl.EPI_BIAS_SILU: 3e-4,
+                  wl.EPI_BIAS_RELU: 0.0}
+
+
+@pytest.mark.parametrize("epi", ALL_ACTS, ids=["gelu"] + ACT_IDS)
+@pytest.mark.parametrize("out", [wl.F16, wl.BF16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("kernel", ["tcgen05", "simt"])
+def test_low_precision_output_activations_over_range(cuda_lib, epi, out, kernel):
+    """z = bias exactly (the product is zero), 16-bit outputs: each output is the exact activation
+    rounded to the output type, give or take the form's bound above (and one rounding step for the
+    value that bound moves it to).  With fp16 outputs the normalised metric (D = |z|, times
+    max|act'|) stays within the 16-bit tolerance everywhere; a bf16 output's own rounding (up to
+    2^-8 of the value) exceeds it where the output is close to |z|, whatever the activation."""
+    g = cuda_lib
+    M, N, K = 128, 4096, 64
+    a = torch.zeros(M, K)
+    b = torch.zeros(K, N)
+    bias = torch.linspace(-12.0, 12.0, N, dtype=torch.float32)
+    ab = wl.BF16
+    p = wl.make_problem("act_range16", M, N, K, ab, out, a, b, alpha=1.0, beta=0.0, bias=bias, epilogue=epi)
+    # a misaligned A base sends the call to the CUDA-core kernel
+    r = run_gemm(g, p, use_workspace=False, a_elem_offset=1 if kernel == "simt" else 0)
+    assert r.status == 0 and r.path == (g.PATH_SIMT if kernel == "simt" else g.PATH_TCGEN05)
+    got = r.values()
+    z = bias.double().numpy()
+    want = ALL_REF[epi](z)[None, :]
+    ulp = 2.0 ** -10 if out == wl.F16 else 2.0 ** -7          # one unit in the last place, relative
+    bound = ulp * np.abs(want) + LOW_FORM_BOUND[epi] * np.abs(z)[None, :] + 1e-30
+    err = np.abs(got - want)
+    assert np.all(err <= bound), float((err / bound).max())
+    if out == wl.F16:
+        D = np.broadcast_to(np.abs(z)[None, :], got.shape)
+        assert oracle.max_normalized_error(got, want, D, epi) <= oracle.tolerance(ab, out)

@@ -297,6 +297,9 @@ def test_gelu_accuracy_over_range(cuda_lib, ab):
     err = np.abs(got - want)
     assert float(err.max()) <= 2e-7 * 9, float(err.max())
     assert np.all(err <= 1e-7 + 4e-7 * np.abs(z)[None, :])
+    # and the stated metric itself: normalised error with D = |z| (times max|GELU'|) within 1e-5
+    D = np.broadcast_to(np.abs(z)[None, :], got.shape)
+    assert oracle.max_normalized_error(got, want, D, wl.EPI_BIAS_GELU) <= 1e-5
 
 
 # ---------------------------------------------------------------- stream-K --
