@@ -65,12 +65,55 @@ def _args(argv=None):
     ap.add_argument("--samples", default=None,
                     help="file for the per-call samples of every cell (default: gpurun_out/bench_samples.json "
                          "when that folder exists)")
+    ap.add_argument("--profile", default=None, metavar="CASE",
+                    help="run only CASE's workload --warmup + --steps times, untimed, for a profiler: "
+                         + ", ".join(sorted(PROFILE_CASES)))
     ap.add_argument("--q4-decode", type=int, default=0, metavar="M",
                     help="only the quantized decode cell with M rows of x (for profiling); prints its JSON")
     ap.add_argument("--q4-reps", type=int, default=50, help="timed calls of the --q4-decode cell")
     ap.add_argument("--q4-kernel", choices=("auto", "ffma", "mma"), default="auto",
                     help="decode kernel of the --q4-decode cell")
     return ap.parse_args(argv)
+
+
+# Workloads --profile runs (the cells' problems), by name.
+PROFILE_CASES = {
+    "headline": lambda wl: wl.fp16_alpha_beta(4096),
+    "gelu_M512": lambda wl: wl.bf16_bias_gelu(512), "gelu_M2048": lambda wl: wl.bf16_bias_gelu(2048),
+    "gelu_M8192": lambda wl: wl.bf16_bias_gelu(8192),
+    "none_M2048": lambda wl: wl.bf16_bias_gelu(2048, epilogue=wl.EPI_NONE),
+    "fp8_4096": lambda wl: wl.fp8_e4m3(4096), "fp8_8192": lambda wl: wl.fp8_e4m3(8192),
+    "bf16_8192": lambda wl: wl.bf16_nn_large(8192), "fp32_4096_NN": lambda wl: wl.fp32_layout("NN", 4096),
+    "mxfp8_4096": None, "mxfp4_4096": None,
+}
+
+
+def run_profile(a):
+    """--profile CASE: the case's calls back to back, nothing timed (for ncu)."""
+    import torch
+    import workloads as wl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import dense_gemm_epilogues_tcgen05_gb300 as g
+    stream = torch.cuda.current_stream()
+    calls = a.warmup + a.steps
+    if a.profile.startswith("mx"):
+        elem = wl.MX_E4M3 if a.profile.startswith("mxfp8") else wl.MX_E2M1
+        mx_cell(g, stream, elem, 4096, steps=max(1, calls // 2), warmup=calls - max(1, calls // 2))
+        info = g.gemm_last_launch()
+    else:
+        p = PROFILE_CASES[a.profile](wl)
+        sets = _make_sets(p, 2, dev)
+        for i in range(calls):
+            _call(g, p, sets[i % 2], stream)
+        torch.cuda.synchronize()
+        info = g.gemm_last_launch()
+    st = g.gemm_device_status()
+    print(json.dumps({"profile": a.profile, "calls": calls, "status": st, "launch": info}), flush=True)
+    if st != 0:
+        raise SystemExit(1)
 
 
 def workload_config(n):
@@ -857,7 +900,11 @@ def main(argv=None):
         raise SystemExit(2)
     if a.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if a.q4_decode:
+    if a.profile:
+        if a.profile not in PROFILE_CASES:
+            raise SystemExit(f"unknown --profile case {a.profile}")
+        run_profile(a)
+    elif a.q4_decode:
         import torch
         import dense_gemm_epilogues_tcgen05_gb300 as g
         g.gemm_set_q4_kernel({"auto": g.Q4_AUTO, "ffma": g.Q4_FFMA, "mma": g.Q4_MMA}[a.q4_kernel])

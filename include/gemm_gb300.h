@@ -374,6 +374,9 @@ gemm_status_t gemm_last_launch(gemm_launch_info_t *info);
  *   - A device with more than 80 pairs of SMs needs a larger stream-K
  *     workspace than the array holds: such calls return GEMM_ERR_WORKSPACE
  *     (use gemm() with a workspace there).
+ *   - fp32 inputs run on the CUDA-core FFMA kernel here, as gemm() without a
+ *     workspace does: the 3xTF32 split needs a workspace that grows with M,
+ *     N and K, which no fixed array can hold (about 8x slower at 4096^3).
  *   - Other errors as gemm().
  */
 gemm_status_t gemm_builtin_scratch(int64_t M, int64_t N, int64_t K,
