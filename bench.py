@@ -690,6 +690,8 @@ def extra_cells(g, stream, peaks):
     cells["baseline_gate_fp16_4096"] = baseline_gate(g, stream, l2)
     for M in (1, 2, 8):
         cells[f"q4_decode_M{M}"] = q4_decode_cell(g, stream, M, compact=True)
+    for M in (64, 4096):
+        cells[f"q4_prefill_M{M}"] = q4_prefill_cell(g, stream, M)
     # block-scaled MXFP8 / MXFP4, against 2x (fp8) and the fp4 rate
     mx = {}
     for nm, elem in (("mxfp8", wl.MX_E4M3), ("mxfp4", wl.MX_E2M1)):
@@ -768,6 +770,53 @@ def mx_cell(g, stream, elem, n, steps=30, warmup=3, name=None):
     return {"tflops": round(p.flops * steps / (total * 1e-3) / 1e12, 1), "ms": round(total / steps, 4),
             "per_call": {"median": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)]}, "n": steps,
             "status": st}
+
+
+def q4_prefill_cell(g, stream, M, N=4096, K=4096, steps=20):
+    """Prefill with 4-bit weights: gemm_q4 with M rows of x (the tensor-core kernel, W
+    dequantised into tensor memory) against the unfused path, gemm_q4_dequantize then
+    gemm() in each call, and against gemm() on a W dequantised once (the dense rate).
+    Seeded random codes / scales (as the decode cells), x ~ N(0,1) fp16, fp16 output;
+    TFLOP/s back to back."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(78)
+    wq = torch.randint(-2 ** 31, 2 ** 31 - 1, (N * K // 8,), dtype=torch.int32, device=dev, generator=gen)
+    s = (torch.rand(N * K // 64, device=dev, generator=gen) * 3 + 1) * 2.0 ** -10
+    sb = torch.stack([s, -8 * s], dim=1).to(torch.float16).reshape(-1)
+    x = torch.randn(M * K, device=dev, generator=gen).to(torch.float16)
+    y = torch.empty(M * N, dtype=torch.float16, device=dev)
+    w_call = torch.empty(N * K, dtype=torch.float16, device=dev)
+    w_once = torch.empty(N * K, dtype=torch.float16, device=dev)
+    g.gemm_q4_dequantize(N, K, wq, sb, w_once, g.F16, stream=stream)
+    ws = _workspace(g, dev)
+    runs = {
+        "fused": lambda: g.gemm_q4(M, N, K, g.F16, x, K, wq, sb, y, N, g.F16, 1.0, 0.0, None, g.EPI_NONE,
+                                   stream=stream),
+        "dequantize_then_gemm": lambda: (g.gemm_q4_dequantize(N, K, wq, sb, w_call, g.F16, stream=stream),
+                                         g.gemm(M, N, K, g.F16, x, K, 1, w_call, 1, K, y, N, g.F16, 1.0, 0.0, None,
+                                                g.EPI_NONE, workspace=ws, workspace_bytes=ws.numel(), stream=stream)),
+        "gemm_on_dequantized_w": lambda: g.gemm(M, N, K, g.F16, x, K, 1, w_once, 1, K, y, N, g.F16, 1.0, 0.0, None,
+                                                g.EPI_NONE, workspace=ws, workspace_bytes=ws.numel(), stream=stream),
+    }
+    out = {"shape": f"{M}x{N}x{K}"}
+    for name, fn in runs.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        out[name] = {"tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 2)}
+    out["status"] = g.gemm_device_status()
+    del wq, sb, x, y, w_call, w_once
+    torch.cuda.empty_cache()
+    return out
 
 
 def q4_decode_cell(g, stream, M, N=16384, K=16384, reps=50, compact=False):

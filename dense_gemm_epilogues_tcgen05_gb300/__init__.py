@@ -275,7 +275,8 @@ def gemm_set_q4_kernel(kind) -> int:
 
 def gemm_q4(M, N, K, x_dtype, X, ldx, Wq, scale_bias, C, ldc, c_dtype, alpha, beta, bias, epilogue,
             stream=None) -> int:
-    """C = cast(epilogue(alpha * x W^T + beta*C + bias)) with 4-bit group-quantized W (decode, M <= 8)."""
+    """C = cast(epilogue(alpha * x W^T + beta*C + bias)) with 4-bit group-quantized W: decode kernels for
+    M <= 8 rows of x, the tensor-core prefill kernel (dequantisation fused in) beyond."""
     st = lib.gemm_q4(M, N, K, x_dtype, _ptr(X), ldx, _ptr(Wq), _ptr(scale_bias), _ptr(C), ldc, c_dtype, alpha,
                      beta, _ptr(bias), epilogue, _stream(stream))
     return _check(st, "gemm_q4")

@@ -998,7 +998,7 @@ gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, con
     if (c_dtype == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
     if (K % 64 != 0) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
-    if (M > kQ4MaxRows) return GEMM_ERR_UNSUPPORTED;
+    if (M > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
     if (epilogue != GEMM_EPI_NONE && bias == nullptr) return GEMM_ERR_INVALID_ARG;
     const bool reads_x = K > 0 && alpha != 0.0f;
@@ -1029,6 +1029,32 @@ gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, con
     a.Wq = Wq;
     a.SB = static_cast<const uint32_t *>(scale_bias);
     a.status = dev->status;
+    if (M > kQ4MaxRows) {
+        // Prefill: the tensor-core product with W dequantised into tensor memory.
+        CUtensorMap tmX, tmW;
+        if ((st = encode_2d(&tmX, x_dtype, X, K, M, ldx, 64, 128)) != GEMM_OK) return st;
+        cuuint64_t wdims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
+        cuuint64_t wstrides[1] = {static_cast<cuuint64_t>(K / 2)};
+        cuuint32_t wbox[2] = {32u, 128u};
+        cuuint32_t westr[2] = {1, 1};
+        if (driver_fns().encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(Wq), wdims, wstrides,
+                                wbox, westr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return GEMM_ERR_CUDA;
+        const long long tiles = ((N + 127) / 128) * ((M + 127) / 128);
+        const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
+        gemm_launch_info_t info = {};
+        info.path = GEMM_PATH_TCGEN05;
+        info.kind = 1;
+        info.bn = 128;
+        info.transposed = 1;
+        info.cluster_ctas = 1;
+        info.grid_ctas = grid;
+        info.tiles = static_cast<int>(tiles);
+        return record(launch_q4_prefill(x_dtype, c_dtype, tmX, tmW, a, grid, s) == cudaSuccess ? GEMM_OK
+                                                                                                : GEMM_ERR_CUDA,
+                      info);
+    }
     const int kind = t_tuning.q4_kernel;
     if (!(kind == GEMM_Q4_MMA || (kind == GEMM_Q4_AUTO && q4_auto_mma(M))))
         return launch_q4_gemv(x_dtype, c_dtype, nullptr, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

@@ -155,6 +155,10 @@ constexpr int kQ4MaxRows = 8;
 cudaError_t launch_q4_gemv(int x_dtype, int out, const CUtensorMap *tmW, const Q4Args &args, cudaStream_t stream);
 cudaError_t launch_q4_dequantize(int out, long long N, long long K, const uint32_t *Wq, const uint32_t *SB, void *W,
                                  cudaStream_t stream);
+//   4-bit prefill (more than kQ4MaxRows rows of x): x by a map over (K, M) with 64 x 128 boxes
+//   (128-byte swizzle), the codes by a map over (K/2 bytes, N) with 32 x 128 boxes; `grid` CTAs
+cudaError_t launch_q4_prefill(int x_dtype, int out, const CUtensorMap &tmX, const CUtensorMap &tmW, const Q4Args &args,
+                              int grid, cudaStream_t stream);
 //   block-scaled product (one SM per 128 x 128 tile) and its scale-factor pack pre-pass:
 cudaError_t launch_mx(int elem, int out, const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs &args, int grid,
                       cudaStream_t stream);

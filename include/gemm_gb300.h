@@ -415,15 +415,19 @@ gemm_status_t gemm_bias_gelu(int64_t M, int64_t N, void *C, int64_t ldc, gemm_dt
 
 /*
  * gemm_q4 -- C = cast(epilogue(alpha * x W^T + beta*C + bias)) for M rows of
- * x (decode: 1 <= M <= 8; M == 0 or N == 0 is a no-op).
+ * x (M == 0 or N == 0 is a no-op).
  *   x_dtype     F16 or BF16.  X is M x ldx row-major, 16-byte aligned base,
  *               ldx >= K with ldx*2 a multiple of 16.
  *   K           a multiple of 64.
  *   C, c_dtype, ldc, alpha, beta, bias, epilogue: as in gemm(), with the
  *               output M x N and bias fp32[N]; the same fused epilogues.
- * Larger M: GEMM_ERR_UNSUPPORTED -- dequantise once with gemm_q4_dequantize
- * and call gemm() (the dense tensor-core path), which is how this library
- * does prefill.  Asynchronous on `stream`; errors as gemm().
+ * Decode (1 <= M <= 8) runs an HBM-streaming kernel (gemm_q4_kernel_t below).
+ * Prefill (M > 8) runs on the tensor cores with the dequantisation fused in:
+ * each 64-k group of W is expanded to x's 16-bit type, round(s*q + b), straight
+ * into tensor memory as the MMA's operand (never written to memory), and
+ * multiplied with x in fp32 accumulation -- the rounding of W that
+ * gemm_q4_dequantize followed by gemm() also has (at most 2^-11 of each |W|
+ * for F16 x, 2^-8 for BF16).  Asynchronous on `stream`; errors as gemm().
  */
 gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype,
                       const void *X, int64_t ldx,
@@ -476,7 +480,8 @@ gemm_status_t gemm_get_tuning(gemm_tuning_t *out);
  * gemm_q4_dequantize -- W[n][k] = round(s*q + b) into the N x K row-major
  * device array W of type w_dtype (F16 or BF16; 16-byte aligned), for
  * gemm(M, N, K, w_dtype, X, ldx, 1, W, 1, K, ...) to multiply (W^T as B,
- * K-contiguous).  The rounding to 16 bits is the only difference from the
+ * K-contiguous) -- the unfused alternative to gemm_q4's prefill, for a W
+ * used by many calls.  The rounding to 16 bits is the only difference from the
  * exact product: at most 2^-11 (F16) or 2^-8 (BF16) of each |W| value.
  * K a multiple of 64.  Asynchronous on `stream`; errors as gemm().
  */

@@ -91,11 +91,6 @@ def test_degenerate(cuda_lib):
     assert g.gemm_device_status() == 0
     y, _ = q4.q4_reference(**p.oracle_args())
     assert np.array_equal(C.cpu().numpy().reshape(2, -1)[:, :40], y.astype(np.float32))
-    # more than 8 rows is the dense path's job
-    with pytest.raises(g.GemmError) as e:
-        g.gemm_q4(9, 40, 128, wl.F16, p.X.cuda(), 128, p.Wq.cuda(), p.SB.cuda(), C, p.ldc, wl.F32, 1.0, 0.0, None,
-                  wl.EPI_NONE)
-    assert e.value.status == g.ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("M", [1, 8])
@@ -142,4 +137,69 @@ def test_prefill_dequantize_then_gemm(cuda_lib):
     g.gemm(M, N, K, wl.F16, p.X.cuda(), K, 1, W, 1, K, C, p.ldc, wl.F16, 1.0, 0.0, None, wl.EPI_NONE)
     assert g.gemm_device_status() == 0
     res = q4.check(p.oracle_args(), C.cpu().view(torch.int16).numpy())
+    assert res["pass"], res
+
+
+# --------------------------------------------------------------- prefill --
+# More than 8 rows of x: the tensor-core kernel with W dequantised into tensor
+# memory ("X3: Metal GEMM" section 7: the prefill GEMM with the dequantisation
+# fused into the multiply-accumulate).
+
+
+@pytest.mark.parametrize("M,N,K", [(9, 64, 64), (128, 128, 128), (200, 129, 1088), (384, 300, 320),
+                                   (1000, 520, 2048)], ids=lambda v: str(v))
+@pytest.mark.parametrize("xd", [wl.F16, wl.BF16], ids=["f16", "bf16"])
+def test_prefill_integer_exact(cuda_lib, M, N, K, xd):
+    """Integer problems (W = s*q + b up to 30, x in -2..2: W exact in 16 bits, sums exact in
+    fp32): bit-exact, at ragged M and N (tiles of 128 x 128 part-filled) and K from one group up."""
+    g = cuda_lib
+    p = wl.q4_problem(300 + M + N + K, M, N, K, xd, wl.F32, integer=True, ldc_pad=5)
+    out = run_q4(g, p)
+    info = g.gemm_last_launch()
+    assert info["path"] == g.PATH_TCGEN05 and info["transposed"] == 1
+    y, _ = q4.q4_reference(**p.oracle_args())
+    got = oracle.output_values(out, p.M, p.N, p.ldc, p.c_dtype)
+    bad = np.argwhere(got != y)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:3].tolist()}: {got[tuple(bad[0])]} vs {y[tuple(bad[0])]}"
+
+
+@pytest.mark.parametrize("cd", [wl.F16, wl.BF16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("epi", [wl.EPI_NONE, wl.EPI_BIAS, wl.EPI_BIAS_GELU, wl.EPI_BIAS_SILU],
+                         ids=["none", "bias", "gelu", "silu"])
+def test_prefill_realistic_tolerance(cuda_lib, cd, epi):
+    """Realistic quantised layers at the 16-bit-output tolerance.  W is rounded to x's 16-bit type
+    (at most 2^-11 of |W| for F16 x), which an fp32 output's 1e-5 does not absorb; the fp32 output
+    is compared with the unfused path, which rounds W alike (next test)."""
+    g = cuda_lib
+    for M, xd in ((512, wl.F16), (300, wl.BF16)):
+        p = wl.q4_problem(17 + M, M, 768, 2048, xd, cd, alpha=1.25, beta=0.5 if epi == wl.EPI_NONE else 0.0,
+                          epilogue=epi)
+        res = q4.check(p.oracle_args(), run_q4(g, p))
+        assert res["pass"], (M, res)
+
+
+def test_prefill_matches_dequantize_then_gemm(cuda_lib):
+    """The fused prefill and the unfused path (dequantise to fp16, then gemm()) round W alike: their
+    outputs agree within fp32 summation order on fp32 outputs."""
+    g = cuda_lib
+    M, N, K = 640, 512, 4096
+    p = wl.q4_problem(62, M, N, K, wl.F16, wl.F32)
+    fused = oracle.output_values(run_q4(g, p), M, N, p.ldc, wl.F32)
+    W = torch.empty(N * K, dtype=torch.float16, device="cuda")
+    g.gemm_q4_dequantize(N, K, p.Wq.cuda(), p.SB.cuda(), W, wl.F16)
+    C = torch.zeros(M * N, dtype=torch.float32, device="cuda")
+    g.gemm(M, N, K, wl.F16, p.X.cuda(), K, 1, W, 1, K, C, N, wl.F32, 1.0, 0.0, None, wl.EPI_NONE)
+    assert g.gemm_device_status() == 0
+    unfused = C.cpu().numpy().reshape(M, N).astype(np.float64)
+    _, D = q4.q4_reference(**p.oracle_args())
+    assert oracle.max_normalized_error(fused, unfused, D, wl.EPI_NONE) <= 1e-5
+
+
+def test_prefill_large_sampled_rows(cuda_lib):
+    """A 4096 x 4096 x 4096 prefill on sampled rows of x."""
+    from gpu_util import sample_rows
+    g = cuda_lib
+    p = wl.q4_problem(71, 4096, 4096, 4096, wl.BF16, wl.BF16)
+    out = run_q4(g, p)
+    res = q4.check(p.oracle_args(), out, rows=sample_rows(4096, n_random=96))
     assert res["pass"], res
