@@ -84,7 +84,7 @@ PROFILE_CASES = {
     "none_M2048": lambda wl: wl.bf16_bias_gelu(2048, epilogue=wl.EPI_NONE),
     "fp8_4096": lambda wl: wl.fp8_e4m3(4096), "fp8_8192": lambda wl: wl.fp8_e4m3(8192),
     "bf16_8192": lambda wl: wl.bf16_nn_large(8192), "fp32_4096_NN": lambda wl: wl.fp32_layout("NN", 4096),
-    "mxfp8_4096": None, "mxfp4_4096": None,
+    "mxfp8_4096": None, "mxfp4_4096": None, "q4_prefill_8192": None,
 }
 
 
@@ -99,7 +99,10 @@ def run_profile(a):
     import dense_gemm_epilogues_tcgen05_gb300 as g
     stream = torch.cuda.current_stream()
     calls = a.warmup + a.steps
-    if a.profile.startswith("mx"):
+    if a.profile == "q4_prefill_8192":
+        q4_prefill_cell(g, stream, 8192, steps=max(1, calls - 3))
+        info = g.gemm_last_launch()
+    elif a.profile.startswith("mx"):
         elem = wl.MX_E4M3 if a.profile.startswith("mxfp8") else wl.MX_E2M1
         mx_cell(g, stream, elem, 4096, steps=max(1, calls // 2), warmup=calls - max(1, calls // 2))
         info = g.gemm_last_launch()
