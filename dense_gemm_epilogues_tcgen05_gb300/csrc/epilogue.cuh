@@ -184,13 +184,17 @@ __device__ __forceinline__ float relu(float z) { return z < 0.0f ? 0.0f : z; }
 // --- cheaper forms for 16-bit outputs -----------------------------------------
 // A 16-bit output rounds to 2^-9 (bf16) or 2^-12 (fp16) of its value, and its
 // tolerance is 2e-3 of the error scale D >= |z|; the forms below stay within
-// 3e-4 |z| of the exact activation and cost no more than one special-function
+// 4e-4 |z| of the exact activation (about a tenth of the output's unit in the
+// last place, relative to |z|) and cost no more than one special-function
 // operation per element (the accurate forms above cost two).  They serve F16
 // and BF16 outputs only, and not when the call keeps an amax (a reduction held
 // to the fp32 tolerance): fp32 and E4M3 outputs and amax calls take the
-// accurate forms.
+// accurate forms.  Every instruction per element shows in the fused cost even
+// where the epilogue overlaps the next tile's main loop (its warps share the
+// issue slots of the MMA and TMA warps), so each form also has a two-lane
+// variant that runs its multiply-adds as f32x2.
 //
-// GELU (erf form): Phi(z) - 1/2 = z P(z^2) on |z| <= 4 (z clamped beyond;
+// GELU (erf form) for F16 outputs: Phi(z) - 1/2 = z P(z^2) on |z| <= 4 (z clamped beyond;
 // Phi(4) = 1 - 3.2e-5), P of degree 6 with the coefficients of a near-minimax
 // fit of the absolute error in Phi (fit_gelu_poly.py beside the package's
 // sources: least squares in the Chebyshev basis, reweighted towards the
@@ -242,6 +246,34 @@ __device__ __forceinline__ float tanh_hw(float u) {
     return r;
 }
 
+// erf-GELU for BF16 outputs: Phi(z) ~ 1/2 + tanh(z (t1 + t3 z^2)) / 2, the
+// two coefficients minimax in the absolute error of Phi (1.4e-4; printed by
+// fit_gelu_poly.py beside the package's sources), with the hardware tanh
+// (at most 2.5e-4 more): at most 3.9e-4 |z| in GELU, a tenth of a bf16
+// output's unit in the last place relative to |z|.  No clamp is needed (tanh
+// saturates), so it costs half the instructions of the polynomial, which
+// F16 outputs keep for their three extra bits.
+namespace gelu_t {
+constexpr float kT1 = 0.7988014221191406f, kT3 = 0.03528204932808876f;
+}  // namespace gelu_t
+
+__device__ __forceinline__ float gelu_erf_tanh(float z) {
+    const float s = z * z;
+    const float u = z * fmaf(gelu_t::kT3, s, gelu_t::kT1);
+    const float hz = 0.5f * z;
+    return fmaf(hz, tanh_hw(u), hz);
+}
+
+// The same operations on two values, two lanes per instruction.
+__device__ __forceinline__ void gelu_erf_tanh2(float &z0, float &z1) {
+    const uint64_t z = f2_pack(z0, z1);
+    const uint64_t s = f2_mul(z, z);
+    float u0, u1;
+    f2_unpack(f2_mul(z, f2_fma(f2_splat(gelu_t::kT3), s, f2_splat(gelu_t::kT1))), u0, u1);
+    const uint64_t hz = f2_mul(f2_splat(0.5f), z);
+    f2_unpack(f2_fma(hz, f2_pack(tanh_hw(u0), tanh_hw(u1)), hz), z0, z1);
+}
+
 // GELU (tanh form) with the hardware tanh: error up to 0.5 |z| 2^-11.
 __device__ __forceinline__ float gelu_tanh_hw(float z) {
     constexpr float kSqrt2OverPi = 0.79788456080286535588f;
@@ -250,10 +282,29 @@ __device__ __forceinline__ float gelu_tanh_hw(float z) {
     return fmaf(hz, tanh_hw(u), hz);
 }
 
+// The same operations on two values, two lanes per instruction.
+__device__ __forceinline__ void gelu_tanh_hw2(float &z0, float &z1) {
+    constexpr float kSqrt2OverPi = 0.79788456080286535588f;
+    const uint64_t z = f2_pack(z0, z1);
+    const uint64_t w = f2_fma(f2_mul(f2_splat(0.044715f), z), f2_mul(z, z), z);
+    float u0, u1;
+    f2_unpack(f2_mul(f2_splat(kSqrt2OverPi), w), u0, u1);
+    const uint64_t hz = f2_mul(f2_splat(0.5f), z);
+    f2_unpack(f2_fma(hz, f2_pack(tanh_hw(u0), tanh_hw(u1)), hz), z0, z1);
+}
+
 // SiLU as z sigmoid(z) = (z/2) (1 + tanh(z/2)) with the hardware tanh.
 __device__ __forceinline__ float silu_hw(float z) {
     const float hz = 0.5f * z;
     return fmaf(hz, tanh_hw(hz), hz);
+}
+
+// The same operations on two values, two lanes per instruction.
+__device__ __forceinline__ void silu_hw2(float &z0, float &z1) {
+    const uint64_t hz = f2_mul(f2_splat(0.5f), f2_pack(z0, z1));
+    float h0, h1;
+    f2_unpack(hz, h0, h1);
+    f2_unpack(f2_fma(hz, f2_pack(tanh_hw(h0), tanh_hw(h1)), hz), z0, z1);
 }
 
 // Whether output type OUT may take the cheaper forms.
@@ -267,7 +318,7 @@ template <int OUT>
 __device__ __forceinline__ float activate_one(float z, int epi, bool precise) {
     const bool kLow = kCheapActivation<OUT> && !precise;
     switch (epi) {
-    case kEpiBiasGelu: return kLow ? gelu_erf_poly(z) : gelu_erf(z);
+    case kEpiBiasGelu: return kLow ? (OUT == kDtBF16 ? gelu_erf_tanh(z) : gelu_erf_poly(z)) : gelu_erf(z);
     case kEpiBiasGeluTanh: return kLow ? gelu_tanh_hw(z) : gelu_tanh(z);
     case kEpiBiasSilu: return kLow ? silu_hw(z) : silu(z);
     case kEpiBiasRelu: return relu(z);
@@ -284,8 +335,13 @@ __device__ __forceinline__ void activate_run(float (&v)[32], int off, int epi, b
     const bool kLow = kCheapActivation<OUT> && !precise;
     if (epi == kEpiBiasGelu) {
         if (kLow) {
+            if constexpr (OUT == kDtBF16) {
 #pragma unroll
-            for (int j = 0; j < CNT; j += 2) gelu_erf_poly2(v[off + j], v[off + j + 1]);
+                for (int j = 0; j < CNT; j += 2) gelu_erf_tanh2(v[off + j], v[off + j + 1]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < CNT; j += 2) gelu_erf_poly2(v[off + j], v[off + j + 1]);
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < CNT; j += 2) gelu_erf2(v[off + j], v[off + j + 1]);
@@ -296,7 +352,7 @@ __device__ __forceinline__ void activate_run(float (&v)[32], int off, int epi, b
     } else if (epi == kEpiBiasSilu) {
         if (kLow) {
 #pragma unroll
-            for (int j = 0; j < CNT; ++j) v[off + j] = silu_hw(v[off + j]);
+            for (int j = 0; j < CNT; j += 2) silu_hw2(v[off + j], v[off + j + 1]);
         } else {
 #pragma unroll
             for (int j = 0; j < CNT; ++j) v[off + j] = silu(v[off + j]);
@@ -304,7 +360,7 @@ __device__ __forceinline__ void activate_run(float (&v)[32], int off, int epi, b
     } else if (epi == kEpiBiasGeluTanh) {
         if (kLow) {
 #pragma unroll
-            for (int j = 0; j < CNT; ++j) v[off + j] = gelu_tanh_hw(v[off + j]);
+            for (int j = 0; j < CNT; j += 2) gelu_tanh_hw2(v[off + j], v[off + j + 1]);
         } else {
 #pragma unroll
             for (int j = 0; j < CNT; ++j) v[off + j] = gelu_tanh(v[off + j]);
@@ -786,7 +842,7 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
             if (e.beta != 0.0f) {
                 if (lane == 0) {
                     mbar_arrive_expect_tx(cbar, kStageBoxBytes);
-                    tma_load_2d(buf, tmC, cbar, row0, col0);
+                    tma_load_2d_hint(buf, tmC, cbar, row0, col0, l2_policy_evict_first());
                 }
                 const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
                 if (!__all_sync(0xffffffffu, got)) return false;
@@ -796,7 +852,7 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d(tmC, buf, row0, col0);
+                tma_store_2d_hint(tmC, buf, row0, col0, l2_policy_evict_first());
                 bulk_commit();
             }
             return true;
@@ -811,7 +867,7 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
         if (e.beta != 0.0f) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(cbar, kStageBoxBytes);
-                tma_load_2d(buf, tmC, cbar, x, row0);
+                tma_load_2d_hint(buf, tmC, cbar, x, row0, l2_policy_evict_first());
             }
             const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
             if (!__all_sync(0xffffffffu, got)) return false;
@@ -821,7 +877,7 @@ __device__ __forceinline__ bool epilogue_chunk32_tma(float (&v)[32], int col0, i
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(tmC, buf, x, row0);
+            tma_store_2d_hint(tmC, buf, x, row0, l2_policy_evict_first());
             bulk_commit();
         }
     }
@@ -875,7 +931,8 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
                 if (lane == 0) {
                     mbar_arrive_expect_tx(cbar, static_cast<uint32_t>(nvalid) * kStageBoxBytes);
                     for (int i = 0; i < nvalid; ++i)
-                        tma_load_2d(area + i * kStageBoxBytes, tmC, cbar, row0, col_base + i * 32);
+                        tma_load_2d_hint(area + i * kStageBoxBytes, tmC, cbar, row0, col_base + i * 32,
+                                         l2_policy_evict_first());
                 }
                 const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
                 if (!__all_sync(0xffffffffu, got)) return false;
@@ -896,7 +953,8 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(tmC, area + i * kStageBoxBytes, row0, col_base + i * 32);
+                    tma_store_2d_hint(tmC, area + i * kStageBoxBytes, row0, col_base + i * 32,
+                                      l2_policy_evict_first());
                     bulk_commit();
                 }
             }
@@ -914,7 +972,9 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
             for (int i = 0; i < nvalid; ++i)
                 for (int h = 0; h < NSUB; ++h) {
                     const int x = col_base + i * 32 + h * PER;
-                    if (x < e.N) tma_load_2d(area + (i * NSUB + h) * kStageBoxBytes, tmC, cbar, x, row0);
+                    if (x < e.N)
+                        tma_load_2d_hint(area + (i * NSUB + h) * kStageBoxBytes, tmC, cbar, x, row0,
+                                         l2_policy_evict_first());
                 }
         }
         const bool got = mbar_wait_bounded(cbar, cphase, abort_flag, status);
@@ -944,7 +1004,8 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
 #pragma unroll
             for (int h = 0; h < NSUB; ++h) {
                 const int x = col_base + i * 32 + h * PER;
-                if (x < e.N) tma_store_2d(tmC, area + (i * NSUB + h) * kStageBoxBytes, x, row0);
+                if (x < e.N)
+                    tma_store_2d_hint(tmC, area + (i * NSUB + h) * kStageBoxBytes, x, row0, l2_policy_evict_first());
             }
             bulk_commit();
         }

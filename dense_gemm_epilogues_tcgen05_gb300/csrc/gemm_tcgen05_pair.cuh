@@ -170,9 +170,15 @@ __device__ __forceinline__ long long partial_index(int ci, int q, int r) {
 }
 
 // PART epilogue: this thread's raw fp32 accumulators of chunks c0 .. c0+n-1 to
-// its cluster's partial slot (coalesced 16-byte stores, L2 only).
+// its cluster's partial slot (coalesced 16-byte stores, L2 only).  The slot is
+// read once, by the tile's owner a few tiles' time later, and then dropped
+// from L2 (owner_row_chunks), so its lines are the last L2 evicts: written
+// with the ordinary priority, operand panels and C pushed many of them out to
+// HBM before the owner came (with both measures, a 4096^3 launch moves 157
+// instead of 172 MB through DRAM).
 __device__ __forceinline__ void store_partial_chunks(uint32_t t_base, int c0, int n, int r, float *slot) {
     if (n <= 0) return;
+    const uint64_t pol = l2_policy_evict_last();
     uint32_t ra[32], rb[32];
     __syncwarp();
     tmem_ld_issue(t_base, ra);
@@ -188,7 +194,7 @@ __device__ __forceinline__ void store_partial_chunks(uint32_t t_base, int c0, in
         for (int q = 0; q < 8; ++q) {
             const float4 v = make_float4(__uint_as_float(cur[4 * q]), __uint_as_float(cur[4 * q + 1]),
                                          __uint_as_float(cur[4 * q + 2]), __uint_as_float(cur[4 * q + 3]));
-            __stcg(reinterpret_cast<float4 *>(slot + partial_index(c0 + i, q, r)), v);
+            st_global_cg_v4_hint(slot + partial_index(c0 + i, q, r), v, pol);
         }
         __syncwarp();
         if (more) tmem_ld_wait(nxt);
@@ -197,7 +203,10 @@ __device__ __forceinline__ void store_partial_chunks(uint32_t t_base, int c0, in
 
 // OWNER epilogue: like epilogue_row_chunks, with the partial sums of
 // `ncontrib` later clusters (slots slot0, slot0 + slot_stride, ...) added to
-// the accumulators before alpha / beta / bias / GELU / cast.
+// the accumulators before alpha / beta / bias / GELU / cast.  Each partial
+// line is discarded from L2 once the warp has added it: the slot is scratch
+// that the next writer fills again, so it never needs to reach HBM.  Slots
+// are 128-byte aligned (the workspace is 256-byte aligned, a slot 128 KB).
 // With e.c_tma the chunks go through the warp's staged C box (rows row0 ..
 // row0+31, row0 < M) instead.  Returns false if a wait for C gave up.
 template <int OUT, bool SC>
@@ -228,6 +237,20 @@ __device__ __forceinline__ bool owner_row_chunks(uint32_t t_base, int col_base, 
                 const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + partial_index(c0 + i, q, r)));
                 v[4 * q] += p.x; v[4 * q + 1] += p.y; v[4 * q + 2] += p.z; v[4 * q + 3] += p.w;
             }
+        }
+        // A value that needs every partial load of this chunk, consumed before
+        // the warp converges: past the __syncwarp no lane has a load of the
+        // lines below outstanding.
+        float dep = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dep += v[4 * q];
+        asm volatile("" ::"f"(dep));
+        __syncwarp();
+        if ((r & 7) == 0) {  // lanes 0, 8, 16, 24: one 128-byte line each of the warp's 512 bytes
+#pragma unroll 1
+            for (int k = 0; k < ncontrib; ++k)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) discard_l2_line(slot0 + k * slot_stride + partial_index(c0 + i, q, r));
         }
         const int col0 = col_base + i * 32;
         // E4M3 outputs never move through shared memory (the host gives them no C map).
@@ -333,6 +356,7 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             // ------------------------------------------------ TMA producer --
             uint32_t stage = 0, phase = 0;
             bool ok = true, issued = false;
+            const uint64_t pol_ab = l2_policy_evict_last();
             SegmentIter it(args, cluster, nclusters);
             Segment seg;
             while (ok && it.next(seg)) {
@@ -359,34 +383,35 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
                     const int k0 = kb * BK;
                     if constexpr (Cfg::X3) {
                         // hi and lo halves of the stacked K-major arrays
-                        tma_load_2d_pair(sA, &tmA, fbar, k0, m0);
-                        tma_load_2d_pair(sA + Cfg::A_LO, &tmA, fbar, k0, m0 + args.lo_row_a);
-                        tma_load_2d_pair(sB, &tmB, fbar, k0, n0);
-                        tma_load_2d_pair(sA + Cfg::B_LO, &tmB, fbar, k0, n0 + args.lo_row_b);
+                        tma_load_2d_pair(sA, &tmA, fbar, k0, m0, pol_ab);
+                        tma_load_2d_pair(sA + Cfg::A_LO, &tmA, fbar, k0, m0 + args.lo_row_a, pol_ab);
+                        tma_load_2d_pair(sB, &tmB, fbar, k0, n0, pol_ab);
+                        tma_load_2d_pair(sA + Cfg::B_LO, &tmB, fbar, k0, n0 + args.lo_row_b, pol_ab);
                     } else if constexpr (CL == 4) {
                         // This CTA's share of the A rows, delivered to both pairs.
                         const uint16_t amask = static_cast<uint16_t>((1u << prank) | (4u << prank));
                         if (!args.a_mn_major) {
                             tma_load_2d_pair_mc(sA + pidx * (BM / 2) * 128, &tmA, fbar, k0,
-                                                m0 + static_cast<int>(pidx) * (BM / 2), amask);
+                                                m0 + static_cast<int>(pidx) * (BM / 2), amask, pol_ab);
                         } else {
                             // BM / SWZ boxes of SWZ rows; the host runs this only when that is even.
                             for (int j = static_cast<int>(pidx); j < BM / SWZ; j += PAIRS)
-                                tma_load_2d_pair_mc(sA + j * 128 * BK, &tmA, fbar, m0 + j * SWZ, k0, amask);
+                                tma_load_2d_pair_mc(sA + j * 128 * BK, &tmA, fbar, m0 + j * SWZ, k0, amask,
+                                                    pol_ab);
                         }
                     } else if (!args.a_mn_major) {
-                        tma_load_2d_pair(sA, &tmA, fbar, k0, m0);
+                        tma_load_2d_pair(sA, &tmA, fbar, k0, m0, pol_ab);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / SWZ; ++j)
-                            tma_load_2d_pair(sA + j * 128 * BK, &tmA, fbar, m0 + j * SWZ, k0);
+                            tma_load_2d_pair(sA + j * 128 * BK, &tmA, fbar, m0 + j * SWZ, k0, pol_ab);
                     }
                     if constexpr (!Cfg::X3) {
                         if (!args.b_mn_major) {
-                            tma_load_2d_pair(sB, &tmB, fbar, k0, n0);
+                            tma_load_2d_pair(sB, &tmB, fbar, k0, n0, pol_ab);
                         } else {
                             for (int j = 0; j * SWZ < bnh; ++j)
-                                tma_load_2d_pair(sB + j * 128 * BK, &tmB, fbar, n0 + j * SWZ, k0);
+                                tma_load_2d_pair(sB + j * 128 * BK, &tmB, fbar, n0 + j * SWZ, k0, pol_ab);
                         }
                     }
                     if (++stage == STAGES) {

@@ -116,6 +116,30 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// L2 eviction priorities for the cache-hint forms of the bulk copies: C is
+// touched once per launch (read for beta*C, then written), so its lines go
+// first; operand panels are read again by other tiles, so theirs go last.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_2d with an L2 eviction policy for the bytes it reads.
+__device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
 // 2-D tiled store of one box from this CTA's shared memory to global memory,
 // tracked by the issuing thread's bulk async-groups.  Box elements outside
 // the tensor are not written.
@@ -124,6 +148,28 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
                      reinterpret_cast<uint64_t>(map)),
                  "r"(smem_u32(smem_src)), "r"(x), "r"(y)
                  : "memory");
+}
+
+// tma_store_2d with an L2 eviction policy for the bytes it writes.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, const void *smem_src, int32_t x, int32_t y,
+                                                  uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y), "l"(policy)
+                 : "memory");
+}
+
+// 16-byte store to global memory, cached in L2 only, with an L2 eviction policy.
+__device__ __forceinline__ void st_global_cg_v4_hint(float *p, const float4 &v, uint64_t policy) {
+    asm volatile("st.global.cg.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
+}
+
+// Drop the 128-byte L2 line at p (128-byte aligned) without writing it back:
+// its bytes become undefined.  For scratch whose last reader is done with it.
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
 // Untiled bulk copy global -> this CTA's shared memory, counted as `bytes`
@@ -410,12 +456,13 @@ __device__ __forceinline__ void sleep_ns(uint32_t ns) { asm volatile("nanosleep.
 
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA (cluster address).
+// `policy`: the L2 eviction policy of the bytes read (l2_policy_*).
 __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map, uint32_t bar_cluster_addr,
-                                                 int32_t x, int32_t y) {
+                                                 int32_t x, int32_t y, uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y)
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y), "l"(policy)
         : "memory");
 }
 
@@ -426,11 +473,11 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
 // leader's barrier when that address is a leader's).
 __device__ __forceinline__ void tma_load_2d_pair_mc(void *smem_dst, const CUtensorMap *map,
                                                     uint32_t bar_cluster_addr, int32_t x, int32_t y,
-                                                    uint16_t cta_mask) {
+                                                    uint16_t cta_mask, uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(cta_mask)
+        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
         : "memory");
 }
 

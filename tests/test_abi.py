@@ -248,7 +248,6 @@ def test_q4_validation_without_gpu(g):
         return g.gemm_q4(M, N, K, g.F16 if xd is None else xd, X, ldx, W, SB, C, N, g.F16 if cd is None else cd,
                          1.0, 0.0, bias, g.EPI_NONE if epi is None else epi, stream=0)
     for kwargs, status in [(dict(K=100), g.ERR_INVALID_ARG),             # K not a multiple of 64
-                           (dict(M=9), g.ERR_UNSUPPORTED),               # decode only
                            (dict(xd=g.F32), g.ERR_UNSUPPORTED),
                            (dict(xd=g.E4M3), g.ERR_UNSUPPORTED),
                            (dict(cd=g.E4M3), g.ERR_UNSUPPORTED),

@@ -94,10 +94,12 @@ def test_activation_accuracy_over_range(cuda_lib, epi, ab):
 ALL_ACTS = [wl.EPI_BIAS_GELU, wl.EPI_BIAS_GELU_TANH, wl.EPI_BIAS_SILU, wl.EPI_BIAS_RELU]
 ALL_REF = {**REF, wl.EPI_BIAS_GELU: oracle.gelu}
 # How far the low-precision-output forms may stray from the exact activation, as a multiple of
-# |z|: the degree-6 polynomial normal CDF of erf-GELU (1.1e-4 in Phi), the hardware tanh of the
-# tanh-GELU and SiLU forms (relative error about 2^-11, times |z|/2), ReLU exact.
-LOW_FORM_BOUND = {wl.EPI_BIAS_GELU: 1.2e-4, wl.EPI_BIAS_GELU_TANH: 3e-4, wl.EPI_BIAS_SILU: 3e-4,
-                  wl.EPI_BIAS_RELU: 0.0}
+# |z|: erf-GELU through the degree-6 polynomial normal CDF for F16 outputs (1.1e-4 in Phi) and
+# through the fitted tanh form for BF16 outputs (1.41e-4 in Phi, plus the hardware tanh's relative
+# error of about 2^-11 times 1/2: 3.9e-4), the hardware tanh of the tanh-GELU and SiLU forms
+# (relative error about 2^-11, times |z|/2), ReLU exact.
+LOW_FORM_BOUND = {(wl.EPI_BIAS_GELU, wl.F16): 1.2e-4, (wl.EPI_BIAS_GELU, wl.BF16): 4e-4,
+                  wl.EPI_BIAS_GELU_TANH: 3e-4, wl.EPI_BIAS_SILU: 3e-4, wl.EPI_BIAS_RELU: 0.0}
 
 
 @pytest.mark.parametrize("epi", ALL_ACTS, ids=["gelu"] + ACT_IDS)
@@ -123,7 +125,8 @@ def test_low_precision_output_activations_over_range(cuda_lib, epi, out, kernel)
     z = bias.double().numpy()
     want = ALL_REF[epi](z)[None, :]
     ulp = 2.0 ** -10 if out == wl.F16 else 2.0 ** -7          # one unit in the last place, relative
-    bound = ulp * np.abs(want) + LOW_FORM_BOUND[epi] * np.abs(z)[None, :] + 1e-30
+    form = LOW_FORM_BOUND[(epi, out)] if epi == wl.EPI_BIAS_GELU else LOW_FORM_BOUND[epi]
+    bound = ulp * np.abs(want) + form * np.abs(z)[None, :] + 1e-30
     err = np.abs(got - want)
     assert np.all(err <= bound), float((err / bound).max())
     if out == wl.F16:
