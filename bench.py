@@ -455,6 +455,36 @@ def cell(g, p, steps, warmup, stream, n_sets=None, baseline=None, mode="fused", 
             "per_call": {"median": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)]}, "n": steps}
 
 
+def interleaved_modes(g, p, modes, calls, rounds, stream, l2=L2_BYTES, name=None):
+    """Time problem p in each of `modes` ("fused": its epilogue; "none": the plain GEMM; "decomposed":
+    the plain GEMM, then the separate bias+GELU pass) in `rounds` alternating rounds, each mode
+    `calls` calls back to back between one event pair per round, on the same inputs (rotated
+    through more than L2).  Per mode: the median rate over rounds, and the per-call median and
+    bootstrap CI from one pass with events around every call."""
+    import torch
+    sets = _make_sets(p, sets_beyond_l2(p, l2), torch.device("cuda", torch.cuda.current_device()))
+    rates = {m: [] for m in modes}
+    for r in range(rounds):
+        for m in (modes if r % 2 == 0 else modes[::-1]):
+            total = time_region(g, p, sets, calls, 3, stream, mode="plain" if m == "none" else m)
+            rates[m].append(p.flops * calls / (total * 1e-3) / 1e12)
+    out = {}
+    for m in modes:
+        per, _ = time_steps(g, p, sets, 30, 1, stream, mode="plain" if m == "none" else m)
+        tf = [p.flops / (t * 1e-3) / 1e12 for t in per]
+        med, ci = bootstrap_ci(tf)
+        if name is not None:
+            SAMPLES[f"{name}_{m}"] = [round(x, 2) for x in tf]
+        rate = statistics.median(rates[m])
+        out[m] = {"tflops": round(rate, 1), "ms": round(p.flops / (rate * 1e12) * 1e3, 4),
+                  "rounds": [round(x, 1) for x in rates[m]],
+                  "per_call": {"median": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)]},
+                  "n": calls * rounds}
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
 def describe_launch(info):
     """One line for the roofline's kernel field, from gemm_last_launch()."""
     if info.get("kind") == 2:
@@ -675,17 +705,16 @@ def extra_cells(g, stream, peaks):
         c = run(f"fp16_{n}", wl.fp16_alpha_beta(n), steps=reps, warmup=20)
         if n in (512, 1024):
             c.update(bimodality(SAMPLES[f"fp16_{n}"]))
-    # config 3: fused bias+GELU against the plain GEMM and against GEMM + the separate bias+GELU pass
+    # config 3: fused bias+GELU against the plain GEMM and against GEMM + the separate bias+GELU pass,
+    # the three timed in alternating rounds on the same inputs (a cost of a few percent is below the
+    # drift between two cells timed one after the other)
     gelu_cost, fusion_gain = {}, {}
-    for M in (512, 2048, 8192):
-        p = wl.bf16_bias_gelu(M)
-        fused = cell(g, p, 30, 5, stream, name=f"gelu_M{M}_fused", l2=l2)
-        plain = cell(g, wl.bf16_bias_gelu(M, epilogue=wl.EPI_NONE), 30, 5, stream, name=f"gelu_M{M}_none", l2=l2)
-        unfused = cell(g, p, 30, 5, stream, mode="decomposed", name=f"gelu_M{M}_decomposed", l2=l2)
-        cost = round(100 * (plain["tflops"] / fused["tflops"] - 1), 2)
-        gain = round(100 * (fused["tflops"] / unfused["tflops"] - 1), 2)
-        cells[f"gelu_M{M}"] = {"fused": fused, "none": plain, "decomposed": unfused, "fused_cost_pct": cost,
-                               "fusion_gain_pct": gain}
+    for M, calls in ((512, 200), (2048, 100), (8192, 30)):
+        c = interleaved_modes(g, wl.bf16_bias_gelu(M), ("fused", "none", "decomposed"), calls, 8, stream, l2,
+                              name=f"gelu_M{M}")
+        cost = round(100 * (c["none"]["tflops"] / c["fused"]["tflops"] - 1), 2)
+        gain = round(100 * (c["fused"]["tflops"] / c["decomposed"]["tflops"] - 1), 2)
+        cells[f"gelu_M{M}"] = dict(c, fused_cost_pct=cost, fusion_gain_pct=gain)
         gelu_cost[M], fusion_gain[M] = cost, gain
     # config 5: fp32 layouts (3xTF32) with ldc padding, and bf16 8192^3 NN
     for lay in ("NN", "NT", "TN", "TT"):

@@ -1171,15 +1171,16 @@ gemm_status_t gemm_mx(int64_t M, int64_t N, int64_t K, gemm_mx_elem_t elem, cons
     if (launch_mx_sf_pack(a_scale, M, blocks, sfa, (M + 127) / 128, kc, s) != cudaSuccess) return GEMM_ERR_CUDA;
     if (launch_mx_sf_pack(b_scale, N, blocks, sfb, (N + 127) / 128, kc, s) != cudaSuccess) return GEMM_ERR_CUDA;
 
-    // Operands as bytes: boxes of 128 bytes of K x 128 rows, 128-byte swizzle, zero fill.
+    // Operands as bytes: boxes of 128 bytes of K x 128 rows (A) or 256 rows (B), 128-byte
+    // swizzle, zero fill.
     CUtensorMap ta, tb;
     if ((st = encode_2d(&ta, GEMM_E4M3, A, k_bytes, M, a_pitch, 128, 128)) != GEMM_OK) return st;
-    if ((st = encode_2d(&tb, GEMM_E4M3, B, k_bytes, N, b_pitch, 128, 128)) != GEMM_OK) return st;
+    if ((st = encode_2d(&tb, GEMM_E4M3, B, k_bytes, N, b_pitch, 128, 256)) != GEMM_OK) return st;
     MxArgs a = {};
     a.e = e;
     a.K = static_cast<int>(K);
     a.tiles_m = static_cast<int>((M + 127) / 128);
-    a.tiles_n = static_cast<int>((N + 127) / 128);
+    a.tiles_n = static_cast<int>((N + 255) / 256);
     a.num_tiles = a.tiles_m * a.tiles_n;
     a.num_kb = static_cast<int>((k_bytes + 127) / 128);
     a.group_m = 8;
@@ -1190,7 +1191,7 @@ gemm_status_t gemm_mx(int64_t M, int64_t N, int64_t K, gemm_mx_elem_t elem, cons
     const int grid = a.num_tiles < dev->num_sms ? a.num_tiles : dev->num_sms;
     info.path = GEMM_PATH_TCGEN05;
     info.kind = 1;
-    info.bn = 128;
+    info.bn = 256;
     info.cluster_ctas = 1;
     info.grid_ctas = grid;
     info.tiles = a.num_tiles;

@@ -14,21 +14,33 @@
 // kind::mxf8f6f4 (one scale per 32 k, K = 32 a instruction) or kind::mxf4
 // (two scales, K = 64 of packed E2M1), each scale read from tensor memory.
 //
-// Roles (one SM per 128 x 128 output tile, persistent over tiles):
-//   warp 0 (one lane)  TMA loads of 128 bytes of K of A's and B's rows into a
-//                      STAGES-deep ring (128-byte swizzle, zero fill past M,
-//                      N and K), plus bulk copies of the stage's scale chunks;
+// Roles (one SM per 128 x 256 output tile, persistent over tiles):
+//   warp 0 (one lane)  TMA loads of 128 bytes of K of 128 rows of A and 256
+//                      rows of B into a STAGES-deep ring (128-byte swizzle,
+//                      zero fill past M, N and K), plus bulk copies of the
+//                      stage's scale chunks (A's row block, B's two);
 //   warp 1 (one lane)  tcgen05.cp of the chunks into the stage's tensor-memory
 //                      scale slot (32x128b, replicated to the four lane
-//                      groups), then the block-scaled MMAs into one of two fp32
-//                      accumulators (columns 0-255; the scale slots follow);
-//   warps 2-5          the shared epilogue (alpha, beta*C, bias, activation,
-//                      cast) from tensor memory, one row per thread.
+//                      groups: row r's scales in column r / 32 of the slot's
+//                      part, so B's 256 rows take eight columns), then the
+//                      block-scaled MMAs (N = 256) into the fp32 accumulator
+//                      (columns 0-255; the scale slots follow);
+//   warps 2-9          the shared epilogue (alpha, beta*C, bias, activation,
+//                      cast), one row and half the columns per thread.
 // The scales arrive row-major (M x K/32, N x K/32) and a pre-pass rewrites them
 // into 512-byte chunks of 128 rows x 4 blocks in the order the tensor-memory
-// copy expects (see MxArgs).  Only the tile width differs from the dense
-// one-SM kernel: two 128-column accumulators leave tensor memory room for the
-// scale slots of every stage in flight.
+// copy expects (see MxArgs).
+//
+// Why 256 columns: every byte of a stage crosses shared memory twice (TMA
+// write, MMA read), and a 128 x 128 tile moved 256 bytes a clock through it at
+// the full MMA rate, twice what it delivers, so that kernel ran at a third of
+// the tensor rate.  B 256 rows wide cuts that to 192.  A 256-column
+// accumulator leaves tensor memory room for one accumulator beside the scale
+// slots, so a tile's epilogue (eight warps) runs before the next tile's MMAs
+// start, while the producer keeps loading the next tile's stages.  (Moving
+// the accumulator into registers first, 128 values a thread, and releasing it
+// at once spilled more than a kilobyte a thread at the 168-register cap of a
+// 10-warp CTA.)
 #include "epilogue.cuh"
 #include "gemm_tcgen05.cuh"
 #include "kernel_args.h"
@@ -50,7 +62,7 @@ template <> struct MxTraits<kMxE2M1> {
 
 template <int ELEM, int STAGES_>
 struct MxConfig {
-    static constexpr int BM = 128, BN = 128;
+    static constexpr int BM = 128, BN = 256;
     static constexpr int STAGES = STAGES_;
     static constexpr int ROW_BYTES = 128;                         // bytes of K per stage
     static constexpr int MMAS = 4;                                // 32 bytes of K each
@@ -58,19 +70,18 @@ struct MxConfig {
     static constexpr int A_BYTES = BM * ROW_BYTES;
     static constexpr int B_BYTES = BN * ROW_BYTES;
     static constexpr int SFA_OFF = A_BYTES + B_BYTES;
-    static constexpr int SFB_OFF = SFA_OFF + CHUNKS * 512;
-    static constexpr int STAGE_BYTES = SFB_OFF + CHUNKS * 512;
-    static constexpr int STAGE_TX = STAGE_BYTES;                  // every byte of the stage arrives by copy
-    static constexpr int ACC_COLS = 2 * BN;                       // two accumulators
-    static constexpr int SF_SLOT_COLS = 8 * CHUNKS;               // A's then B's chunks, 4 columns each
+    static constexpr int SFB_OFF = SFA_OFF + CHUNKS * 512;         // B's row blocks 0 and 1, CHUNKS each
+    static constexpr int STAGE_TX = SFB_OFF + 2 * CHUNKS * 512;    // bytes a stage receives
+    static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
+    static constexpr int ACC_COLS = BN;                           // one accumulator
+    static constexpr int SF_SLOT_COLS = 12 * CHUNKS;              // A: 4 per chunk; B: 8 per chunk
     static constexpr int TMEM_COLS = 512;
-    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_WARPS = 8;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
-    static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned (128-byte swizzle atoms)");
-    static_assert(ACC_COLS + STAGES * SF_SLOT_COLS <= TMEM_COLS, "scale slots fit beside the accumulators");
-    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barriers fit their slot");
+    static_assert(ACC_COLS + STAGES * SF_SLOT_COLS <= TMEM_COLS, "scale slots fit beside the accumulator");
+    static_assert((2 * STAGES + 3) * 8 + 8 <= BAR_BYTES, "barriers fit their slot");
     static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
     static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: it allocates all 512 TMEM columns");
 };
@@ -88,8 +99,8 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
-    uint64_t *tempty = tfull + 2;
-    uint64_t *mma_done = tempty + 2;
+    uint64_t *tempty = tfull + 1;
+    uint64_t *mma_done = tempty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -101,10 +112,8 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], Cfg::EPI_WARPS);
-        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, Cfg::EPI_WARPS);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -128,11 +137,16 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
             uint32_t stage = 0, phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             bool ok = true;
+            const long long rb_b = (N + 127) / 128;  // B's row blocks in the scale pack
             for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
                 int tm, tn;
                 tile_coords(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
                 const unsigned char *sfa_row = args.sfa + static_cast<long long>(tm) * args.kc_count * 512;
-                const unsigned char *sfb_row = args.sfb + static_cast<long long>(tn) * args.kc_count * 512;
+                // B's second row block of the tile; past N it does not exist in the
+                // pack, and the first one stands in (those rows of B are zero-filled).
+                const long long rb0 = 2LL * tn, rb1 = rb0 + 1 < rb_b ? rb0 + 1 : rb0;
+                const unsigned char *sfb_row0 = args.sfb + rb0 * args.kc_count * 512;
+                const unsigned char *sfb_row1 = args.sfb + rb1 * args.kc_count * 512;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status)) {
                         ok = false;
@@ -146,7 +160,9 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
                     tma_load_2d(sA + Cfg::A_BYTES, &tmB, &full[stage], kb * Cfg::ROW_BYTES, tn * BN);
                     const long long chunk = static_cast<long long>(kb) * Cfg::CHUNKS * 512;
                     bulk_load_1d(sA + Cfg::SFA_OFF, sfa_row + chunk, Cfg::CHUNKS * 512, &full[stage]);
-                    bulk_load_1d(sA + Cfg::SFB_OFF, sfb_row + chunk, Cfg::CHUNKS * 512, &full[stage]);
+                    bulk_load_1d(sA + Cfg::SFB_OFF, sfb_row0 + chunk, Cfg::CHUNKS * 512, &full[stage]);
+                    bulk_load_1d(sA + Cfg::SFB_OFF + Cfg::CHUNKS * 512, sfb_row1 + chunk, Cfg::CHUNKS * 512,
+                                 &full[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -167,10 +183,8 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
             bool ok = true, issued = false;
             int local = 0;
             for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++local) {
-                const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
-                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, args.status)) break;
+                if (!mbar_wait_bounded(tempty, (local & 1) ^ 1u, abort_flag, args.status)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status)) {
                         ok = false;
@@ -179,13 +193,16 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + stage * Cfg::STAGE_BYTES);
                     const uint32_t b_addr = a_addr + Cfg::A_BYTES;
-                    // this stage's scale slot: A's chunks, then B's, 4 columns per chunk
+                    // this stage's scale slot: A's chunks (4 columns each), then B's
+                    // (8 columns each: rows 0-127, then rows 128-255)
                     const uint32_t sfa_t = tmem_base + Cfg::ACC_COLS + stage * Cfg::SF_SLOT_COLS;
                     const uint32_t sfb_t = sfa_t + 4 * Cfg::CHUNKS;
 #pragma unroll
                     for (int c = 0; c < Cfg::CHUNKS; ++c) {
                         tc_cp_32x128b_x4(sfa_t + 4 * c, plain16_desc(a_addr + Cfg::SFA_OFF + 512 * c));
-                        tc_cp_32x128b_x4(sfb_t + 4 * c, plain16_desc(a_addr + Cfg::SFB_OFF + 512 * c));
+                        tc_cp_32x128b_x4(sfb_t + 8 * c, plain16_desc(a_addr + Cfg::SFB_OFF + 512 * c));
+                        tc_cp_32x128b_x4(sfb_t + 8 * c + 4,
+                                         plain16_desc(a_addr + Cfg::SFB_OFF + Cfg::CHUNKS * 512 + 512 * c));
                     }
 #pragma unroll
                     for (int ks = 0; ks < Cfg::MMAS; ++ks) {
@@ -197,8 +214,8 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
                         const uint32_t idesc = mma_idesc_bs(MxTraits<ELEM>::kFmt, BM, BN, sf_id, sf_id);
                         const uint64_t ad = sw128_desc(a_addr + ks * 32, 16u, 1024u);
                         const uint64_t bd = sw128_desc(b_addr + ks * 32, 16u, 1024u);
-                        tc_mma_bs<MxTraits<ELEM>::kKind>(d_tmem, ad, bd, idesc, sfa_t + 4 * chunk, sfb_t + 4 * chunk,
-                                                         (kb | ks) != 0 ? 1u : 0u);
+                        tc_mma_bs<MxTraits<ELEM>::kKind>(tmem_base, ad, bd, idesc, sfa_t + 4 * chunk,
+                                                         sfb_t + 8 * chunk, (kb | ks) != 0 ? 1u : 0u);
                     }
                     issued = true;
                     tc_commit(&empty[stage]);
@@ -207,7 +224,7 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
                         phase ^= 1u;
                     }
                 }
-                if (ok) tc_commit(&tfull[acc]);
+                if (ok) tc_commit(tfull);
             }
             if (*abort_flag && issued) {
                 tc_commit(mma_done);
@@ -216,27 +233,26 @@ __global__ void __launch_bounds__(MxConfig<ELEM, STAGES>::THREADS, 1)
         }
     } else {
         // ------------------------------------------------------- epilogue --
-        const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+        const int quad = warp & 3;           // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+        const int half = (warp - 2) >> 2;    // which 128 of the tile's 256 columns
         const EpiParams &e = args.e;
         int local = 0;
         for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++local) {
-            const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
             int tm, tn;
             tile_coords(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
-            const int m0 = tm * BM, n0 = tn * BN;
-            const bool got = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, args.status);
+            const int m0 = tm * BM, col_base = tn * BN + half * 128;
+            const bool got = mbar_wait_bounded(tfull, local & 1, abort_flag, args.status);
             if (__any_sync(0xffffffffu, !got)) break;  // warp-uniform exit
             tc_fence_after();
             const int row = m0 + quad * 32 + lane;
             const bool row_ok = row < M;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-            int nvalid = BN / 32;
-            const int left = (N - n0 + 31) >> 5;  // chunks that start inside the matrix
-            if (left < nvalid) nvalid = left;
-            epilogue_row_chunks<OUT, BN / 32>(t_row, n0, nvalid, row, row_ok, e.bias + n0, e);
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
+            int nvalid = (N - col_base + 31) >> 5;  // chunks that start inside the matrix
+            nvalid = nvalid < 0 ? 0 : (nvalid > 4 ? 4 : nvalid);
+            epilogue_row_chunks<OUT, 4, false>(t_row, col_base, nvalid, row, row_ok, e.bias + col_base, e);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (lane == 0) mbar_arrive(tempty);
         }
     }
 
@@ -268,7 +284,7 @@ __global__ void mx_sf_pack_kernel(const unsigned char *__restrict__ src, long lo
 template <int ELEM, int OUT>
 cudaError_t launch_mx_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs &args, int grid,
                           cudaStream_t stream) {
-    constexpr int STAGES = 6;
+    constexpr int STAGES = 4;
     using Cfg = MxConfig<ELEM, STAGES>;
     auto kern = gemm_mx_kernel<ELEM, OUT, STAGES>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);

@@ -67,7 +67,7 @@ def test_integer_exact(cuda_lib, elem, shape):
     st, out = run_mx(g, p, code)
     assert st == 0
     info = g.gemm_last_launch()
-    assert info["path"] == g.PATH_TCGEN05 and info["kind"] == 1 and info["bn"] == 128
+    assert info["path"] == g.PATH_TCGEN05 and info["kind"] == 1 and info["bn"] == 256
     y, _ = omx.mx_reference(**p.oracle_args())
     got = oracle.output_values(out, p.M, p.N, p.ldc, p.c_dtype)
     bad = np.argwhere(got != y)
