@@ -215,7 +215,8 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
                    rows: Optional[Sequence[int]] = None,
                    alpha_scale: Optional[np.ndarray] = None, row_scale: Optional[np.ndarray] = None,
                    col_scale: Optional[np.ndarray] = None,
-                   residual: Optional[np.ndarray] = None, ldr: int = 0, r_dtype: Optional[int] = None):
+                   residual: Optional[np.ndarray] = None, ldr: int = 0, r_dtype: Optional[int] = None,
+                   k_ascending: bool = False):
     """Reference output y (float64, not rounded to the output type) and scale D.
 
     A, B, C are raw code arrays (flat) in the given element types; ``bias`` is
@@ -235,6 +236,11 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
     the output type when r_dtype is None): added after the activation,
     y_ij = act(z_ij) + r_ij, the post-activation residual of a transformer
     block; D takes |r_ij| too.
+
+    The sums over k come from a float64 matrix product (BLAS, its own order
+    of additions); with ``k_ascending`` they are accumulated one k at a time
+    in ascending order instead, the triple loop's order (slow: for small
+    cases and for checking that the order moves sums by rounding only).
     """
     if min(M, N, K) < 0:
         raise ValueError("negative size")
@@ -254,8 +260,15 @@ def gemm_reference(M: int, N: int, K: int, ab_dtype: int,
             fac *= np.asarray(row_scale, np.float32).astype(np.float64).reshape(-1)[row_sel][:, None]
         if col_scale is not None:
             fac *= np.asarray(col_scale, np.float32).astype(np.float64).reshape(-1)[None, :N]
-        z += fac * (a @ b)
-        D += np.abs(fac) * (np.abs(a) @ np.abs(b))
+        if k_ascending:
+            ab, aabs = np.zeros((R, N)), np.zeros((R, N))
+            for k in range(K):
+                ab += a[:, k, None] * b[None, k, :]
+                aabs += np.abs(a[:, k, None]) * np.abs(b[None, k, :])
+        else:
+            ab, aabs = a @ b, np.abs(a) @ np.abs(b)
+        z += fac * ab
+        D += np.abs(fac) * aabs
     if be != 0.0 and R > 0 and N > 0:
         c = decode(strided_codes(C, M, N, ldc, 1, row_sel), c_dtype)
         z += be * c

@@ -553,3 +553,31 @@ def test_residual_zero_and_absent_agree():
     ones = torch.ones(9 * 11, dtype=torch.float16).view(torch.int16).numpy()
     y1, _ = oracle.gemm_reference(**a, residual=ones, ldr=11)
     assert np.array_equal(y1, y0 + 1.0)
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.F16, wl.BF16, wl.E4M3])
+def test_k_ascending_order_matches_brute_force_exactly(dtype):
+    """The triple loop's order (one k at a time, ascending) gives the exact rational result on
+    small-integer data, like the matrix-product path, at ragged sizes with padded strides."""
+    for seed, (M, N, K) in enumerate([(3, 5, 7), (4, 1, 9), (1, 6, 2)]):
+        p = wl.random_problem(300 + seed, M, N, K, dtype, wl.F32, layout="TN", alpha=1.5, beta=-0.5,
+                              epilogue=wl.EPI_BIAS, integer=True, lda_pad=1, ldb_pad=2, ldc_pad=3)
+        y, _ = oracle.gemm_reference(k_ascending=True, **p.oracle_args())
+        exact = _frac_ref(p)
+        assert all(Fraction(float(y[i, j])) == exact[i][j] for i in range(M) for j in range(N))
+
+
+@pytest.mark.parametrize("dtype,out", [(wl.F16, wl.F16), (wl.BF16, wl.BF16), (wl.E4M3, wl.F32), (wl.F32, wl.F32)])
+def test_summation_order_moves_sums_by_rounding_only(dtype, out):
+    """On real-valued data the matrix product (its own order of additions) and the k-ascending
+    loop differ by at most the float64 rounding of K additions: |diff| <= K * 2^-52 * D, and D
+    is the same sum of absolute values either way up to that rounding."""
+    for M, N, K in [(37, 29, 513), (8, 64, 2048)]:
+        p = wl.random_problem(400 + K, M, N, K, dtype, out, layout="NT", alpha=0.75, beta=0.25,
+                              epilogue=wl.EPI_BIAS_GELU)
+        y1, D1 = oracle.gemm_reference(**p.oracle_args())
+        y2, D2 = oracle.gemm_reference(k_ascending=True, **p.oracle_args())
+        bound = K * 2.0 ** -52 * D1 * oracle.lipschitz(wl.EPI_BIAS_GELU) + 1e-300
+        assert np.all(np.abs(y1 - y2) <= bound)
+        assert np.all(np.abs(D1 - D2) <= K * 2.0 ** -52 * D1)
+        assert not np.array_equal(y1, np.zeros_like(y1))
