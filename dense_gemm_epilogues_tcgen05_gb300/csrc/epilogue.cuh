@@ -1014,17 +1014,23 @@ __device__ __forceinline__ bool epilogue_rows_tma_burst(uint32_t t_base, int col
     return true;
 }
 
-// Transposed counterpart of epilogue_prefetch: the warp's block of C is rows
-// col_base .. col_base + 32*nchunk - 1 (within M) by columns row0 .. row0+31
-// (within N); each of those rows' 64 bytes is prefetched into L2 when beta
-// != 0.  Returns this lane's column bias.  Warp-collective.
+// Transposed counterpart of epilogue_prefetch: the warp's block of the
+// output is rows col_base .. col_base + 32*nchunk - 1 (within M) by columns
+// row0 .. row0+31 (within N); each of those rows' 64 bytes of a residual,
+// and of C when `with_c` and beta != 0, is prefetched into L2.  Returns this
+// lane's column bias.  Warp-collective.
+// Callers ask for C only on a CTA's last tile, whose epilogue nothing
+// overlaps: for every other tile the TMA-staged C boxes arrive while the next
+// tile's main loop runs anyway, and prefetching their C a main loop ahead
+// pushed operand panels out of L2 (8 MB more HBM reads at 4096^3).
 template <int OUT>
-__device__ __forceinline__ float epilogue_prefetch_t(int col_base, int nchunk, int row0, const EpiParams &e) {
+__device__ __forceinline__ float epilogue_prefetch_t(int col_base, int nchunk, int row0, const EpiParams &e,
+                                                     bool with_c) {
     using OutT = typename Elem<OUT>::T;
     const int lane = threadIdx.x & 31;
     const int n = row0 + lane;
     const float b = (e.epilogue != kEpiNone && n < e.N) ? e.bias[n] : 0.0f;
-    if (e.beta != 0.0f && row0 < e.N) {
+    if (with_c && e.beta != 0.0f && row0 < e.N) {
         const int m_end = min(col_base + nchunk * 32, e.M);
         for (int m = col_base + lane; m < m_end; m += 32) {
             const OutT *p = reinterpret_cast<const OutT *>(e.C) + (long long)m * e.ldc + row0;
@@ -1042,11 +1048,12 @@ __device__ __forceinline__ float epilogue_prefetch_t(int col_base, int nchunk, i
 
 // Epilogue inputs of one warp's columns, fetched before the accumulator is
 // ready so their latency overlaps the main loop: the 32*nchunk bias values
-// go to shared memory (bias_s, 16-byte aligned), and this thread's row of C
-// (when beta != 0) is prefetched into L2.  Warp-collective.
+// go to shared memory (bias_s, 16-byte aligned), and this thread's row of a
+// residual, and of C when `with_c` and beta != 0 (see epilogue_prefetch_t),
+// is prefetched into L2.  Warp-collective.
 template <int OUT>
 __device__ __forceinline__ void epilogue_prefetch(float *bias_s, int col_base, int nchunk, int row, bool row_ok,
-                                                  const EpiParams &e) {
+                                                  const EpiParams &e, bool with_c) {
     using OutT = typename Elem<OUT>::T;
     const int lane = threadIdx.x & 31;
     if (e.epilogue != kEpiNone) {
@@ -1056,7 +1063,7 @@ __device__ __forceinline__ void epilogue_prefetch(float *bias_s, int col_base, i
         }
     }
     const int ncols = min(nchunk * 32, e.N - col_base);  // only columns inside the matrix
-    if (e.beta != 0.0f && row_ok && ncols > 0) {
+    if (with_c && e.beta != 0.0f && row_ok && ncols > 0) {
         const OutT *crow = reinterpret_cast<const OutT *>(e.C) + (long long)row * e.ldc + col_base;
         const int bytes = ncols * static_cast<int>(sizeof(OutT));
         const char *p = reinterpret_cast<const char *>(crow);

@@ -522,9 +522,9 @@ __global__ void __launch_bounds__(PairConfig<AB, STAGES, BNH>::THREADS, 1)
             float bias_lane = 0.0f;
             if (seg.kind != kSegPart) {
                 if (e.swap)
-                    bias_lane = epilogue_prefetch_t<OUT>(n_tile + c_begin * 32, c_end - c_begin, row0, e);
+                    bias_lane = epilogue_prefetch_t<OUT>(n_tile + c_begin * 32, c_end - c_begin, row0, e, last);
                 else
-                    epilogue_prefetch<OUT>(bias_s, n_tile + c_begin * 32, c_end - c_begin, row, row < M, e);
+                    epilogue_prefetch<OUT>(bias_s, n_tile + c_begin * 32, c_end - c_begin, row, row < M, e, last);
             }
             const bool got = pair_wait<CL>(&tfull[acc], acc_phase, abort_flag, args.status, abort_local, rank);
             if (__any_sync(0xffffffffu, !got)) break;
