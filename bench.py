@@ -806,8 +806,10 @@ def mx_cell(g, stream, elem, n, steps=30, warmup=3, name=None):
 
 def q4_prefill_cell(g, stream, M, N=4096, K=4096, steps=20):
     """Prefill with 4-bit weights: gemm_q4 with M rows of x (the tensor-core kernel, W
-    dequantised into tensor memory) against the unfused path, gemm_q4_dequantize then
-    gemm() in each call, and against gemm() on a W dequantised once (the dense rate).
+    dequantised into tensor memory), gemm_q4_ws (the same below Q4_DEQUANT_ROWS rows, W
+    expanded once into its workspace and the dense kernel above), the unfused path
+    (gemm_q4_dequantize then gemm() in each call) and gemm() on a W dequantised once (the
+    dense rate).
     Seeded random codes / scales (as the decode cells), x ~ N(0,1) fp16, fp16 output;
     TFLOP/s back to back."""
     import torch
@@ -823,9 +825,14 @@ def q4_prefill_cell(g, stream, M, N=4096, K=4096, steps=20):
     w_once = torch.empty(N * K, dtype=torch.float16, device=dev)
     g.gemm_q4_dequantize(N, K, wq, sb, w_once, g.F16, stream=stream)
     ws = _workspace(g, dev)
+    q4ws_need = g.gemm_q4_workspace_size(M, N, K, g.F16)
+    q4ws = torch.empty(max(q4ws_need, 256), dtype=torch.uint8, device=dev)
     runs = {
         "fused": lambda: g.gemm_q4(M, N, K, g.F16, x, K, wq, sb, y, N, g.F16, 1.0, 0.0, None, g.EPI_NONE,
                                    stream=stream),
+        # the public call for long prompts: fused below Q4_DEQUANT_ROWS rows, W expanded once above
+        "gemm_q4_ws": lambda: g.gemm_q4_ws(M, N, K, g.F16, x, K, wq, sb, y, N, g.F16, 1.0, 0.0, None, g.EPI_NONE,
+                                           workspace=q4ws, workspace_bytes=q4ws_need, stream=stream),
         "dequantize_then_gemm": lambda: (g.gemm_q4_dequantize(N, K, wq, sb, w_call, g.F16, stream=stream),
                                          g.gemm(M, N, K, g.F16, x, K, 1, w_call, 1, K, y, N, g.F16, 1.0, 0.0, None,
                                                 g.EPI_NONE, workspace=ws, workspace_bytes=ws.numel(), stream=stream)),
@@ -846,7 +853,7 @@ def q4_prefill_cell(g, stream, M, N=4096, K=4096, steps=20):
         ms = e0.elapsed_time(e1) / steps
         out[name] = {"tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1), "us": round(ms * 1e3, 2)}
     out["status"] = g.gemm_device_status()
-    del wq, sb, x, y, w_call, w_once
+    del wq, sb, x, y, w_call, w_once, q4ws
     torch.cuda.empty_cache()
     return out
 

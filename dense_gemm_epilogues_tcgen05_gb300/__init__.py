@@ -25,6 +25,7 @@ __all__ = [
     "SCHED_AUTO", "SCHED_TILES", "SCHED_STREAM_K", "ORDER_AUTO", "ORDER_AS_GIVEN", "ORDER_TRANSPOSED",
     "gemm_set_operand_order", "MCAST_AUTO", "MCAST_OFF", "MCAST_ON", "gemm_set_multicast", "gemm_last_launch",
     "BASELINE_SIMT", "BASELINE_MMA_SYNC", "gemm_baseline", "gemm_q4", "gemm_q4_dequantize", "Q4_MAX_ROWS",
+    "gemm_q4_ws", "gemm_q4_workspace_size", "Q4_DEQUANT_ROWS",
     "Q4_AUTO", "Q4_FFMA", "Q4_MMA", "gemm_set_q4_kernel",
     "gemm_ex", "gemm_get_tuning", "MX_E4M3", "MX_E2M1", "gemm_mx", "gemm_mx_workspace_size",
     "gemm_set_tile_policy", "gemm_query_tile", "gemm_set_schedule", "gemm_builtin_scratch", "gemm_wait_selftest",
@@ -47,8 +48,9 @@ ORDER_AUTO, ORDER_AS_GIVEN, ORDER_TRANSPOSED = 0, 1, 2
 MCAST_AUTO, MCAST_OFF, MCAST_ON = 0, 1, 2
 # gemm_baseline_t
 BASELINE_SIMT, BASELINE_MMA_SYNC = 0, 1
-# gemm_q4 takes at most this many rows of x (decode)
+# rows of x the decode kernels take; gemm_q4 runs the fused prefill beyond
 Q4_MAX_ROWS = 8
+Q4_DEQUANT_ROWS = 384  # GEMM_Q4_DEQUANT_ROWS: from this many rows of x gemm_q4_ws expands W once
 # gemm_q4_kernel_t
 Q4_AUTO, Q4_FFMA, Q4_MMA = 0, 1, 2
 # gemm_mx_elem_t
@@ -128,6 +130,12 @@ lib.gemm_q4.restype = _int
 lib.gemm_q4.argtypes = [_i64, _i64, _i64, _int, ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p,
                         ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
                         ctypes.c_void_p]
+lib.gemm_q4_ws.restype = _int
+lib.gemm_q4_ws.argtypes = [_i64, _i64, _i64, _int, ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p,
+                           ctypes.c_void_p, _i64, _int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p, _int,
+                           ctypes.c_void_p, _sz, ctypes.c_void_p]
+lib.gemm_q4_workspace_size.restype = _sz
+lib.gemm_q4_workspace_size.argtypes = [_i64, _i64, _i64, _int]
 lib.gemm_q4_dequantize.restype = _int
 lib.gemm_q4_dequantize.argtypes = [_i64, _i64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, _int,
                                    ctypes.c_void_p]
@@ -280,6 +288,20 @@ def gemm_q4(M, N, K, x_dtype, X, ldx, Wq, scale_bias, C, ldc, c_dtype, alpha, be
     st = lib.gemm_q4(M, N, K, x_dtype, _ptr(X), ldx, _ptr(Wq), _ptr(scale_bias), _ptr(C), ldc, c_dtype, alpha,
                      beta, _ptr(bias), epilogue, _stream(stream))
     return _check(st, "gemm_q4")
+
+
+def gemm_q4_ws(M, N, K, x_dtype, X, ldx, Wq, scale_bias, C, ldc, c_dtype, alpha, beta, bias, epilogue,
+               workspace=None, workspace_bytes=0, stream=None) -> int:
+    """gemm_q4 with a workspace: from Q4_DEQUANT_ROWS rows of x, W is expanded once into the workspace and
+    multiplied by the dense kernel (faster for long prompts); otherwise gemm_q4."""
+    st = lib.gemm_q4_ws(M, N, K, x_dtype, _ptr(X), ldx, _ptr(Wq), _ptr(scale_bias), _ptr(C), ldc, c_dtype, alpha,
+                        beta, _ptr(bias), epilogue, _ptr(workspace), workspace_bytes, _stream(stream))
+    return _check(st, "gemm_q4_ws")
+
+
+def gemm_q4_workspace_size(M, N, K, x_dtype) -> int:
+    """Bytes of workspace gemm_q4_ws uses for this shape (0: it runs the fused kernels)."""
+    return int(lib.gemm_q4_workspace_size(M, N, K, x_dtype))
 
 
 def gemm_q4_dequantize(N, K, Wq, scale_bias, W, w_dtype, stream=None) -> int:

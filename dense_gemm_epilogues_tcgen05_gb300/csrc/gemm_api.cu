@@ -1072,6 +1072,43 @@ gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, con
     return launch_q4_gemv(x_dtype, c_dtype, &tmW, a, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+size_t gemm_q4_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype) {
+    if (M < GEMM_Q4_DEQUANT_ROWS || N <= 0 || K <= 0 || K % 64 != 0) return 0;
+    if (x_dtype != GEMM_F16 && x_dtype != GEMM_BF16) return 0;
+    return round256(static_cast<size_t>(N) * static_cast<size_t>(K) * 2) + gemm_workspace_size(M, N, K, x_dtype);
+}
+
+gemm_status_t gemm_q4_ws(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype, const void *X, int64_t ldx,
+                         const uint32_t *Wq, const void *scale_bias, void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                         float alpha, float beta, const float *bias, gemm_epilogue_t epilogue, void *workspace,
+                         size_t workspace_bytes, gemm_stream_t stream) {
+    const size_t need = gemm_q4_workspace_size(M, N, K, x_dtype);
+    const bool use = need > 0 && workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 &&
+                     workspace_bytes >= need && alpha != 0.0f;
+    if (!use)
+        return gemm_q4(M, N, K, x_dtype, X, ldx, Wq, scale_bias, C, ldc, c_dtype, alpha, beta, bias, epilogue,
+                       stream);
+    // gemm_q4's argument rules first (the dense path accepts more), then the two calls.
+    if (N > INT32_MAX || K > INT32_MAX || M > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    if (!valid_dtype(c_dtype)) return GEMM_ERR_INVALID_ARG;
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
+    if (c_dtype == GEMM_E4M3) return GEMM_ERR_UNSUPPORTED;
+    if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (epilogue != GEMM_EPI_NONE && bias == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (X == nullptr || Wq == nullptr || scale_bias == nullptr || ldx < K) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(X) & 15u) != 0 || (ldx * 2) % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(Wq) & 15u) != 0 || (reinterpret_cast<uintptr_t>(scale_bias) & 3u) != 0)
+        return GEMM_ERR_MISALIGNED;
+    gemm_status_t st;
+    if ((st = check_range(workspace, need)) != GEMM_OK) return st;
+    unsigned char *W = static_cast<unsigned char *>(workspace);
+    const size_t w_bytes = round256(static_cast<size_t>(N) * static_cast<size_t>(K) * 2);
+    if ((st = gemm_q4_dequantize(N, K, Wq, scale_bias, W, x_dtype, stream)) != GEMM_OK) return st;
+    // W is N x K row-major: as B (K x N) it is K-contiguous, b_stride_k = 1, b_stride_n = K.
+    return gemm(M, N, K, x_dtype, X, ldx, 1, W, 1, K, C, ldc, c_dtype, alpha, beta, bias, epilogue, W + w_bytes,
+                workspace_bytes - w_bytes, stream);
+}
+
 gemm_status_t gemm_q4_dequantize(int64_t N, int64_t K, const uint32_t *Wq, const void *scale_bias, void *W,
                                  gemm_dtype_t w_dtype, gemm_stream_t stream) {
     if (N < 0 || K < 0 || K % 64 != 0) return GEMM_ERR_INVALID_ARG;

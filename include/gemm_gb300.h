@@ -438,6 +438,39 @@ gemm_status_t gemm_q4(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype,
                       gemm_stream_t stream);
 
 /*
+ * gemm_q4_ws -- gemm_q4 with a caller-owned workspace, for long prompts.  The
+ * fused prefill converts each 64-k group of W once per 128 rows of x, so from
+ * a few hundred rows of x up it is faster to expand W once into 16 bits and
+ * run the dense tensor-core kernel (GB300, N = K = 4096: fused 31 / 33 / 60 /
+ * 187 us at M = 64 / 256 / 1024 / 4096 against 35 / 35 / 37 / 93 us for
+ * gemm_q4_dequantize + gemm()).  When gemm_q4_workspace_size(M, N, K,
+ * x_dtype) is non-zero and the workspace (256-byte aligned device memory, not
+ * overlapping any operand) holds that many bytes, the call does exactly
+ * that: W into the workspace as x_dtype (the same rounding of W as the fused
+ * kernel), then gemm() with the rest of the workspace for its partial sums.
+ * Otherwise it runs gemm_q4.  Same arguments, results within the same
+ * tolerances, and errors as gemm_q4; asynchronous on `stream`.
+ */
+gemm_status_t gemm_q4_ws(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype,
+                         const void *X, int64_t ldx,
+                         const uint32_t *Wq, const void *scale_bias,
+                         void *C, int64_t ldc, gemm_dtype_t c_dtype,
+                         float alpha, float beta,
+                         const float *bias, gemm_epilogue_t epilogue,
+                         void *workspace, size_t workspace_bytes,
+                         gemm_stream_t stream);
+
+/*
+ * gemm_q4_workspace_size -- bytes of workspace gemm_q4_ws uses for this shape:
+ * 0 below GEMM_Q4_DEQUANT_ROWS rows of x (the fused kernel is faster there) or
+ * for an x_dtype other than F16 / BF16, else the 16-bit W (256-byte rounded)
+ * plus gemm_workspace_size(M, N, K, x_dtype).  Pure function of its
+ * arguments; touches no device.
+ */
+#define GEMM_Q4_DEQUANT_ROWS 384
+size_t gemm_q4_workspace_size(int64_t M, int64_t N, int64_t K, gemm_dtype_t x_dtype);
+
+/*
  * The kernel behind gemm_q4.  Both compute the same sums (per 64-k group,
  * s * sum_k x q + b * sum_k x, in fp32) and meet the same tolerances; they
  * differ in how the weights move and where the products are formed.

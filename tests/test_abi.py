@@ -286,3 +286,27 @@ def test_mx_workspace_size_and_validation_without_gpu(g):
             g.gemm_mx(128, 128, K, elem, *args, cd, 1.0, 0.0, None, g.EPI_NONE, stream=0)
         assert ei.value.status == status
     assert g.gemm_mx(0, 128, 128, g.MX_E4M3, *args, g.F32, 1.0, 0.0, None, g.EPI_NONE, stream=0) == 0   # no-op
+
+
+def test_q4_ws_workspace_size_and_fallback_without_gpu(g):
+    """gemm_q4_workspace_size: 0 below Q4_DEQUANT_ROWS rows of x (the fused kernels run there) or for a
+    non-16-bit x, else the 16-bit W rounded to 256 bytes plus gemm()'s own workspace.  gemm_q4_ws without
+    a usable workspace is gemm_q4: the same argument errors before any CUDA call."""
+    assert g.Q4_DEQUANT_ROWS == 384
+    assert g.gemm_q4_workspace_size(383, 4096, 4096, g.F16) == 0
+    w = 4096 * 4096 * 2
+    assert g.gemm_q4_workspace_size(384, 4096, 4096, g.F16) == w + g.gemm_workspace_size(384, 4096, 4096, g.F16)
+    assert g.gemm_q4_workspace_size(4096, 4096, 4096, g.BF16) == w + g.gemm_workspace_size(4096, 4096, 4096, g.BF16)
+    assert g.gemm_q4_workspace_size(1000, 100, 192, g.F16) == (100 * 192 * 2 + 255) // 256 * 256 + \
+        g.gemm_workspace_size(1000, 100, 192, g.F16)
+    assert g.gemm_q4_workspace_size(4096, 4096, 4096, g.F32) == 0
+    assert g.gemm_q4_workspace_size(4096, 4096, 100, g.F16) == 0      # K not a multiple of 64
+    assert g.gemm_q4_workspace_size(4096, 0, 4096, g.F16) == 0
+    X, W, SB, C = 0x100000, 0x200000, 0x300000, 0x400000
+    for kw, status in [(dict(K=100), g.ERR_INVALID_ARG), (dict(xd=g.F32), g.ERR_UNSUPPORTED),
+                       (dict(ldx=132), g.ERR_MISALIGNED)]:
+        K = kw.get("K", 128)
+        with pytest.raises(g.GemmError) as e:
+            g.gemm_q4_ws(16, 64, K, kw.get("xd", g.F16), X, kw.get("ldx", 128), W, SB, C, 64, g.F16, 1.0, 0.0,
+                         None, g.EPI_NONE, workspace=None, workspace_bytes=0, stream=0)
+        assert e.value.status == status, kw

@@ -36,8 +36,9 @@ def q4k(request, cuda_lib):
     g.gemm_set_q4_kernel(g.Q4_AUTO)
 
 
-def run_q4(g, p):
-    """Run a Q4Problem on the GPU with guarded C; returns the output codes (M x ldc flat)."""
+def run_q4(g, p, workspace=False):
+    """Run a Q4Problem on the GPU with guarded C; returns the output codes (M x ldc flat).  With
+    `workspace`, through gemm_q4_ws with the workspace it asks for (guarded too)."""
     view = wl.CODE_VIEW[p.c_dtype]
     n = p.C.numel()
     host = torch.full((2 * GUARD + n,), CANARY[p.c_dtype], dtype=view)
@@ -48,9 +49,19 @@ def run_q4(g, p):
     c_ptr = cbuf.data_ptr() + GUARD * cbuf.element_size()
     X, Wq, SB = p.X.cuda(), p.Wq.cuda(), p.SB.cuda()
     bias = None if p.bias is None else p.bias.cuda()
-    g.gemm_q4(p.M, p.N, p.K, p.x_dtype, X, p.ldx, Wq, SB, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias,
-              p.epilogue)
-    assert g.gemm_device_status() == 0
+    if workspace:
+        need = g.gemm_q4_workspace_size(p.M, p.N, p.K, p.x_dtype)
+        wsb = torch.full((need + 2 * 256,), 0x5A, dtype=torch.uint8, device="cuda")
+        g.gemm_q4_ws(p.M, p.N, p.K, p.x_dtype, X, p.ldx, Wq, SB, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias,
+                     p.epilogue, workspace=wsb.data_ptr() + 256, workspace_bytes=need)
+        assert g.gemm_device_status() == 0
+        back_ws = wsb.cpu()
+        assert bool((back_ws[:256] == 0x5A).all()) and bool((back_ws[256 + need:] == 0x5A).all()), "workspace guard"
+        run_q4.last_workspace = back_ws[256:256 + need]
+    else:
+        g.gemm_q4(p.M, p.N, p.K, p.x_dtype, X, p.ldx, Wq, SB, c_ptr, p.ldc, p.c_dtype, p.alpha, p.beta, bias,
+                  p.epilogue)
+        assert g.gemm_device_status() == 0
     back = cbuf.cpu()
     assert bool((back[:GUARD] == CANARY[p.c_dtype]).all()) and bool((back[GUARD + n:] == CANARY[p.c_dtype]).all())
     out = back[GUARD:GUARD + n]
@@ -203,3 +214,43 @@ def test_prefill_large_sampled_rows(cuda_lib):
     out = run_q4(g, p)
     res = q4.check(p.oracle_args(), out, rows=sample_rows(4096, n_random=96))
     assert res["pass"], res
+
+
+# ------------------------------------------------ long prompts (gemm_q4_ws) --
+
+
+def _dequantized_w(g, p):
+    W = torch.empty(p.N * p.K, dtype=wl.TORCH_DTYPE[p.x_dtype], device="cuda")
+    g.gemm_q4_dequantize(p.N, p.K, p.Wq.cuda(), p.SB.cuda(), W, p.x_dtype)
+    return W.cpu().view(torch.uint8)
+
+
+@pytest.mark.parametrize("M,N,K,xd", [(384, 200, 1088, wl.F16), (1000, 520, 2048, wl.BF16)], ids=lambda v: str(v))
+def test_q4_ws_integer_exact(cuda_lib, M, N, K, xd):
+    """From Q4_DEQUANT_ROWS rows of x with its workspace, gemm_q4_ws expands W once into the workspace
+    (its first N*K*2 bytes are then gemm_q4_dequantize's W, byte for byte) and runs the dense kernel:
+    bit-exact on integer problems at ragged N, the workspace's guard bytes intact."""
+    g = cuda_lib
+    p = wl.q4_problem(500 + M + N, M, N, K, xd, wl.F32, integer=True, ldc_pad=3)
+    out = run_q4(g, p, workspace=True)
+    assert torch.equal(run_q4.last_workspace[:N * K * 2], _dequantized_w(g, p))
+    y, _ = q4.q4_reference(**p.oracle_args())
+    got = oracle.output_values(out, p.M, p.N, p.ldc, p.c_dtype)
+    assert np.array_equal(got, y)
+
+
+@pytest.mark.parametrize("epi", [wl.EPI_NONE, wl.EPI_BIAS_GELU], ids=["none", "gelu"])
+def test_q4_ws_realistic_tolerance_and_fallback(cuda_lib, epi):
+    """Realistic layers through gemm_q4_ws meet the 16-bit tolerance at M = 512 (W expanded into the
+    workspace, dense kernel) and at M = 64 (below Q4_DEQUANT_ROWS it asks for no workspace and runs the
+    fused prefill)."""
+    g = cuda_lib
+    for M in (512, 64):
+        p = wl.q4_problem(520 + M, M, 768, 1024, wl.BF16, wl.BF16, epilogue=epi)
+        out = run_q4(g, p, workspace=True)
+        if M >= g.Q4_DEQUANT_ROWS:
+            assert torch.equal(run_q4.last_workspace[:768 * 1024 * 2], _dequantized_w(g, p))
+        else:
+            assert run_q4.last_workspace.numel() == 0
+        res = q4.check(p.oracle_args(), out)
+        assert res["pass"], res
