@@ -1208,6 +1208,53 @@ gemm_status_t gemm_mx(int64_t M, int64_t N, int64_t K, gemm_mx_elem_t elem, cons
     if (launch_mx_sf_pack(a_scale, M, blocks, sfa, (M + 127) / 128, kc, s) != cudaSuccess) return GEMM_ERR_CUDA;
     if (launch_mx_sf_pack(b_scale, N, blocks, sfb, (N + 127) / 128, kc, s) != cudaSuccess) return GEMM_ERR_CUDA;
 
+    if (M > 128) {
+        // SM pairs, 256 x 256 tiles (gemm_mx_pair.cu): operands as bytes in boxes of
+        // 128 bytes of K x 128 rows (each CTA's half), 128-byte swizzle, zero fill; the
+        // chunked scales as rows of 256 bytes, one box = one stage's chunks of a
+        // 128-row block.  Up to 128 rows of A the one-SM kernel's 128 x 256 tiles
+        // waste no half-empty pair tile.
+        CUtensorMap ta, tb, tsa, tsb;
+        if ((st = encode_2d(&ta, GEMM_E4M3, A, k_bytes, M, a_pitch, 128, 128)) != GEMM_OK) return st;
+        if ((st = encode_2d(&tb, GEMM_E4M3, B, k_bytes, N, b_pitch, 128, 128)) != GEMM_OK) return st;
+        const cuuint32_t sf_rows = static_cast<cuuint32_t>(elem == GEMM_MX_E2M1 ? 4 : 2);
+        for (int o = 0; o < 2; ++o) {
+            const int64_t rows = o == 0 ? M : N;
+            cuuint64_t dims[2] = {256u, static_cast<cuuint64_t>(2 * ((rows + 127) / 128) * kc)};
+            cuuint64_t strides[1] = {256u};
+            cuuint32_t box[2] = {256u, sf_rows};
+            cuuint32_t estr[2] = {1, 1};
+            if (driver_fns().encode(o == 0 ? &tsa : &tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, o == 0 ? sfa : sfb, dims,
+                                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return GEMM_ERR_CUDA;
+        }
+        MxArgs a = {};
+        a.e = e;
+        a.K = static_cast<int>(K);
+        a.tiles_m = static_cast<int>((M + 255) / 256);
+        a.tiles_n = static_cast<int>((N + 255) / 256);
+        a.num_tiles = a.tiles_m * a.tiles_n;
+        a.num_kb = static_cast<int>((k_bytes + 127) / 128);
+        a.group_m = 8;
+        a.sfa = sfa;
+        a.sfb = sfb;
+        a.kc_count = static_cast<int>(kc);
+        a.status = dev->status;
+        const int max_clusters = dev->num_sms / 2;
+        const int clusters = a.num_tiles < max_clusters ? a.num_tiles : max_clusters;
+        info.path = GEMM_PATH_TCGEN05;
+        info.kind = 2;
+        info.bn = 256;
+        info.cluster_ctas = 2;
+        info.grid_ctas = 2 * clusters;
+        info.tiles = a.num_tiles;
+        return record(launch_mx_pair(elem, c_dtype, ta, tb, tsa, tsb, a, clusters, s) == cudaSuccess ? GEMM_OK
+                                                                                                      : GEMM_ERR_CUDA,
+                      info);
+    }
+
     // Operands as bytes: boxes of 128 bytes of K x 128 rows (A) or 256 rows (B), 128-byte
     // swizzle, zero fill.
     CUtensorMap ta, tb;

@@ -162,6 +162,11 @@ cudaError_t launch_q4_prefill(int x_dtype, int out, const CUtensorMap &tmX, cons
 //   block-scaled product (one SM per 128 x 128 tile) and its scale-factor pack pre-pass:
 cudaError_t launch_mx(int elem, int out, const CUtensorMap &ta, const CUtensorMap &tb, const MxArgs &args, int grid,
                       cudaStream_t stream);
+// The same product on SM pairs, 256 x 256 tiles: tsa / tsb map the chunked
+// scales as rows of 256 bytes (two per chunk), boxes of 2 x chunks-per-stage
+// rows; `clusters` CTA pairs.
+cudaError_t launch_mx_pair(int elem, int out, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tsa,
+                           const CUtensorMap &tsb, const MxArgs &args, int clusters, cudaStream_t stream);
 cudaError_t launch_mx_sf_pack(const unsigned char *src, long long rows, long long blocks, unsigned char *dst,
                               long long row_blocks, long long kc_count, cudaStream_t stream);
 cudaError_t launch_wait_selftest(const unsigned int *never_set, unsigned long long limit_ns, unsigned int *status,

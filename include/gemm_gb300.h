@@ -542,7 +542,9 @@ typedef enum {
 
 /*
  * gemm_mx -- the block-scaled product above on the tensor cores
- * (tcgen05.mma kind::mxf8f6f4 / kind::mxf4, scales applied by the MMA).
+ * (tcgen05.mma kind::mxf8f6f4 / kind::mxf4, scales applied by the MMA): up
+ * to 128 rows of A one SM per 128 x 256 output tile, beyond that SM pairs
+ * (cta_group::2) per 256 x 256 tile.
  *   K              a multiple of 32 (whole scale blocks); M, N, K >= 0.
  *   A, lda         M x K elements, row-major (K-contiguous), row pitch lda
  *                  ELEMENTS (lda >= K; even for E2M1).  16-byte aligned base,

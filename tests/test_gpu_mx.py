@@ -5,7 +5,8 @@ Integer-valued elements with scales 2^-1 .. 2^1 keep every product and sum
 exact in fp32, so MXFP8 and MXFP4 must match the oracle bit for bit (fp32
 outputs; 16-bit outputs as the round-to-nearest-even cast of the exact value)
 -- at ragged M, N, K, with a scale drawn per row and block, which pins the
-scale layout in tensor memory.  Quantised normal inputs meet the normalised
+scale layout in tensor memory of both kernels (one SM up to 128 rows of A,
+SM pairs beyond).  Quantised normal inputs meet the normalised
 tolerance, including the 4096^3 MXFP8 workload on sampled rows.  Guard
 canaries around C and its ldc padding must stay intact.
 """
@@ -49,11 +50,13 @@ def run_mx(g, p, elem_code, *, workspace_bytes=None):
 
 
 SHAPES = [
-    (128, 128, 128),     # one tile, one stage of MXFP8
+    (128, 128, 128),     # one tile, one stage of MXFP8 (one-SM kernel: at most 128 rows)
+    (130, 300, 64),      # SM pairs from 129 rows: the peer CTA holds 2 rows, N ends inside B's second block
     (200, 136, 96),      # ragged M and N, K ending inside a stage
     (256, 384, 512),     # several tiles
+    (300, 136, 96),      # a second row of pair tiles whose peer half is empty
     (384, 640, 1056),    # K = 33 blocks: a stage with one block
-    (1000, 520, 2048),   # many tiles per CTA, long K
+    (1000, 520, 2048),   # many tiles per CTA pair, long K
 ]
 
 
@@ -67,7 +70,9 @@ def test_integer_exact(cuda_lib, elem, shape):
     st, out = run_mx(g, p, code)
     assert st == 0
     info = g.gemm_last_launch()
-    assert info["path"] == g.PATH_TCGEN05 and info["kind"] == 1 and info["bn"] == 256
+    # up to 128 rows one SM per 128 x 256 tile, beyond SM pairs on 256 x 256 tiles
+    assert info["path"] == g.PATH_TCGEN05 and info["bn"] == 256
+    assert (info["kind"], info["cluster_ctas"]) == ((1, 1) if M <= 128 else (2, 2))
     y, _ = omx.mx_reference(**p.oracle_args())
     got = oracle.output_values(out, p.M, p.N, p.ldc, p.c_dtype)
     bad = np.argwhere(got != y)
