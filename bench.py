@@ -455,6 +455,11 @@ def cell(g, p, steps, warmup, stream, n_sets=None, baseline=None, mode="fused", 
             "per_call": {"median": round(med, 1), "ci95": [round(ci[0], 1), round(ci[1], 1)]}, "n": steps}
 
 
+def paired_pct(num, den):
+    """Median over rounds of 100 * (num_r / den_r - 1): rates taken side by side in each round."""
+    return statistics.median(100.0 * (a / b - 1.0) for a, b in zip(num, den))
+
+
 def interleaved_modes(g, p, modes, calls, rounds, stream, l2=L2_BYTES, name=None):
     """Time problem p in each of `modes` ("fused": its epilogue; "none": the plain GEMM; "decomposed":
     the plain GEMM, then the separate bias+GELU pass) in `rounds` alternating rounds, each mode
@@ -712,8 +717,10 @@ def extra_cells(g, stream, peaks):
     for M, calls in ((512, 200), (2048, 100), (8192, 30)):
         c = interleaved_modes(g, wl.bf16_bias_gelu(M), ("fused", "none", "decomposed"), calls, 8, stream, l2,
                               name=f"gelu_M{M}")
-        cost = round(100 * (c["none"]["tflops"] / c["fused"]["tflops"] - 1), 2)
-        gain = round(100 * (c["fused"]["tflops"] / c["decomposed"]["tflops"] - 1), 2)
+        # each round's modes ran next to each other: the median of the per-round ratios is
+        # robust to the clock drifting between rounds (seen at M = 8192 under the power cap)
+        cost = round(paired_pct(c["none"]["rounds"], c["fused"]["rounds"]), 2)
+        gain = round(paired_pct(c["fused"]["rounds"], c["decomposed"]["rounds"]), 2)
         cells[f"gelu_M{M}"] = dict(c, fused_cost_pct=cost, fusion_gain_pct=gain)
         gelu_cost[M], fusion_gain[M] = cost, gain
     # config 5: fp32 layouts (3xTF32) with ldc padding, and bf16 8192^3 NN

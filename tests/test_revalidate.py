@@ -93,3 +93,22 @@ def test_command_line_exit_status(tmp_path):
     good.write_text(json.dumps(line) + "\n")
     r = subprocess.run(args, capture_output=True, text=True)
     assert r.returncode == 1 and "value = 2MNK / ms_per_step" in json.loads(r.stdout)["failed"]
+
+
+def test_gelu_cost_from_rounds_is_the_median_of_paired_ratios():
+    """With the rounds recorded, the fused cost is the median over rounds of none_r / fused_r - 1 (each
+    round's modes ran side by side): one round with the clock in another state moves the ratio of the
+    medians but not this."""
+    line, samples = _line_and_samples()
+    fused = [1770.0, 1778.0, 1781.0, 1667.0, 1667.0, 1638.0, 1649.0, 1619.0]
+    none = [1813.0, 1822.0, 1820.0, 1700.0, 1710.0, 1669.0, 1808.0, 1653.0]
+    dec = [x / 1.6 for x in fused]
+    paired = float(np.median([100 * (a / b - 1) for a, b in zip(none, fused)]))
+    line["cells"]["gelu_M8192"] = {"fused": {"tflops": float(np.median(fused)), "rounds": fused},
+                                   "none": {"tflops": float(np.median(none)), "rounds": none},
+                                   "decomposed": {"tflops": float(np.median(dec)), "rounds": dec},
+                                   "fused_cost_pct": round(paired, 2), "fusion_gain_pct": 60.0}
+    assert paired < 3.0 < 100 * (np.median(none) / np.median(fused) - 1)
+    assert _failed(line, samples) == []
+    line["cells"]["gelu_M8192"]["fused_cost_pct"] = round(100 * (np.median(none) / np.median(fused) - 1), 2)
+    assert "gelu_M8192 fused cost %" in _failed(line, samples)
