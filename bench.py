@@ -63,8 +63,8 @@ def _args(argv=None):
     ap.add_argument("--no-cells", action="store_true", help="skip the per-configuration cells")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
     ap.add_argument("--samples", default=None,
-                    help="file for the per-call samples of every cell (default: gpurun_out/bench_samples.json "
-                         "when that folder exists)")
+                    help="file for the per-call samples of every cell (default: bench_samples.json at the "
+                         "repository root)")
     ap.add_argument("--profile", default=None, metavar="CASE",
                     help="run only CASE's workload --warmup + --steps times, untimed, for a profiler: "
                          + ", ".join(sorted(PROFILE_CASES)))
@@ -676,9 +676,7 @@ def run_ours(a):
     summary["headline_tflops"] = round(value, 1)
     summary["headline_frac"] = out["roofline"]["frac"]
     out["summary"] = summary
-    path = a.samples
-    if path is None and os.path.isdir(os.path.join(REPO, "gpurun_out")):
-        path = os.path.join(REPO, "gpurun_out", "bench_samples.json")
+    path = a.samples if a.samples is not None else os.path.join(REPO, "bench_samples.json")
     if path:
         try:
             with open(path, "w") as f:
