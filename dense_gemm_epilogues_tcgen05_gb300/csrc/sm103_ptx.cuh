@@ -52,15 +52,23 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-// True once the phase with parity `parity` has completed.
+// True once the phase with parity `parity` has completed.  A thread whose
+// phase is not complete is suspended until it completes or kWaitSuspendNs
+// pass, instead of coming straight back to poll: polling waiters (the
+// epilogue warps through a whole main loop, the MMA warp between stages)
+// took issue slots from the warps that share their sub-partition.  With the
+// hint, on GB300: fp16 4096^3 +6-8 %, fp8 4096^3 +7 %, bf16 8192^3 +6 %,
+// MXFP8 8192^3 +9 % (interleaved A/B on one box).
+constexpr uint32_t kWaitSuspendNs = 10000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar_addr), "r"(parity)
+        : "r"(bar_addr), "r"(parity), "r"(kWaitSuspendNs)
         : "memory");
     return ok != 0;
 }
