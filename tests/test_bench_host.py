@@ -176,3 +176,15 @@ def test_cells_rotate_inputs_beyond_l2():
     n = bench.sets_beyond_l2(p, l2_bytes=129 * 10 ** 6)
     assert n * bench.set_bytes(p) > 129 * 10 ** 6
     assert bench.sets_beyond_l2(wl.fp32_square(256)) >= 2
+
+
+def test_paired_cost_is_robust_to_clock_drift_between_rounds():
+    """The fused cost is the median over rounds of none_r / fused_r - 1: a round in which the plain GEMM
+    ran in a faster clock state than its fused partner moves one ratio, not the result, while the ratio
+    of the two medians moves with it."""
+    fused = [1770.0, 1778.0, 1781.0, 1667.0, 1667.0, 1638.0, 1649.0, 1619.0]
+    none = [f * 1.02 for f in fused]
+    assert abs(bench.paired_pct(none, fused) - 2.0) < 1e-9
+    none[6] = 1808.0  # one round of the plain GEMM in the fast state
+    assert abs(bench.paired_pct(none, fused) - 2.0) < 1e-9
+    assert 100 * (np.median(none) / np.median(fused) - 1) > 2.5
