@@ -44,21 +44,10 @@
 #include "epilogue.cuh"
 #include "gemm_tcgen05.cuh"
 #include "kernel_args.h"
+#include "mx_traits.cuh"
 #include "sm103_ptx.cuh"
 
 namespace gb300 {
-
-template <int ELEM> struct MxTraits;
-template <> struct MxTraits<kMxE4M3> {
-    static constexpr int kChunks = 1;          // 128 bytes of K = 128 elements = 4 blocks = one chunk
-    static constexpr int kKind = kKindMxf8f6f4;
-    static constexpr uint32_t kFmt = 0;        // E4M3
-};
-template <> struct MxTraits<kMxE2M1> {
-    static constexpr int kChunks = 2;          // 128 bytes of K = 256 elements = 8 blocks = two chunks
-    static constexpr int kKind = kKindMxf4;
-    static constexpr uint32_t kFmt = 1;        // E2M1 (kind::mxf4)
-};
 
 template <int ELEM, int STAGES_>
 struct MxConfig {

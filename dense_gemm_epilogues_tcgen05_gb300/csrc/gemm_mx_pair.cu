@@ -26,23 +26,12 @@
 #include "epilogue.cuh"
 #include "gemm_tcgen05.cuh"
 #include "kernel_args.h"
+#include "mx_traits.cuh"
 #include "sm103_ptx.cuh"
 
 namespace gb300 {
 
 namespace {
-
-template <int ELEM> struct MxpTraits;
-template <> struct MxpTraits<kMxE4M3> {
-    static constexpr int kChunks = 1;
-    static constexpr int kKind = kKindMxf8f6f4;
-    static constexpr uint32_t kFmt = 0;
-};
-template <> struct MxpTraits<kMxE2M1> {
-    static constexpr int kChunks = 2;
-    static constexpr int kKind = kKindMxf4;
-    static constexpr uint32_t kFmt = 1;
-};
 
 template <int ELEM, int STAGES_>
 struct MxpConfig {
@@ -50,7 +39,7 @@ struct MxpConfig {
     static constexpr int STAGES = STAGES_;
     static constexpr int ROW_BYTES = 128;
     static constexpr int MMAS = 4;
-    static constexpr int CHUNKS = MxpTraits<ELEM>::kChunks;
+    static constexpr int CHUNKS = MxTraits<ELEM>::kChunks;
     static constexpr int A_BYTES = BM * ROW_BYTES;
     static constexpr int B_BYTES = BNH * ROW_BYTES;
     static constexpr int SF_BLOCK = CHUNKS * 512;             // one 128-row block's chunks of a stage
@@ -69,20 +58,6 @@ struct MxpConfig {
     static_assert((2 * STAGES + 3) * 8 + 16 <= BAR_BYTES, "barriers fit their slot");
     static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
 };
-
-template <int CL>
-__device__ __forceinline__ void mxp_raise_abort_others(uint32_t abort_local, uint32_t rank) {
-#pragma unroll
-    for (uint32_t r = 0; r < static_cast<uint32_t>(CL); ++r)
-        if (r != rank) st_shared_cluster_u32(mapa_shared(abort_local, r), 1u);
-}
-
-__device__ __forceinline__ bool mxp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                         unsigned int *status, uint32_t abort_local, uint32_t rank) {
-    if (mbar_wait_bounded(bar, parity, abort_flag, status)) return true;
-    mxp_raise_abort_others<2>(abort_local, rank);
-    return false;
-}
 
 }  // namespace
 
@@ -159,7 +134,7 @@ __global__ void __launch_bounds__(MxpConfig<ELEM, STAGES>::THREADS, 1)
                 rb0 = rb0 < rbs_b ? rb0 : rbs_b - 1;
                 rb1 = rb1 < rbs_b ? rb1 : rbs_b - 1;
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mxp_wait(&empty[stage], phase ^ 1u, abort_flag, args.status, abort_local, rank)) {
+                    if (!pair_wait<2>(&empty[stage], phase ^ 1u, abort_flag, args.status, abort_local, rank)) {
                         ok = false;
                         break;
                     }
@@ -198,10 +173,10 @@ __global__ void __launch_bounds__(MxpConfig<ELEM, STAGES>::THREADS, 1)
             bool ok = true, issued = false;
             int local = 0;
             for (int tile = cluster; ok && tile < args.num_tiles; tile += nclusters, ++local) {
-                if (!mxp_wait(tempty, (local & 1) ^ 1u, abort_flag, args.status, abort_local, rank)) break;
+                if (!pair_wait<2>(tempty, (local & 1) ^ 1u, abort_flag, args.status, abort_local, rank)) break;
                 tc_fence_after();
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mxp_wait(&full[stage], phase, abort_flag, args.status, abort_local, rank)) {
+                    if (!pair_wait<2>(&full[stage], phase, abort_flag, args.status, abort_local, rank)) {
                         ok = false;
                         break;
                     }
@@ -223,10 +198,10 @@ __global__ void __launch_bounds__(MxpConfig<ELEM, STAGES>::THREADS, 1)
                         const uint32_t chunk = Cfg::CHUNKS == 1 ? 0u : static_cast<uint32_t>(ks >> 1);
                         const uint32_t sf_id = Cfg::CHUNKS == 1 ? static_cast<uint32_t>(ks)
                                                                 : static_cast<uint32_t>((ks & 1) * 2);
-                        const uint32_t idesc = mma_idesc_bs(MxpTraits<ELEM>::kFmt, 2 * BM, 2 * BNH, sf_id, sf_id);
+                        const uint32_t idesc = mma_idesc_bs(MxTraits<ELEM>::kFmt, 2 * BM, 2 * BNH, sf_id, sf_id);
                         const uint64_t ad = sw128_desc(a_addr + ks * 32, 16u, 1024u);
                         const uint64_t bd = sw128_desc(b_addr + ks * 32, 16u, 1024u);
-                        tc_mma_bs_pair<MxpTraits<ELEM>::kKind>(tmem_base, ad, bd, idesc, sfa_t + 4 * chunk,
+                        tc_mma_bs_pair<MxTraits<ELEM>::kKind>(tmem_base, ad, bd, idesc, sfa_t + 4 * chunk,
                                                                sfb_t + 8 * chunk, (kb | ks) != 0 ? 1u : 0u);
                     }
                     issued = true;
@@ -254,7 +229,7 @@ __global__ void __launch_bounds__(MxpConfig<ELEM, STAGES>::THREADS, 1)
             tile_coords(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
             const int row = tm * 2 * BM + static_cast<int>(rank) * BM + quad * 32 + lane;
             const int col_base = tn * 2 * BNH + half * 128;
-            const bool got = mxp_wait(tfull, local & 1, abort_flag, args.status, abort_local, rank);
+            const bool got = pair_wait<2>(tfull, local & 1, abort_flag, args.status, abort_local, rank);
             if (__any_sync(0xffffffffu, !got)) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;

@@ -87,24 +87,6 @@ struct PairConfig {
     static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the pair allocates all 512 TMEM columns");
 };
 
-// Raise the abort flag (at shared address `abort_local`) of every other CTA
-// of the cluster.
-template <int CL>
-__device__ __forceinline__ void raise_abort_others(uint32_t abort_local, uint32_t rank) {
-#pragma unroll
-    for (uint32_t r = 0; r < static_cast<uint32_t>(CL); ++r)
-        if (r != rank) st_shared_cluster_u32(mapa_shared(abort_local, r), 1u);
-}
-
-// A bounded wait that, when it gives up, also raises the other CTAs' abort flags.
-template <int CL>
-__device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int *status, uint32_t abort_local, uint32_t rank) {
-    if (mbar_wait_bounded(bar, parity, abort_flag, status)) return true;
-    raise_abort_others<CL>(abort_local, rank);
-    return false;
-}
-
 // ----------------------------------------------------------- schedule --
 // A cluster's work is a sequence of segments: (tile, k-blocks [kb_begin,
 // kb_end)).  First its piece [u0, u1) of the stream-K unit range (the k-blocks
