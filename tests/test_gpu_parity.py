@@ -99,8 +99,16 @@ def test_odd_ldc_uses_masked_store(cuda_lib):
 # ------------------------------------------------------------------ workloads --
 
 def test_fp32_256(cuda_lib):
+    """fp32 with a workspace runs as 3xTF32 on the tensor cores (what the launch record says);
+    gemm_query_path reports the path without one (the FFMA kernel), as the header documents."""
     r = run_gemm(cuda_lib, wl.fp32_square(256))
     assert r.path == cuda_lib.PATH_SIMT
+    info = cuda_lib.gemm_last_launch()
+    assert info["path"] == cuda_lib.PATH_TCGEN05 and info["tf32x3"] == 1
+    res = r.check()
+    assert res["pass"], res
+    r = run_gemm(cuda_lib, wl.fp32_square(256), use_workspace=False)
+    assert cuda_lib.gemm_last_launch()["path"] == cuda_lib.PATH_SIMT
     res = r.check()
     assert res["pass"], res
 
