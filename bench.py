@@ -688,7 +688,8 @@ def run_ours(a):
 
 
 def extra_cells(g, stream, peaks):
-    """One cell per workload configuration (SURVEY configs 1-5), the fused-vs-unfused
+    """One cell per workload configuration (fp16 sweep and ragged shape, fp8 with fp16 twins,
+    fp32 layouts, bf16 and block-scaled inputs), the fused-vs-unfused
     bias+GELU comparison, the cheap-baseline gate and the quantized decode cells.
     Returns (cells, summary); the summary repeats the per-dtype headline figures."""
     import torch
@@ -701,14 +702,14 @@ def extra_cells(g, stream, peaks):
         cells[name] = c
         return c
 
-    # config 1: fp32 256^3 (3xTF32 with the workspace), latency-bound
+    # fp32 256^3 (3xTF32 with the workspace), latency-bound
     run("fp32_256", wl.fp32_square(256), steps=100, warmup=10)
-    # config 2: fp16 alpha/beta sweep with ragged 1000^3; small sizes keep per-call samples and the two-mode test
+    # fp16 alpha/beta sweep with ragged 1000^3; small sizes keep per-call samples and the two-mode test
     for n, reps in ((512, 300), (1024, 300), (2048, 100), (1000, 100)):
         c = run(f"fp16_{n}", wl.fp16_alpha_beta(n), steps=reps, warmup=20)
         if n in (512, 1024):
             c.update(bimodality(SAMPLES[f"fp16_{n}"]))
-    # config 3: fused bias+GELU against the plain GEMM and against GEMM + the separate bias+GELU pass,
+    # fused bias+GELU against the plain GEMM and against GEMM + the separate bias+GELU pass,
     # the three timed in alternating rounds on the same inputs (a cost of a few percent is below the
     # drift between two cells timed one after the other)
     gelu_cost, fusion_gain = {}, {}
@@ -721,7 +722,7 @@ def extra_cells(g, stream, peaks):
         gain = round(paired_pct(c["fused"]["rounds"], c["decomposed"]["rounds"]), 2)
         cells[f"gelu_M{M}"] = dict(c, fused_cost_pct=cost, fusion_gain_pct=gain)
         gelu_cost[M], fusion_gain[M] = cost, gain
-    # config 5: fp32 layouts (3xTF32) with ldc padding, and bf16 8192^3 NN
+    # fp32 layouts (3xTF32) with ldc padding, and bf16 8192^3 NN
     for lay in ("NN", "NT", "TN", "TT"):
         run(f"fp32_4096_{lay}", wl.fp32_layout(lay, 4096), steps=20, warmup=3)
     cells["baseline_gate_fp16_4096"] = baseline_gate(g, stream, l2)
@@ -729,14 +730,14 @@ def extra_cells(g, stream, peaks):
         cells[f"q4_decode_M{M}"] = q4_decode_cell(g, stream, M, compact=True)
     for M in (64, 4096):
         cells[f"q4_prefill_M{M}"] = q4_prefill_cell(g, stream, M)
-    # block-scaled MXFP8 / MXFP4 (SURVEY NEXT-1), against 2x (fp8) and the fp4 rate
+    # block-scaled MXFP8 / MXFP4, against 2x (fp8) and the fp4 rate
     mx = {}
     for nm, elem in (("mxfp8", wl.MX_E4M3), ("mxfp4", wl.MX_E2M1)):
         c = mx_cell(g, stream, elem, 4096, name=f"{nm}_4096")
         c["frac_of_2x_bf16_peak"] = round(c["tflops"] / (2 * peaks["bf16_tflops"]), 4)
         cells[f"{nm}_4096"] = c
         mx[nm] = c["tflops"]
-    # config 4 (fp8 with its fp16 twins, bf16 output, and an fp32-output cell) and the large
+    # fp8 with its fp16 twins (bf16 output, and an fp32-output cell) and the large
     # bf16 cells last, so that the tail of the line carries them
     fp8 = {}
     for n in (2048, 4096, 8192):
