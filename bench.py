@@ -658,7 +658,7 @@ def run_ours(a):
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 burst (fp16 runs at the bf16 rate)",
                      "kernel": kernel},
-        "clocks": sampler.summary(),
+        "clocks": {**sampler.summary(), "region_ms": round(total, 3)},
         "gpu_launches": a.steps,
         "launch": launch,
         "provenance": provenance(p),
@@ -668,8 +668,14 @@ def run_ours(a):
     del sets
     torch.cuda.empty_cache()
     if not a.no_cells:
-        cells, summary = extra_cells(g, stream, peaks)
+        # The timed region above lasts a few milliseconds, less than nvidia-smi's sampling
+        # period; the cells keep the GPU busy for about ten seconds, so their samples show the
+        # clocks and throttle reasons under sustained load.
+        cells_sampler = ClockSampler(0)
+        with cells_sampler:
+            cells, summary = extra_cells(g, stream, peaks)
         out["cells"] = cells
+        out["clocks_cells"] = cells_sampler.summary()
     else:
         summary = {}
     out["cpu_baseline"] = cpu_baseline(p, a.cpu_seconds)

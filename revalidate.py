@@ -127,9 +127,11 @@ def revalidate(line: dict, samples: dict | None, peaks: dict | None) -> Checker:
     prov = line.get("provenance") or {}
     missing = [f for f in PROVENANCE_FIELDS if not prov.get(f)]
     ck.true("provenance complete", not missing, detail=missing or None)
-    reasons = (line.get("clocks") or {}).get("reasons") or []
-    bad = [r for r in reasons if any(r.startswith(x) for x in REJECTING_REASONS)]
-    ck.true("no rejecting throttle reason", not bad, detail=bad or None)
+    for key in ("clocks", "clocks_cells"):
+        if key == "clocks" or key in line:
+            reasons = (line.get(key) or {}).get("reasons") or []
+            bad = [r for r in reasons if any(r.startswith(x) for x in REJECTING_REASONS)]
+            ck.true(f"no rejecting throttle reason ({key})", not bad, detail=bad or None)
     return ck
 
 

@@ -45,6 +45,17 @@ def test_clock_record_parsing():
     assert "hw_slowdown" in bad["reasons"]
 
 
+def test_clock_sampler_around_a_region_without_nvidia_smi(monkeypatch):
+    """The sampler wraps a region whatever the host has: without nvidia-smi it says so."""
+    monkeypatch.setenv("PATH", "/nonexistent")
+    monkeypatch.setattr(bench.time, "sleep", lambda s: None)
+    sampler = bench.ClockSampler(0)
+    with sampler:
+        done = sum(range(1000))
+    assert done == 499500
+    assert sampler.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+
 def test_measured_peaks_fallback(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "REPO", str(tmp_path))
     p = bench.measured_peaks()

@@ -69,7 +69,9 @@ def test_consistent_line_passes():
      "baseline gate: win at 1.10x"),
     (lambda l, s: l["e2e"].update(h2d_bytes_per_step=0), "e2e h2d bytes per step = A + B + C"),
     (lambda l, s: l["provenance"].pop("recipe_hash"), "provenance complete"),
-    (lambda l, s: l["clocks"]["reasons"].append("hw_slowdown"), "no rejecting throttle reason"),
+    (lambda l, s: l["clocks"]["reasons"].append("hw_slowdown"), "no rejecting throttle reason (clocks)"),
+    (lambda l, s: l.update(clocks_cells={"reasons": ["sw_thermal_slowdown"]}),
+     "no rejecting throttle reason (clocks_cells)"),
 ])
 def test_each_disagreement_is_flagged(mutate, flag):
     line, samples = _line_and_samples()
