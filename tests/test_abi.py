@@ -310,3 +310,17 @@ def test_q4_ws_workspace_size_and_fallback_without_gpu(g):
             g.gemm_q4_ws(16, 64, K, kw.get("xd", g.F16), X, kw.get("ldx", 128), W, SB, C, 64, g.F16, 1.0, 0.0,
                          None, g.EPI_NONE, workspace=None, workspace_bytes=0, stream=0)
         assert e.value.status == status, kw
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """The binding has no fallback: imported where libgemm_gb300.so is absent, it raises ImportError."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "dense_gemm_epilogues_tcgen05_gb300"
+    pkg.mkdir()
+    shutil.copy(os.path.join(REPO, "dense_gemm_epilogues_tcgen05_gb300", "__init__.py"), pkg / "__init__.py")
+    r = subprocess.run([sys.executable, "-c", "import dense_gemm_epilogues_tcgen05_gb300"], cwd=tmp_path,
+                       capture_output=True, text=True, env={**os.environ, "PYTHONPATH": str(tmp_path)})
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libgemm_gb300.so is missing" in r.stderr
