@@ -1,5 +1,6 @@
 // Test aid: the host-side planner of the C ABI -- the tile cost model, the
-// cluster shape, the stream-K schedule and its cut table -- exposed with C
+// cluster shape, the stream-K schedule and its cut table, an operand's byte
+// extent and whether a tensor map can read it -- exposed with C
 // linkage so that CPU tests can call it with a GPU's resource counts (SMs,
 // resident clusters) given as numbers.  The library's host source is compiled
 // into this test library as it stands; the kernel launchers it refers to come
@@ -40,5 +41,17 @@ int plan_stream_k_feasible(long long units, int num_kb, int clusters, int dp_til
 }
 
 int plan_max_sk_clusters() { return kMaxSkClusters; }
+
+// Bytes from an operand's first element to one past its last (the range checked against its allocation).
+unsigned long long plan_span_bytes(int64_t rows, int64_t cols, int64_t s_rows, int64_t s_cols, int es) {
+    return span_bytes(rows, cols, s_rows, s_cols, es);
+}
+
+// How an (mn x k) operand at address `base` is read: 0 no tensor map (CUDA-core path), 1 by a
+// K-contiguous map, 2 by an MN-contiguous map.  The address is only tested for alignment.
+int plan_operand_kind(unsigned long long base, int64_t mn, int64_t k, int64_t s_mn, int64_t s_k, int es) {
+    const Operand o = plan_operand(reinterpret_cast<const void *>(base), mn, k, s_mn, s_k, es);
+    return !o.tma ? 0 : (o.mn_major ? 2 : 1);
+}
 
 }  // extern "C"

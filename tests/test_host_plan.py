@@ -1,4 +1,5 @@
-"""The host planner on the CPU: tile cost model, cluster shape, stream-K schedule and cut table.
+"""The host planner on the CPU: tile cost model, cluster shape, stream-K schedule and cut table,
+operand extents and tensor-map eligibility.
 
 ``host_plan_harness.cu`` compiles the library's host source into a test library
 (linked against libgemm_gb300.so for the kernel launchers, which no test here
@@ -45,6 +46,9 @@ def plan(tmp_path_factory):
     lib.plan_choose_schedule.argtypes = [i64, i32, i32, i32, i32, i32, i32p, llp, u32p, i32p]
     lib.plan_stream_k_cuts.argtypes = [ll, i32, i32, i32, ll, u32p]
     lib.plan_stream_k_feasible.argtypes = [ll, i32, i32, i32, ll, ll, u32p]
+    lib.plan_span_bytes.restype = ctypes.c_ulonglong
+    lib.plan_span_bytes.argtypes = [i64, i64, i64, i64, i32]
+    lib.plan_operand_kind.argtypes = [ctypes.c_ulonglong, i64, i64, i64, i64, i32]
     return lib
 
 
@@ -196,3 +200,44 @@ def test_tile_choice(plan):
     # with only 8 resident pairs, 1024^3: pair 256 needs 2 waves (512), pair 128 4 (768),
     # one-SM 256 one wave (384), one-SM 128 one wave (256)
     assert tile(plan, 1024, 1024, pairs=8) == (1, 128)
+
+
+def test_span_bytes_is_the_last_element_plus_one(plan):
+    """The byte extent checked against an operand's allocation, against brute force over every
+    element's offset (row-major, column-major, padded and broadcast strides)."""
+    rng = random.Random(11)
+    for _ in range(300):
+        rows, cols = rng.randint(0, 9), rng.randint(0, 9)
+        s_rows, s_cols = rng.choice([0, 1, cols, cols + 3, 17]), rng.choice([0, 1, rows, rows + 5, 13])
+        es = rng.choice([1, 2, 4])
+        want = 0 if rows == 0 or cols == 0 else \
+            (max(i * s_rows + j * s_cols for i in range(rows) for j in range(cols)) + 1) * es
+        assert plan.plan_span_bytes(rows, cols, s_rows, s_cols, es) == want, (rows, cols, s_rows, s_cols, es)
+    assert plan.plan_span_bytes(4096, 4096, 4096, 1, 2) == 4096 * 4096 * 2
+
+
+def test_operand_read_by_tensor_map_when_the_rules_allow(plan):
+    """A tensor map needs a 16-byte aligned base, a contiguous inner dimension and an outer pitch
+    that is a multiple of 16 bytes (below 2^40); K-contiguous is taken first, then MN-contiguous,
+    else the operand goes to the CUDA-core path."""
+    base = 1 << 20
+    # fp16 A, M x K = 64 x 1000: row-major (K-contiguous, pitch 2000 B), its transpose, a padded pitch
+    assert plan.plan_operand_kind(base, 64, 1000, 1000, 1, 2) == 1
+    assert plan.plan_operand_kind(base, 64, 1000, 1, 64, 2) == 2
+    assert plan.plan_operand_kind(base, 64, 1000, 1008, 1, 2) == 1
+    # pitches that are not a multiple of 16 bytes: 1001 fp16, 1002 e4m3, 66 fp16 (MN-contiguous)
+    assert plan.plan_operand_kind(base, 64, 1001, 1001, 1, 2) == 0
+    assert plan.plan_operand_kind(base, 64, 1002, 1002, 1, 1) == 0
+    assert plan.plan_operand_kind(base, 64, 1000, 1, 66, 2) == 0
+    # e4m3 needs a 16-element pitch, fp16 an 8-element one
+    assert plan.plan_operand_kind(base, 64, 1008, 1008, 1, 1) == 1
+    assert plan.plan_operand_kind(base, 64, 1000, 1000, 1, 1) == 0
+    # misaligned base (8 bytes off), or neither dimension contiguous
+    assert plan.plan_operand_kind(base + 8, 64, 1000, 1000, 1, 2) == 0
+    assert plan.plan_operand_kind(base, 64, 1000, 2000, 2, 2) == 0
+    # one row: the outer pitch is never used, so any pitch is fine
+    assert plan.plan_operand_kind(base, 1, 1000, 7, 1, 2) == 1
+    # a pitch of 2^40 bytes is beyond a tensor map's range
+    assert plan.plan_operand_kind(base, 64, 8, 1 << 39, 1, 2) == 0
+    # when both would do (a square block with both strides legal) the K-contiguous map wins
+    assert plan.plan_operand_kind(base, 1, 1, 8, 1, 2) == 1
