@@ -9,6 +9,10 @@ trusting the harness that wrote it.  This script is that check for
   the measured peak in MEASURED_PEAKS.json, pct of the nominal peak;
 * every per-call summary it has samples for: median and the 95 % bootstrap CI
   of the median (10^4 resamples, seed 0, percentile method);
+* every cell's rate from its time per call (flops / ms), its fraction of
+  twice the bf16 peak where it states one, and each quantized decode cell's
+  roofline fraction (algorithmic bytes / time / measured HBM bandwidth) and
+  per-call median;
 * the derived ratios and gates: fp8 over its fp16 twin (>= 1.5 counts as
   accelerated), fused bias+GELU cost against none and gain against the
   decomposed pass, the cheap-baseline gate (tcgen05 >= 1.10 x the strongest
@@ -26,6 +30,7 @@ import argparse
 import json
 import math
 import os
+import re
 import sys
 
 import numpy as np
@@ -41,6 +46,26 @@ def median_and_ci(samples, reps=10000, seed=0):
     rng = np.random.default_rng(seed)
     meds = np.median(x[rng.integers(0, x.size, size=(reps, x.size))], axis=1)
     return float(np.median(x)), (float(np.percentile(meds, 2.5)), float(np.percentile(meds, 97.5)))
+
+
+def cell_flops(name: str):
+    """2 M N K of a cell, from its name (None for a cell whose name fixes no GEMM shape)."""
+    m = re.fullmatch(r"(?:fp32|fp16|fp8|fp16_twin|bf16|mxfp8|mxfp4)_(\d+)(?:_(?:NN|NT|TN|TT|nn|f32out))?", name)
+    if m:
+        return 2.0 * int(m.group(1)) ** 3
+    m = re.fullmatch(r"gelu_M(\d+)", name)
+    if m:
+        return 2.0 * int(m.group(1)) * 4096 * 4096
+    if name == "baseline_gate_fp16_4096":
+        return 2.0 * 4096 ** 3
+    return None
+
+
+def _timed_records(name, cell):
+    """(suffix, record) of every timed mode of a cell: the cell itself, or its modes."""
+    if "tflops" in cell and "ms" in cell:
+        return [("", cell)]
+    return [(f".{k}", v) for k, v in cell.items() if isinstance(v, dict) and "tflops" in v and "ms" in v]
 
 
 class Checker:
@@ -90,6 +115,28 @@ def revalidate(line: dict, samples: dict | None, peaks: dict | None) -> Checker:
                 ck.close(f"{name} per-call median", cell["per_call"]["median"], med)
                 ck.close(f"{name} per-call CI", cell["per_call"]["ci95"][1], ci[1])
     cells = line.get("cells") or {}
+    # each cell's rate from its own time per call: tflops = flops / ms (both rounded as recorded)
+    for name, cell in cells.items():
+        for mode, rec in _timed_records(name, cell):
+            flops = cell_flops(name)
+            if flops and rec.get("ms"):
+                want = flops / (rec["ms"] * 1e-3) / 1e12
+                ck.close(f"{name}{mode} tflops = flops / ms", rec["tflops"], want,
+                         rel=0.5e-4 / rec["ms"] + 1e-4, abs_=0.06)
+        if peaks is not None and "frac_of_2x_bf16_peak" in cell:
+            ck.close(f"{name} frac of 2x bf16 peak", cell["frac_of_2x_bf16_peak"],
+                     cell["tflops"] / (2 * peaks["bf16_tflops"]), rel=0, abs_=2e-4)
+        m = re.fullmatch(r"q4_decode_M(\d+)", name)
+        if m and cell.get("us") and peaks is not None and "hbm_gbs" in peaks:
+            Mq = int(m.group(1))
+            Nq, Kq = (int(v) for v in cell["shape"].split("x")[1:])
+            nbytes = Nq * Kq // 2 + (Nq * Kq // 64) * 4 + 2 * Mq * Kq + 2 * Mq * Nq
+            ck.close(f"{name} frac = bytes / us / HBM peak", cell["frac"],
+                     nbytes / (cell["us"] * 1e-6) / 1e9 / peaks["hbm_gbs"], rel=0, abs_=2e-4)
+            if samples is not None and name in samples.get("samples", samples):
+                med, ci = median_and_ci(samples.get("samples", samples)[name])
+                ck.close(f"{name} per-call median GB/s", cell["gbs"], med)
+                ck.close(f"{name} per-call CI", cell["ci95"][1], ci[1])
     # fp8 over the fp16 twin, and the accelerated gate
     for n in (2048, 4096, 8192):
         c8, c16 = cells.get(f"fp8_{n}"), cells.get(f"fp16_twin_{n}")

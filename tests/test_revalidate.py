@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 REPO = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+Q4_BYTES = 16384 * 16384 // 2 + (16384 * 16384 // 64) * 4 + 2 * 16384 + 2 * 16384
 sys.path.insert(0, REPO)
 import revalidate as rv  # noqa: E402
 
@@ -18,6 +19,8 @@ def _line_and_samples():
     rng = np.random.default_rng(5)
     head = list(np.round(1490 + rng.normal(0, 5, 30), 2))
     cell = list(np.round(2680 + rng.normal(0, 8, 30), 2))
+    q4 = list(np.round(3207 + rng.normal(0, 3, 50), 1))
+    qm, qci = rv.median_and_ci(q4)
     hm, hci = rv.median_and_ci(head)
     cm, cci = rv.median_and_ci(cell)
     M = N = K = 4096
@@ -34,8 +37,11 @@ def _line_and_samples():
         "clocks": {"reasons": ["sw_power_cap"]},
         "cells": {
             "fp8_4096": {"tflops": 2892.8, "over_fp16": round(2892.8 / 1605.2, 3),
+                         "frac_of_2x_bf16_peak": round(2892.8 / (2 * 1954.3), 4),
                          "per_call": {"median": round(cm, 1), "ci95": [round(cci[0], 1), round(cci[1], 1)]}},
-            "fp16_twin_4096": {"tflops": 1605.2},
+            "fp16_twin_4096": {"tflops": 1605.2, "ms": round(2.0 * 4096 ** 3 / 1605.2e12 * 1e3, 4)},
+            "q4_decode_M1": {"shape": "1x16384x16384", "gbs": round(qm, 1), "ci95": [round(qci[0], 1), round(qci[1], 1)],
+                             "us": 47.64, "frac": round(Q4_BYTES / 47.64e-6 / 1e9 / 6655.6, 4), "n": 50},
             "gelu_M2048": {"fused": {"tflops": 1480.0}, "none": {"tflops": 1534.6}, "decomposed": {"tflops": 980.0},
                            "fused_cost_pct": round(100 * (1534.6 / 1480.0 - 1), 2),
                            "fusion_gain_pct": round(100 * (1480.0 / 980.0 - 1), 2)},
@@ -44,11 +50,11 @@ def _line_and_samples():
                                         "over_strongest": round(1532.1 / 290.0, 3), "win": True},
         },
     }
-    samples = {"unit": "TFLOP/s per call", "samples": {"headline": head, "fp8_4096": cell}}
+    samples = {"unit": "TFLOP/s per call", "samples": {"headline": head, "fp8_4096": cell, "q4_decode_M1": q4}}
     return line, samples
 
 
-def _failed(line, samples, peaks={"bf16_tflops": 1954.3}):
+def _failed(line, samples, peaks={"bf16_tflops": 1954.3, "hbm_gbs": 6655.6}):
     return [c["check"] for c in rv.revalidate(line, samples, peaks).checks if not c["ok"]]
 
 
@@ -69,6 +75,10 @@ def test_consistent_line_passes():
      "baseline gate: win at 1.10x"),
     (lambda l, s: l["e2e"].update(h2d_bytes_per_step=0), "e2e h2d bytes per step = A + B + C"),
     (lambda l, s: l["provenance"].pop("recipe_hash"), "provenance complete"),
+    (lambda l, s: l["cells"]["fp16_twin_4096"].update(ms=0.09), "fp16_twin_4096 tflops = flops / ms"),
+    (lambda l, s: l["cells"]["fp8_4096"].update(frac_of_2x_bf16_peak=0.8), "fp8_4096 frac of 2x bf16 peak"),
+    (lambda l, s: l["cells"]["q4_decode_M1"].update(frac=0.6), "q4_decode_M1 frac = bytes / us / HBM peak"),
+    (lambda l, s: l["cells"]["q4_decode_M1"].update(gbs=3300.0), "q4_decode_M1 per-call median GB/s"),
     (lambda l, s: l["clocks"]["reasons"].append("hw_slowdown"), "no rejecting throttle reason (clocks)"),
     (lambda l, s: l.update(clocks_cells={"reasons": ["sw_thermal_slowdown"]}),
      "no rejecting throttle reason (clocks_cells)"),
